@@ -1,0 +1,338 @@
+"""Pins of the fp64 oracle against what the pages and mathematics fix (CPU only).
+
+Each check is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a transposed operand) fails at least one of them; the
+planted-mistake tests at the end demonstrate that for several such slips.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import attention as A
+from oracle import online_softmax as OS
+from exact_tiled_attention_07_gb300.inputs import attention_flops
+
+RNG = np.random.default_rng(1234)
+
+
+def _rand(*shape, rng=RNG):
+    return rng.standard_normal(shape)
+
+
+# --------------------------------------------------------------------------
+# values printed on the pages
+# --------------------------------------------------------------------------
+
+
+def test_online_softmax_worked_example(golden):
+    kv, rows = golden("online_softmax_worked_example.txt")
+    x = kv["x"]
+    trace = oracle.online_softmax_trace(x, int(kv["block"][0]))
+    assert len(trace) == len(rows)
+    for (n_read, m, ell), (g_read, g_m, g_ell) in zip(trace, rows):
+        assert n_read == int(g_read)
+        assert m == g_m
+        assert abs(ell - g_ell) < 5e-7  # the page prints six decimals
+    # the final denominator is the whole-row one, exactly up to rounding
+    assert abs(trace[-1][2] - sum(math.exp(t - 6.0) for t in x)) < 1e-15
+
+
+def test_merge_exercise3(golden):
+    kv, _ = golden("merge_exercise3.txt")
+    (_, m1, l1), = oracle.online_softmax_trace(kv["x1"], 2)
+    (_, m2, l2), = oracle.online_softmax_trace(kv["x2"], 2)
+    assert (m1, round(l1, 6)) == tuple(kv["state1"])
+    assert (m2, round(l2, 6)) == tuple(kv["state2"])
+    m, ell = oracle.merge_states(m1, l1, m2, l2)
+    assert (m, round(ell, 6)) == tuple(kv["merged"])
+    # merged state equals the state of the concatenated stream
+    (_, md, ld), = oracle.online_softmax_trace(kv["x1"] + kv["x2"], 4)
+    assert m == md and abs(ell - ld) < 1e-15
+
+
+def test_merge_outputs_equal_whole_row():
+    # merging two normalised partial outputs reproduces softmax-weighted sums of the whole row
+    s = _rand(10) * 3
+    v = _rand(10, 4)
+    def part(lo, hi):
+        m = s[lo:hi].max()
+        e = np.exp(s[lo:hi] - m)
+        return m, e.sum(), (e @ v[lo:hi]) / e.sum()
+    m1, l1, o1 = part(0, 6)
+    m2, l2, o2 = part(6, 10)
+    _, _, o = oracle.merge_states(m1, l1, m2, l2, o1, o2)
+    p = np.exp(s - s.max()); p /= p.sum()
+    np.testing.assert_allclose(o, p @ v, atol=1e-15, rtol=0)
+
+
+def test_flop_convention_exercise1(golden):
+    kv, _ = golden("exercise1_qkt_accounting.txt")
+    n, d, e = int(kv["N"][0]), int(kv["d"][0]), int(kv["bytes_per_element"][0])
+    # the forward counts two N×N×d contractions; one of them is Exercise 1's Q·Kᵀ
+    assert attention_flops(1, 1, n, d, False, "fwd") / 2 == kv["flops"][0]
+    qkt_bytes = e * (n * d + d * n + n * n)
+    assert qkt_bytes == kv["bytes"][0]
+    assert round(kv["flops"][0] / qkt_bytes, 1) == kv["intensity"][0]
+    assert attention_flops(2, 3, 128, 64, True, "bwd") == 2.5 * 4 * 6 * 128 * 128 * 64 / 2
+
+
+def test_causal_tile_count(golden):
+    kv, _ = golden("causal_tile_count.txt")
+    t = int(kv["blocks_per_side"][0])
+    br = 16
+    assert oracle.causal_tiles_visited(t * br, br, br) == kv["visited"][0]
+    assert round(kv["visited"][0] / kv["total"][0], 3) == kv["fraction"][0]
+    # the tiled forward visits exactly that many block pairs
+    cnt = []
+    q, k, v = _rand(t * br, 4), _rand(t * br, 4), _rand(t * br, 4)
+    OS.tiled_fwd_fa2_order(q, k, v, 0.5, True, br, br, count=cnt)
+    assert cnt == [136]
+    for tt in (1, 2, 7, 32):
+        assert oracle.causal_tiles_visited(tt * 128, 128, 128) == tt * (tt + 1) // 2
+
+
+# --------------------------------------------------------------------------
+# the tiled method equals the definition to fp64 rounding
+# --------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("br,bc", [(16, 16), (32, 64), (64, 32), (256, 256), (48, 80)])
+def test_tiled_forward_equals_standard(causal, br, bc):
+    n, d = 256, 32
+    rng = np.random.default_rng(7)
+    q, k, v = (rng.standard_normal((1, 1, n, d)) for _ in range(3))
+    tau = 1 / math.sqrt(d)
+    o_ref, l_ref = oracle.attn_fwd64(q, k, v, tau, causal)
+    for fn in (OS.tiled_fwd_fa2_order, OS.tiled_fwd_fa1_order):
+        o, lse = fn(q[0, 0], k[0, 0], v[0, 0], tau, causal, br, bc)
+        assert np.abs(o - o_ref[0, 0]).max() < 5e-15
+        assert np.abs(lse - l_ref[0, 0]).max() < 5e-15
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_recompute_backward_equals_definition(causal):
+    n, d = 160, 16
+    rng = np.random.default_rng(9)
+    q, k, v, do = (rng.standard_normal((1, 1, n, d)) for _ in range(4))
+    tau = 0.3
+    o, lse = oracle.attn_fwd64(q, k, v, tau, causal)
+    dq, dk, dv, _ = oracle.attn_bwd64(q, k, v, do, tau, causal)
+    for br, bc in [(32, 32), (64, 48), (160, 160)]:
+        tq, tk, tv = OS.tiled_bwd_recompute(q[0, 0], k[0, 0], v[0, 0], o[0, 0], do[0, 0], lse[0, 0], tau, causal, br, bc)
+        for a, b in ((tq, dq), (tk, dk), (tv, dv)):
+            assert np.abs(a - b[0, 0]).max() < 1e-13 * max(1.0, np.abs(b).max())
+
+
+# --------------------------------------------------------------------------
+# mathematics: invariants, closed forms, finite differences
+# --------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probability_rows(causal):
+    q, k = _rand(33, 8), _rand(33, 8)
+    _, p, _, _ = A.probabilities64(q, k, 0.7, causal, np.arange(33))
+    assert (p >= 0).all()
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-15, rtol=0)
+    if causal:
+        assert (p[np.triu_indices(33, 1)] == 0).all()
+
+
+def test_single_key_closed_form():
+    q, k, v = _rand(2, 3, 1, 5), _rand(2, 3, 1, 5), _rand(2, 3, 1, 5)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd64(q, k, v, 0.25, causal)
+        np.testing.assert_array_equal(o, v)
+        np.testing.assert_allclose(lse, 0.25 * (q * k).sum(-1), atol=1e-15, rtol=0)
+
+
+def test_equal_keys_give_means():
+    n, d = 12, 4
+    q = _rand(1, 1, n, d)
+    k = np.broadcast_to(_rand(1, 1, 1, d), (1, 1, n, d)).copy()
+    v = _rand(1, 1, n, d)
+    o, lse = oracle.attn_fwd64(q, k, v, 1.0, False)
+    np.testing.assert_allclose(o[0, 0], np.broadcast_to(v[0, 0].mean(0), (n, d)), atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], (q[0, 0] @ k[0, 0, 0]) + math.log(n), atol=1e-14)
+    o, lse = oracle.attn_fwd64(q, k, v, 1.0, True)
+    prefix = np.cumsum(v[0, 0], axis=0) / np.arange(1, n + 1)[:, None]
+    np.testing.assert_allclose(o[0, 0], prefix, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], (q[0, 0] @ k[0, 0, 0]) + np.log(np.arange(1, n + 1)), atol=1e-14)
+
+
+def test_constant_values_pass_through():
+    q, k = _rand(1, 2, 9, 3), _rand(1, 2, 9, 3)
+    v = np.ones((1, 2, 9, 3))
+    for causal in (False, True):
+        o, _ = oracle.attn_fwd64(q, k, v, 1.3, causal)
+        np.testing.assert_allclose(o, 1.0, atol=1e-15, rtol=0)
+
+
+def test_per_query_shift_invariance():
+    # an extra coordinate with q' = c_i / τ and k' = 1 adds c_i to every score of row i
+    n, d, tau = 10, 4, 0.5
+    q, k, v = _rand(1, 1, n, d), _rand(1, 1, n, d), _rand(1, 1, n, d)
+    c = _rand(n) * 5
+    q2 = np.concatenate([q, (c / tau)[None, None, :, None]], axis=-1)
+    k2 = np.concatenate([k, np.ones((1, 1, n, 1))], axis=-1)
+    for causal in (False, True):
+        o1, l1 = oracle.attn_fwd64(q, k, v, tau, causal)
+        o2, l2 = oracle.attn_fwd64(q2, k2, v, tau, causal)
+        np.testing.assert_allclose(o2, o1, atol=1e-14)
+        np.testing.assert_allclose(l2 - l1, c[None, None, :], atol=1e-13)
+
+
+def test_key_offset_moves_probability_mass():
+    # a per-key offset c_j (the long-sequence workload's recipe) multiplies column j of e^S by e^(c_j)
+    n, d, tau = 8, 3, 0.5
+    q, k, v = _rand(1, 1, n, d), _rand(1, 1, n, d), _rand(1, 1, n, d)
+    c = _rand(n)
+    q2 = np.concatenate([np.ones((1, 1, n, 1)), q], axis=-1)
+    k2 = np.concatenate([(c / tau)[None, None, :, None], k], axis=-1)
+    _, p1, _, _ = A.probabilities64(q[0, 0], k[0, 0], tau, False, np.arange(n))
+    _, p2, _, _ = A.probabilities64(q2[0, 0], k2[0, 0], tau, False, np.arange(n))
+    w = p1 * np.exp(c)[None, :]
+    np.testing.assert_allclose(p2, w / w.sum(1, keepdims=True), atol=1e-15)
+
+
+def _fd_grads(q, k, v, do, tau, causal, h=1e-5, fwd=None):
+    fwd = fwd or oracle.attn_fwd64
+
+    def f(qq, kk, vv):
+        return float((fwd(qq, kk, vv, tau, causal)[0] * do).sum())
+
+    out = []
+    for which in range(3):
+        args = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(args[which])
+        it = np.nditer(args[which], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            a_p = [x.copy() for x in args]
+            a_m = [x.copy() for x in args]
+            a_p[which][idx] += h
+            a_m[which][idx] -= h
+            g[idx] = (f(*a_p) - f(*a_m)) / (2 * h)
+        out.append(g)
+    return out
+
+
+@pytest.mark.parametrize("n,d,causal", [(1, 3, False), (5, 4, False), (7, 3, True), (9, 2, True), (6, 5, False)])
+def test_backward_matches_finite_differences(n, d, causal):
+    rng = np.random.default_rng(n * 31 + d)
+    q, k, v, do = (rng.standard_normal((1, 2, n, d)) for _ in range(4))
+    tau = 0.8
+    dq, dk, dv, _ = oracle.attn_bwd64(q, k, v, do, tau, causal)
+    fq, fk, fv = _fd_grads(q, k, v, do, tau, causal)
+    for a, b in ((dq, fq), (dk, fk), (dv, fv)):
+        assert np.abs(a - b).max() < 1e-8
+
+
+def test_d_identity():
+    rng = np.random.default_rng(3)
+    q, k, v, do = (rng.standard_normal((2, 2, 40, 8)) for _ in range(4))
+    for causal in (False, True):
+        o, _ = oracle.attn_fwd64(q, k, v, 0.4, causal)
+        _, _, _, dd = oracle.attn_bwd64(q, k, v, do, 0.4, causal)
+        np.testing.assert_allclose(dd, (do * o).sum(-1), atol=1e-13, rtol=0)
+
+
+# --------------------------------------------------------------------------
+# sampled paths agree with the full definition
+# --------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_paths_match_full(causal):
+    rng = np.random.default_rng(11)
+    b_, h_, n, d = 2, 2, 70, 8
+    q, k, v, do = (rng.standard_normal((b_, h_, n, d)) for _ in range(4))
+    tau = 0.35
+    o, lse = oracle.attn_fwd64(q, k, v, tau, causal)
+    dq, dk, dv, dd = oracle.attn_bwd64(q, k, v, do, tau, causal)
+    samples = np.array([[0, 0, 0], [1, 1, 69], [0, 1, 33], [1, 0, 5]])
+    so, sl = oracle.attn_fwd64_rows(q, k, v, tau, causal, samples)
+    sq, sd = oracle.attn_bwd64_query_rows(q, k, v, do, tau, causal, samples)
+    for t, (b, h, i) in enumerate(samples):
+        np.testing.assert_allclose(so[t], o[b, h, i], atol=1e-14)
+        np.testing.assert_allclose(sl[t], lse[b, h, i], atol=1e-14)
+        np.testing.assert_allclose(sq[t], dq[b, h, i], atol=1e-13)
+        np.testing.assert_allclose(sd[t], dd[b, h, i], atol=1e-13)
+    keys = np.array([0, 7, 69, 40])
+    skk, svv = oracle.attn_bwd64_key_rows(q, k, v, do, tau, causal, 1, 0, keys)
+    np.testing.assert_allclose(skk, dk[1, 0, keys], atol=1e-13)
+    np.testing.assert_allclose(svv, dv[1, 0, keys], atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each slip below is caught by one of the pins above
+# --------------------------------------------------------------------------
+
+
+def _bwd_dropped_d(q, k, v, do, tau, causal):
+    """Copy of the definition's backward with the −D term dropped from dS."""
+    q, k, v, do = (np.asarray(t, float) for t in (q, k, v, do))
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            rows = np.arange(q.shape[2])
+            _, p, _, _ = A.probabilities64(q[b, h], k[b, h], tau, causal, rows)
+            dp = do[b, h] @ v[b, h].T
+            ds = p * dp
+            dv[b, h] = p.T @ do[b, h]
+            dq[b, h] = tau * ds @ k[b, h]
+            dk[b, h] = tau * ds.T @ q[b, h]
+    return dq, dk, dv
+
+
+def test_planted_dropped_d_term_fails_fd():
+    rng = np.random.default_rng(5)
+    q, k, v, do = (rng.standard_normal((1, 1, 5, 3)) for _ in range(4))
+    bq, bk, _ = _bwd_dropped_d(q, k, v, do, 0.8, False)
+    fq, fk, _ = _fd_grads(q, k, v, do, 0.8, False)
+    assert np.abs(bq - fq).max() > 1e-3 and np.abs(bk - fk).max() > 1e-3
+
+
+def test_planted_transposed_probabilities_fail_prefix_means():
+    n, d = 6, 2
+    q = _rand(1, 1, n, d)
+    k = np.broadcast_to(_rand(1, 1, 1, d), (1, 1, n, d)).copy()
+    v = _rand(1, 1, n, d)
+    _, p, _, _ = A.probabilities64(q[0, 0], k[0, 0], 1.0, True, np.arange(n))
+    wrong = p.T @ v[0, 0]
+    prefix = np.cumsum(v[0, 0], axis=0) / np.arange(1, n + 1)[:, None]
+    assert np.abs(wrong - prefix).max() > 1e-3
+
+
+def test_planted_missing_rescale_fails_worked_example(golden):
+    kv, rows = golden("online_softmax_worked_example.txt")
+    x, blk = kv["x"], 3
+    m, ell, trace = -math.inf, 0.0, []
+    for s in range(0, len(x), blk):
+        b = x[s:s + blk]
+        m_new = max(m, max(b))
+        ell = ell + sum(math.exp(t - m_new) for t in b)  # slip: old ℓ not rescaled
+        m = m_new
+        trace.append(ell)
+    assert any(abs(a - r[2]) > 1e-3 for a, r in zip(trace, rows))
+
+
+def test_planted_wrong_sign_fails_probability_rows():
+    s = _rand(4, 7)
+    m = s.max(1, keepdims=True)
+    e = np.exp(m - s)  # slip: sign flipped
+    p = e / e.sum(1, keepdims=True)
+    _, p_ok, _, _ = A.probabilities64(s, np.eye(7), 1.0, False, np.arange(4))
+    assert np.abs(p - p_ok).max() > 1e-2
+
+
+def test_planted_missing_tau_in_dk_fails_fd():
+    rng = np.random.default_rng(6)
+    q, k, v, do = (rng.standard_normal((1, 1, 4, 3)) for _ in range(4))
+    _, dk, _, _ = oracle.attn_bwd64(q, k, v, do, 0.5, False)
+    _, fk, _ = _fd_grads(q, k, v, do, 0.5, False)
+    assert np.abs(dk / 0.5 - fk).max() > 1e-3
