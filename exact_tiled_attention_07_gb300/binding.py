@@ -1,0 +1,214 @@
+"""Thin Python binding of the C ABI in ``include/fa.h`` (argument marshalling only).
+
+Every entry point keeps the C name and takes torch CUDA tensors in place of
+device pointers; shapes come from the tensors.  Nothing here computes: each
+call checks the tensors, hands their pointers to ``libfa_gb300.so`` and turns a
+non-OK status into ``FAError``.  If the library was not built the first call
+raises: there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "FAError", "library_path", "load_library", "DTYPE_CODES",
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
+    "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
+    "fa_last_error_message", "attention_forward", "attention_backward", "EXPORTED_SYMBOLS",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_FILE = "libfa_gb300.so"
+
+FA_OK = 0
+DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+EXPORTED_SYMBOLS = (
+    "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
+    "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
+    "fa_last_error_message",
+)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(HERE, LIB_FILE)
+
+
+def load_library():
+    """Load ``libfa_gb300.so`` (built by ``exact_tiled_attention_07_gb300.build``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"the CUDA library {path} is not built; run __graft_entry__.build() first")
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_bwd_workspace_size.restype = sz
+        lib.fa_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, f, i, i, vp]
+        lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, i, vp]
+        lib.fa_bwd_main.argtypes = [vp] * 7 + [sz, i, i, i, i, f, i, i, vp]
+        lib.fa_bwd_dq_convert.argtypes = [vp, sz, vp, i, i, i, i, f, i, vp]
+        lib.fa_check_device_error.argtypes = [vp]
+        lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
+        lib.fa_uses_tensor_cores.argtypes = [i, i, i]
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_last_error_message.argtypes = []
+        lib.fa_last_error_message.restype = ctypes.c_char_p
+        for name in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
+                     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != FA_OK:
+        lib = load_library()
+        msg = lib.fa_last_error_message().decode() or lib.fa_status_string(status).decode()
+        raise FAError(status, msg)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _shape4(t):
+    if t.dim() != 4:
+        raise ValueError(f"expected a [B, H, N, d] tensor, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous [B, H, N, d]")
+    return tuple(int(s) for s in t.shape)
+
+
+def _dt(t):
+    try:
+        return DTYPE_CODES[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}") from None
+
+
+def _same(ref, *ts):
+    for t in ts:
+        if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device or not t.is_contiguous():
+            raise ValueError("Q, K, V, O, dO, dQ, dK, dV must share shape, dtype and device and be contiguous")
+
+
+def fa_fwd(Q, K, V, O, L, scale, causal, stream=None):
+    B, H, N, d = _shape4(Q)
+    _same(Q, K, V, O)
+    if L.dtype != torch.float32 or L.numel() != B * H * N or not L.is_contiguous():
+        raise ValueError("L must be a contiguous fp32 tensor of B*H*N elements")
+    _check(load_library().fa_fwd(_p(Q), _p(K), _p(V), _p(O), _p(L), B, H, N, d, float(scale), int(bool(causal)),
+                                 _dt(Q), _stream(stream)))
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, stream=None):
+    B, H, N, d = _shape4(Q)
+    _same(Q, K, V, O, dO, dQ, dK, dV)
+    _check(load_library().fa_bwd(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV), _p(workspace),
+                                 workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
+                                 int(bool(causal)), _dt(Q), _stream(stream)))
+
+
+def fa_bwd_preprocess(O, dO, L, workspace, stream=None):
+    B, H, N, d = _shape4(O)
+    _same(O, dO)
+    _check(load_library().fa_bwd_preprocess(_p(O), _p(dO), _p(L), _p(workspace),
+                                            workspace.numel() * workspace.element_size(), B, H, N, d, _dt(O),
+                                            _stream(stream)))
+
+
+def fa_bwd_main(Q, K, V, dO, dK, dV, workspace, scale, causal, stream=None):
+    B, H, N, d = _shape4(Q)
+    _same(Q, K, V, dO, dK, dV)
+    _check(load_library().fa_bwd_main(_p(Q), _p(K), _p(V), _p(dO), _p(dK), _p(dV), _p(workspace),
+                                      workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
+                                      int(bool(causal)), _dt(Q), _stream(stream)))
+
+
+def fa_bwd_dq_convert(workspace, dQ, scale, stream=None):
+    B, H, N, d = _shape4(dQ)
+    _check(load_library().fa_bwd_dq_convert(_p(workspace), workspace.numel() * workspace.element_size(), _p(dQ),
+                                            B, H, N, d, float(scale), _dt(dQ), _stream(stream)))
+
+
+def fa_check_device_error(stream=None):
+    _check(load_library().fa_check_device_error(_stream(stream)))
+
+
+def fa_tile_counter(stream=None, reset=False) -> int:
+    v = ctypes.c_ulonglong(0)
+    _check(load_library().fa_tile_counter(_stream(stream), ctypes.byref(v), int(bool(reset))))
+    return int(v.value)
+
+
+def fa_uses_tensor_cores(pass_: str, dtype, d: int) -> bool:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return bool(load_library().fa_uses_tensor_cores(0 if pass_ == "fwd" else 1, code, int(d)))
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_last_error_message() -> str:
+    return load_library().fa_last_error_message().decode()
+
+
+# ---------------------------------------------------------------------------
+# conveniences: allocate outputs with torch, then call the entry points above
+# ---------------------------------------------------------------------------
+
+
+def attention_forward(q, k, v, causal=False, scale=None, stream=None):
+    """O, L = fa_fwd(q, k, v); outputs allocated on q's device."""
+    B, H, N, d = _shape4(q)
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, do, lse, causal=False, scale=None, workspace=None, stream=None):
+    """dQ, dK, dV = fa_bwd(...); outputs (and workspace, unless given) allocated with torch."""
+    B, H, N, d = _shape4(q)
+    scale = d ** -0.5 if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        nbytes = fa_bwd_workspace_size(B, H, N, d)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)
+    return dq, dk, dv

@@ -1,0 +1,287 @@
+// C ABI (include/fa.h): argument validation, workspace carving, kernel selection.
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "fa.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+// Device error word written by kernels (see ptx.cuh) and the tile counter.
+__device__ unsigned long long g_err_word;
+__device__ unsigned long long g_tile_counter;
+
+thread_local char t_msg[512] = "";
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+struct DeviceSyms {
+  unsigned long long* err = nullptr;
+  unsigned long long* counter = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceSyms g_syms[kMaxDevices];
+std::mutex g_syms_mu;
+
+// Device addresses of the file-scope device symbols for the current device.
+fa_status device_syms(DeviceSyms* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_syms_mu);
+  DeviceSyms& s = g_syms[dev];
+  if (!s.err) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_err_word)) != cudaSuccess)
+      return fail(FA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
+    void* c = nullptr;
+    if ((e = cudaGetSymbolAddress(&c, g_tile_counter)) != cudaSuccess)
+      return fail(FA_ERR_CUDA, "cudaGetSymbolAddress(tile counter): %s", cudaGetErrorString(e));
+    s.counter = static_cast<unsigned long long*>(c);
+    s.err = static_cast<unsigned long long*>(p);
+  }
+  *out = s;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(fa_dtype dt) { return dt == FA_FP32 ? 4 : 2; }
+
+// Shared shape/pointer checks. Returns FA_OK and sets *empty when there is nothing to do.
+fa_status check_common(int B, int H, int N, int d, fa_dtype dt, bool* empty) {
+  *empty = false;
+  if (dt != FA_BF16 && dt != FA_FP16 && dt != FA_FP32) return fail(FA_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  if (B < 0 || H < 0 || N < 0) return fail(FA_ERR_INVALID_ARG, "negative size B=%d H=%d N=%d", B, H, N);
+  if (d < 1 || d > 256) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d outside [1, 256]", d);
+  const int64_t bh = (int64_t)B * H;
+  if (bh > INT32_MAX) return fail(FA_ERR_INVALID_ARG, "B*H=%lld too large", (long long)bh);
+  if ((int64_t)N > (int64_t)INT32_MAX - 128) return fail(FA_ERR_INVALID_ARG, "N=%d too large", N);
+  const int64_t npad = padded_rows(N);
+  if (bh > 0 && npad > 0 && (double)bh * (double)npad * (double)(d + 2) * 4.0 > 9.0e18)
+    return fail(FA_ERR_INVALID_ARG, "problem too large");
+  if (bh == 0 || N == 0) *empty = true;
+  return FA_OK;
+}
+
+fa_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
+  int i = 0;
+  for (const void* p : ptrs) {
+    if (!p) return fail(FA_ERR_INVALID_ARG, "%s: pointer %d is null", what, i);
+    if (!aligned16(p)) return fail(FA_ERR_INVALID_ARG, "%s: pointer %d is not 16-byte aligned", what, i);
+    ++i;
+  }
+  return FA_OK;
+}
+
+fa_status check_scale(float scale) {
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  return FA_OK;
+}
+
+fa_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  t_msg[0] = 0;
+  return FA_OK;
+}
+
+size_t workspace_bytes_for(int B, int H, int N, int d) {
+  const size_t bh = (size_t)B * H, npad = (size_t)padded_rows(N);
+  return bh * npad * 4 * (2 + (size_t)d);
+}
+
+fa_status carve(BwdArgs* a, void* ws, size_t ws_bytes, int B, int H, int N, int d) {
+  const size_t need = workspace_bytes_for(B, H, N, d);
+  if (ws_bytes < need) return fail(FA_ERR_INVALID_ARG, "workspace of %zu bytes < %zu required", ws_bytes, need);
+  const size_t rows = (size_t)B * H * padded_rows(N);
+  float* base = static_cast<float*>(ws);
+  a->delta = base;
+  a->lse2 = base + rows;
+  a->dq_acc = base + 2 * rows;
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream) {
+  bool empty;
+  fa_status st = check_common(B, H, N, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if ((st = check_ptrs({Q, K, V, O, L}, "fa_fwd")) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  DeviceSyms syms;
+  if ((st = device_syms(&syms)) != FA_OK) return st;
+  FwdArgs a{Q, K, V, O, L, B * H, N, d, scale, causal ? 1 : 0, (int)dtype, syms.err, syms.counter,
+            static_cast<cudaStream_t>(stream)};
+  if (fwd_tc_supported(a.dtype, d)) return launched(launch_fwd_tc(a), "fa_fwd (tensor-core kernel)");
+  return launched(launch_fwd_simt(a), "fa_fwd (CUDA-core kernel)");
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  bool empty;
+  if (check_common(B, H, N, d, FA_FP32, &empty) != FA_OK) return 0;
+  return workspace_bytes_for(B, H, N, d);
+}
+
+fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* L, void* workspace, size_t workspace_bytes,
+                            int B, int H, int N, int d, fa_dtype dtype, void* stream) {
+  bool empty;
+  fa_status st = check_common(B, H, N, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if ((st = check_ptrs({O, dO, L, workspace}, "fa_bwd_preprocess")) != FA_OK) return st;
+  BwdArgs a{};
+  if ((st = carve(&a, workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
+  a.o = O;
+  a.dout = dO;
+  a.lse = L;
+  a.bh = B * H;
+  a.n = N;
+  a.d = d;
+  a.dtype = (int)dtype;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launched(launch_bwd_pre(a), "fa_bwd_preprocess");
+}
+
+fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
+                      void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                      fa_dtype dtype, void* stream) {
+  bool empty;
+  fa_status st = check_common(B, H, N, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if ((st = check_ptrs({Q, K, V, dO, dK, dV, workspace}, "fa_bwd_main")) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  BwdArgs a{};
+  if ((st = carve(&a, workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
+  DeviceSyms syms;
+  if ((st = device_syms(&syms)) != FA_OK) return st;
+  a.q = Q;
+  a.k = K;
+  a.v = V;
+  a.dout = dO;
+  a.dk = dK;
+  a.dv = dV;
+  a.bh = B * H;
+  a.n = N;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.dtype = (int)dtype;
+  a.err = syms.err;
+  a.counter = syms.counter;
+  a.stream = static_cast<cudaStream_t>(stream);
+  if (bwd_tc_supported(a.dtype, d)) return launched(launch_bwd_tc(a), "fa_bwd_main (tensor-core kernel)");
+  return launched(launch_bwd_simt(a), "fa_bwd_main (CUDA-core kernels)");
+}
+
+fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void* dQ, int B, int H, int N, int d,
+                            float scale, fa_dtype dtype, void* stream) {
+  bool empty;
+  fa_status st = check_common(B, H, N, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if ((st = check_ptrs({workspace, dQ}, "fa_bwd_dq_convert")) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  BwdArgs a{};
+  if ((st = carve(&a, const_cast<void*>(workspace), workspace_bytes, B, H, N, d)) != FA_OK) return st;
+  a.dq = dQ;
+  a.bh = B * H;
+  a.n = N;
+  a.d = d;
+  a.scale = scale;
+  a.dtype = (int)dtype;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launched(launch_dq_convert(a), "fa_bwd_dq_convert");
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
+                 void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream) {
+  bool empty;
+  fa_status st = check_common(B, H, N, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if ((st = check_ptrs({Q, K, V, O, dO, L, dQ, dK, dV, workspace}, "fa_bwd")) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if ((st = fa_bwd_preprocess(O, dO, L, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK) return st;
+  if ((st = fa_bwd_main(Q, K, V, dO, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream)) !=
+      FA_OK)
+    return st;
+  return fa_bwd_dq_convert(workspace, workspace_bytes, dQ, B, H, N, d, scale, dtype, stream);
+}
+
+fa_status fa_check_device_error(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  DeviceSyms syms;
+  fa_status st = device_syms(&syms);
+  if (st != FA_OK) return st;
+  unsigned long long w = 0;
+  if ((e = cudaMemcpy(&w, syms.err, sizeof(w), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail(FA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+  if (w == 0) {
+    t_msg[0] = 0;
+    return FA_OK;
+  }
+  const unsigned long long zero = 0;
+  cudaMemcpy(syms.err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  const unsigned code = (unsigned)(w >> 56), site = (unsigned)((w >> 40) & 0xFFFF);
+  const unsigned long long block = w & 0xFFFFFFFFFFull;
+  if (code == DERR_TIMEOUT)
+    return fail(FA_ERR_TIMEOUT, "a bounded wait expired (site %u, block %llu)", site, block);
+  return fail(FA_ERR_DEVICE, "device check %u failed (site %u, block %llu)", code, site, block);
+}
+
+fa_status fa_tile_counter(void* stream, unsigned long long* value, int reset) {
+  if (!value) return fail(FA_ERR_INVALID_ARG, "fa_tile_counter: null output");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  DeviceSyms syms;
+  fa_status st = device_syms(&syms);
+  if (st != FA_OK) return st;
+  if ((e = cudaMemcpy(value, syms.counter, sizeof(*value), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail(FA_ERR_CUDA, "reading the tile counter: %s", cudaGetErrorString(e));
+  if (reset) {
+    const unsigned long long zero = 0;
+    if ((e = cudaMemcpy(syms.counter, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return fail(FA_ERR_CUDA, "resetting the tile counter: %s", cudaGetErrorString(e));
+  }
+  return FA_OK;
+}
+
+int fa_uses_tensor_cores(int pass, fa_dtype dtype, int d) {
+  return pass == 0 ? (int)fwd_tc_supported((int)dtype, d) : (int)bwd_tc_supported((int)dtype, d);
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported dtype or head dimension";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+    case FA_ERR_DEVICE: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+const char* fa_last_error_message(void) { return t_msg; }
+
+}  // extern "C"

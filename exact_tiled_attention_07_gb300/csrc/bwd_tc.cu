@@ -1,0 +1,413 @@
+// Tensor-core backward for bf16/fp16, head dims 64/128 (sm_103a: TMA, tcgen05, TMEM).
+//
+// Recomputing backward ("Lecture 8 · GPU Performance & FlashAttention" §5.4; "FlashAttention
+// and GPU memory" §09): nothing N x N was stored, so every (key tile j, query tile i) pair
+// recomputes its scores from Q, K and the saved row statistic L:
+//     S^T = K_j Q_i^T,   P^T = exp2(S^T tau log2e - L_i log2e)       (= e^(S - m)/l)
+//     dV_j += P^T dO_i,   dP^T = V_j dO_i^T,   dS^T = P^T o (dP^T - D_i)
+//     dK_j += dS^T Q_i,   dQ_i += dS K_j      (tau applied to dK here and to dQ on conversion)
+// with D_i = sum_k dO_ik O_ik precomputed by the preprocess kernel (the §5.4 identity).
+//
+// One CTA owns a 128-key tile of one head for its whole life: K_j, V_j stay in shared
+// memory and the dK_j, dV_j accumulators stay in TMEM, while 128-row query tiles
+// (Q_i, dO_i, L_i, D_i) stream through a two-stage TMA ring.  Working transposed puts keys on
+// TMEM lanes, so one thread owns one key row: P^T and dS^T need no cross-thread reduction,
+// P^T goes back into TMEM as the A operand of dV += P^T dO, and dS^T goes to shared memory
+// where the same swizzled bytes serve as the K-major A operand of dK += dS^T Q and as the
+// MN-major A operand of dQ = dS K.  The per-tile dQ_i partial (TMEM, reusing the dP^T
+// columns) is drained by a second warpgroup and added into the fp32 accumulator in global
+// memory with vector atomics.
+//
+// TMEM columns: [0,128) S^T / P^T, [128,256) dP^T then dQ_i, [256,256+d) dV, [256+d,256+2d) dK.
+// Causal: a key tile only meets query tiles at or after its diagonal (whole tiles in the
+// future are skipped, §5.3) and only the diagonal pair is masked element-wise.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;  // query rows per step
+constexpr int BN = 128;  // key rows per CTA
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KB = D / 64;
+  static constexpr int TILE_BYTES = BN * D * 2;  // K, V, Q_i, dO_i tiles (128 rows each)
+  static constexpr int DS_BYTES = BN * BM * 2;
+  static constexpr int THREADS = 320;             // WG0 compute, WG1 dQ drain, TMA warp, MMA warp
+  static constexpr int PRODUCER_WARP = 8;
+  static constexpr int MMA_WARP = 9;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE_BYTES;
+  static constexpr int OFF_Q = OFF_V + TILE_BYTES;           // [2] stages
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;      // [2] stages
+  static constexpr int OFF_DS = OFF_DO + 2 * TILE_BYTES;
+  static constexpr int OFF_VEC = OFF_DS + DS_BYTES;          // [2] stages x (L2[128], D[128]) fp32
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * BM * 4;
+  static constexpr int NBAR = 16;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
+};
+
+enum BwdBar {
+  B_KV = 0,
+  B_QD_FULL = 1,   // [2]
+  B_QD_EMPTY = 3,  // [2]
+  B_S_FULL = 5,
+  B_DP_FULL = 6,
+  B_P_READY = 7,
+  B_DS_READY = 8,
+  B_DQ_FULL = 9,
+  B_DQ_FREE = 10,
+  B_ACC_FULL = 11,
+  B_DRAIN = 12,
+};
+
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row16(void* base, int64_t row, const uint32_t (&pk)[16], int chunk) {
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(base) + row * D * 2 + chunk * 64);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const float* __restrict__ lse2, const float* __restrict__ delta, float* __restrict__ dq_acc,
+                  void* __restrict__ dk_out, void* __restrict__ dv_out, int n, int npad, int ktiles,
+                  float scale, int causal, unsigned long long* err, unsigned long long* counter) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const ErrCtx ctx{err, abort_flag};
+
+  const int head = blockIdx.x / ktiles;
+  const int kt = blockIdx.x - head * ktiles;  // heavy (early) key tiles first under causal
+  const int k0 = kt * BN;
+  const int qtiles = (n + BM - 1) / BM;
+  const int i_start = causal ? kt : 0;  // BM == BN: query tile kt holds the diagonal
+  const int nsteps = qtiles - i_start;
+  const float scale_log2 = scale * 1.4426950408889634f;
+
+  if (threadIdx.x == 0) {
+    if ((smem_u32(smem) & 1023u) != 0) report_error(err, DERR_BAD_SMEM_ALIGN, 1);
+    *abort_flag = (smem_u32(smem) & 1023u) != 0;
+    mbar_init(bar + B_KV, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar + B_QD_FULL + s, 1);
+      mbar_init(bar + B_QD_EMPTY + s, 1);
+    }
+    mbar_init(bar + B_S_FULL, 1);
+    mbar_init(bar + B_DP_FULL, 1);
+    mbar_init(bar + B_P_READY, 128);
+    mbar_init(bar + B_DS_READY, 128);
+    mbar_init(bar + B_DQ_FULL, 1);
+    mbar_init(bar + B_DQ_FREE, 128);
+    mbar_init(bar + B_ACC_FULL, 1);
+    mbar_init(bar + B_DRAIN, 1);
+    fence_barrier_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const bool start_ok = (*abort_flag == 0);
+
+  if (warp == C::PRODUCER_WARP) {
+    // ------------------------------------------------------------------ TMA producer
+    if (start_ok && lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(bar + B_KV, 2 * C::TILE_BYTES);
+      for (int kb = 0; kb < C::KB; ++kb) {
+        tma_load_3d(smem + C::OFF_K + kb * (BN * 128), &tm_k, bar + B_KV, kb * 64, k0, head);
+        tma_load_3d(smem + C::OFF_V + kb * (BN * 128), &tm_v, bar + B_KV, kb * 64, k0, head);
+      }
+      int issued = 0;
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i & 1, use = i >> 1;
+        if (use > 0 && !mbar_wait(bar + B_QD_EMPTY + s, (use - 1) & 1, ctx, 110)) break;
+        const int q0 = (i_start + i) * BM;
+        uint64_t* fb = bar + B_QD_FULL + s;
+        mbar_arrive_expect_tx(fb, 2 * C::TILE_BYTES + 2 * BM * 4);
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_3d(smem + C::OFF_Q + s * C::TILE_BYTES + kb * (BM * 128), &tm_q, fb, kb * 64, q0, head);
+          tma_load_3d(smem + C::OFF_DO + s * C::TILE_BYTES + kb * (BM * 128), &tm_do, fb, kb * 64, q0, head);
+        }
+        float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + s * 2 * BM;
+        bulk_load(vec, lse2 + (int64_t)head * npad + q0, BM * 4, fb);
+        bulk_load(vec + BM, delta + (int64_t)head * npad + q0, BM * 4, fb);
+        issued = i + 1;
+      }
+      ErrCtx nctx = ctx;
+      int no_abort = 0;
+      nctx.abort = &no_abort;
+      mbar_wait(bar + B_KV, 0, nctx, 111);
+      for (int i = issued - 1; i >= 0 && i >= issued - 2; --i) mbar_wait(bar + B_QD_FULL + (i & 1), (i >> 1) & 1, nctx, 112);
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (start_ok && lane == 0) {
+      const uint32_t idesc_s = make_idesc_f16(BN, BM, BF16, false, false);   // S^T, dP^T: M=keys, N=queries
+      const uint32_t idesc_kv = make_idesc_f16(BN, D, BF16, false, true);    // dV, dK: M=keys, N=d
+      const uint32_t idesc_q = make_idesc_f16(BM, D, BF16, true, true);      // dQ: M=queries (MN-major A)
+      const uint32_t ks = smem_u32(smem + C::OFF_K), vs = smem_u32(smem + C::OFF_V);
+      const uint32_t dss = smem_u32(smem + C::OFF_DS);
+      bool ok = mbar_wait(bar + B_KV, 0, ctx, 120);
+      for (int i = 0; ok && i < nsteps; ++i) {
+        const int s = i & 1;
+        const uint32_t qs = smem_u32(smem + C::OFF_Q + s * C::TILE_BYTES);
+        const uint32_t dos = smem_u32(smem + C::OFF_DO + s * C::TILE_BYTES);
+        if (!(ok = mbar_wait(bar + B_QD_FULL + s, (i >> 1) & 1, ctx, 121))) break;
+        tc_fence_after();
+        // S^T = K Q_i^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk * 16 / 64) * (BN * 128) + (kk * 16 % 64) * 2;
+          umma_ss(tbase + C::COL_S, make_sdesc_sw128(ks + off, 16, 1024), make_sdesc_sw128(qs + off, 16, 1024),
+                  idesc_s, kk > 0);
+        }
+        umma_commit(bar + B_S_FULL);
+        // dP^T = V dO_i^T (its columns held dQ_{i-1}: wait until that was read out)
+        if (i > 0) {
+          if (!(ok = mbar_wait(bar + B_DQ_FREE, (i - 1) & 1, ctx, 122))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk * 16 / 64) * (BN * 128) + (kk * 16 % 64) * 2;
+          umma_ss(tbase + C::COL_DP, make_sdesc_sw128(vs + off, 16, 1024), make_sdesc_sw128(dos + off, 16, 1024),
+                  idesc_s, kk > 0);
+        }
+        umma_commit(bar + B_DP_FULL);
+        // dV += P^T dO_i (P^T from TMEM, K = queries)
+        if (!(ok = mbar_wait(bar + B_P_READY, i & 1, ctx, 123))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_ts(tbase + C::COL_DV, tbase + C::COL_S + kk * 8, make_sdesc_sw128(dos + kk * 2048, BM * 128, 1024),
+                  idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i (dS^T K-major in smem)
+        if (!(ok = mbar_wait(bar + B_DS_READY, i & 1, ctx, 124))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint32_t off = (kk * 16 / 64) * (BN * 128) + (kk * 16 % 64) * 2;
+          umma_ss(tbase + C::COL_DK, make_sdesc_sw128(dss + off, 16, 1024),
+                  make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024), idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar + B_QD_EMPTY + s);
+        // dQ_i = dS K_j (dS read MN-major from the same buffer, K_j MN-major), into the dP^T columns
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ss(tbase + C::COL_DP, make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024),
+                  make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024), idesc_q, kk > 0);
+        umma_commit(bar + B_DQ_FULL);
+      }
+      if (ok) umma_commit(bar + B_ACC_FULL);
+      ErrCtx nctx = ctx;
+      int no_abort = 0;
+      nctx.abort = &no_abort;
+      umma_commit(bar + B_DRAIN);
+      mbar_wait(bar + B_DRAIN, 0, nctx, 125);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ WG0: P^T, dS^T, epilogue
+    const uint32_t lane_base = warp * 32;
+    const int rit = warp * 32 + lane;  // key row within the tile
+    const int key = k0 + rit;
+    const bool key_ok = key < n;
+    uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
+    const uint32_t sw = (uint32_t)(rit & 7);
+    bool ok = start_ok;
+    for (int i = 0; ok && i < nsteps; ++i) {
+      const int s = i & 1;
+      const int q0 = (i_start + i) * BM;
+      const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
+      const float* dvec = l2v + BM;
+      // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (i >> 1) & 1, ctx, 133));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, i & 1, ctx, 130));
+      if (!ok) break;
+      tc_fence_after();
+      float p[BM];
+#pragma unroll
+      for (int c = 0; c < BM / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + c * 32), r);
+        tmem_wait_ld();
+        reg_fence(r);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) p[c * 32 + t] = __uint_as_float(r[t]);
+      }
+      // queries q0 + c with c < mask_below are in the past of this key (causal diagonal)
+      const int mask_below = causal ? key - q0 : 0;
+#pragma unroll
+      for (int c = 0; c < BM; ++c) {
+        const float e = ex2(fmaf(p[c], scale_log2, -l2v[c]));
+        p[c] = (key_ok && c >= mask_below) ? e : 0.f;
+      }
+#pragma unroll
+      for (int h = 0; h < BM / 64; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) pk[t] = pack2<BF16>(p[h * 64 + 2 * t], p[h * 64 + 2 * t + 1]);
+        tmem_st32(tmem_addr(tbase, lane_base, C::COL_S + h * 32), pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar + B_P_READY);
+      // dS^T = P^T o (dP^T - D)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DP_FULL, i & 1, ctx, 131));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < BM / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + c * 32), r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const int qa = c * 32 + 2 * t;
+          const float d0 = p[qa] * (__uint_as_float(r[2 * t]) - dvec[qa]);
+          const float d1 = p[qa + 1] * (__uint_as_float(r[2 * t + 1]) - dvec[qa + 1]);
+          pk[t] = pack2<BF16>(d0, d1);
+        }
+        // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
+        uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
+          *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar + B_DS_READY);
+    }
+    // epilogue: dV, dK (x tau) from TMEM to global
+    if (ok && nsteps > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, 0, ctx, 132));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col = which ? C::COL_DK : C::COL_DV;
+          const float f = which ? scale : 1.f;
+          void* dst = which ? dk_out : dv_out;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem_addr(tbase, lane_base, col + c * 32), r);
+            tmem_wait_ld();
+            reg_fence(r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              pk[t] = pack2<BF16>(__uint_as_float(r[2 * t]) * f, __uint_as_float(r[2 * t + 1]) * f);
+            if (key_ok) store_row16<D, BF16>(dst, (int64_t)head * n + key, pk, c);
+          }
+        }
+        if (counter && rit == 0) atomicAdd(counter, (unsigned long long)nsteps);
+      }
+    } else if (ok && nsteps == 0 && key_ok) {
+      // no query meets this key tile: zero gradients (not reachable for square causal masks)
+      uint32_t pk[16] = {};
+      for (int c = 0; c < D / 32; ++c) {
+        store_row16<D, BF16>(dk_out, (int64_t)head * n + key, pk, c);
+        store_row16<D, BF16>(dv_out, (int64_t)head * n + key, pk, c);
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ WG1: drain dQ_i partials
+    const uint32_t lane_base = (warp & 3) * 32;
+    const int rit = (warp & 3) * 32 + lane;  // query row within the tile
+    bool ok = start_ok;
+    for (int i = 0; ok && i < nsteps; ++i) {
+      const int q0 = (i_start + i) * BM;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, i & 1, ctx, 140));
+      if (!ok) break;
+      tc_fence_after();
+      float acc[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + c * 32), r);
+        tmem_wait_ld();
+        reg_fence(r);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[c * 32 + t] = __uint_as_float(r[t]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar + B_DQ_FREE);
+      float4* dst = reinterpret_cast<float4*>(dq_acc + ((int64_t)head * npad + q0 + rit) * D);
+#pragma unroll
+      for (int c = 0; c < D / 4; ++c)
+        atomicAdd(dst + c, make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_d(const BwdArgs& a) {
+  using C = BwdCfg<D>;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, a.bh, BN) ||
+      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, a.bh, BN) ||
+      !make_tmap_16bit_3d(&tdo, a.dout, BF16, D, a.n, a.bh, BM))
+    return cudaErrorInvalidValue;
+  auto kern = bwd_tc_kernel<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int ktiles = (a.n + BN - 1) / BN;
+  const int npad = (int)padded_rows(a.n);
+  kern<<<(unsigned)(a.bh * ktiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, tdo, a.lse2, a.delta, a.dq_acc, a.dk,
+                                                                      a.dv, a.n, npad, ktiles, a.scale, a.causal,
+                                                                      a.err, a.counter);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int dtype, int d) { return (dtype == DT_BF16 || dtype == DT_FP16) && (d == 64 || d == 128); }
+
+cudaError_t launch_bwd_tc(const BwdArgs& a) {
+  const bool bf = a.dtype == DT_BF16;
+  switch (a.d) {
+    case 64: return bf ? launch_bwd_d<64, true>(a) : launch_bwd_d<64, false>(a);
+    case 128: return bf ? launch_bwd_d<128, true>(a) : launch_bwd_d<128, false>(a);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,460 @@
+// Tensor-core forward for bf16/fp16, head dims 64/128/256 (sm_103a: TMA, tcgen05, TMEM).
+//
+// What it computes (per head, rows i of Q): O_i = softmax(tau q_i K^T [+ causal mask]) V and
+// L_i = m_i + ln l_i, exactly, with S and P only ever on chip ("Lecture 8 · GPU Performance
+// & FlashAttention" §5.3 tiled forward, §5.4 what is kept for the backward; "FlashAttention
+// and GPU memory" §07/§08).
+//
+// Work split (FA2 order, "Lecture 8" §8.1): one CTA owns NQ query tiles of 128 rows of one
+// head and streams 128-key tiles K_j, V_j through a shared-memory ring.  Roles:
+//   * softmax warpgroup q (4 warps, one thread per query row): reads S_q from TMEM,
+//     applies the causal/ragged mask, runs the online softmax in the exp2 domain (§5.2),
+//     writes P (16-bit) back into TMEM over S, rescales the O accumulator in TMEM when the
+//     running maximum grows, and at the end divides by l and stores O and L;
+//   * TMA warp: Q once, then K_j and V_j into the ring (rows past N read as zeros);
+//   * MMA warp (one thread): S_q = Q_q K_j^T (both operands in smem) and
+//     O_q += P_q V_j (P from TMEM, V from smem), accumulating in TMEM.
+// With NQ = 2 (d = 64, 128) the two query tiles ping-pong: while one warpgroup does its
+// softmax the tensor core runs the other tile's GEMMs (the interleave of "FlashAttention
+// and GPU memory" §11).  With NQ = 1 (d = 256: O alone fills half of TMEM) S is
+// double-buffered instead, so S_{j+1} is computed during the softmax of block j.
+//
+// Lazy rescaling: the reference maximum m used in exp2(x - m) is only raised when the new
+// block maximum exceeds it by more than 8 (log2 units); until then P <= 2^8.  The final
+// O / l and L = m + ln l use the same m, so the result is unchanged (the online-softmax
+// identity holds for any reference value, §5.2).
+//
+// Causal: key tiles wholly in the future of a query tile are never loaded or multiplied
+// (§5.3 closing paragraph); only diagonal tiles are masked element-wise.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per tile
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NQ = (D == 256) ? 1 : 2;
+  static constexpr int KB = D / 64;                 // 64-column (128-byte) blocks per row
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int TILE_BYTES = BN * D * 2;
+  static constexpr int STAGES = (D == 64) ? 8 : (D == 128 ? 4 : 2);
+  static constexpr int SOFTMAX_WARPS = 4 * NQ;
+  static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
+  static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
+  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  // TMEM columns
+  static constexpr int S_COL0 = 0, S_COL1 = 128;
+  static constexpr int O_COL0 = 256;
+  static constexpr int O_COL1 = (NQ == 2) ? 256 + D : 256;
+  // shared memory
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = NQ * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + STAGES * TILE_BYTES;
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+};
+
+struct FwdSmemBars {
+  uint64_t* q_full;
+  uint64_t* kv_full;
+  uint64_t* kv_empty;
+  uint64_t* s_full;   // [2]
+  uint64_t* p_full;   // [2]
+  uint64_t* o_full;   // [2]
+  uint64_t* pv_done;  // [1] (NQ = 1)
+  uint64_t* drain;    // [1]
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, float* __restrict__ lse, int n,
+                  int bh_count, int tiles_per_head, float scale_log2, int causal, unsigned long long* err,
+                  unsigned long long* counter) {
+  using C = FwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  FwdSmemBars B;
+  B.q_full = bars;
+  B.kv_full = bars + 1;
+  B.kv_empty = bars + 1 + C::STAGES;
+  B.s_full = bars + 1 + 2 * C::STAGES;
+  B.p_full = B.s_full + 2;
+  B.o_full = B.p_full + 2;
+  B.pv_done = B.o_full + 2;
+  B.drain = B.pv_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const ErrCtx ctx{err, abort_flag};
+
+  // work item: head-major so concurrently running CTAs share K/V in L2; heavy causal tiles first
+  const int head = blockIdx.x / tiles_per_head;
+  int tile = blockIdx.x - head * tiles_per_head;
+  if (causal) tile = tiles_per_head - 1 - tile;
+  const int qrow0 = tile * (C::NQ * BM);
+  const int nblocks = (n + BN - 1) / BN;
+  int nq[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int first = qrow0 + q * BM;
+    if (q >= C::NQ || first >= n) {
+      nq[q] = 0;
+    } else if (causal) {
+      nq[q] = min(nblocks, (min(first + BM, n) - 1) / BN + 1);
+    } else {
+      nq[q] = nblocks;
+    }
+  }
+  const int nmax = max(nq[0], nq[1]);
+
+  if (threadIdx.x == 0) {
+    if ((smem_u32(smem) & 1023u) != 0) report_error(err, DERR_BAD_SMEM_ALIGN, 0);
+    *abort_flag = (smem_u32(smem) & 1023u) != 0;
+    mbar_init(B.q_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(B.kv_full + s, 1);
+      mbar_init(B.kv_empty + s, 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(B.s_full + q, 1);
+      mbar_init(B.p_full + q, 128);
+      mbar_init(B.o_full + q, 1);
+    }
+    mbar_init(B.pv_done, 1);
+    mbar_init(B.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const bool start_ok = (*abort_flag == 0);
+
+  if (warp == C::PRODUCER_WARP) {
+    // ------------------------------------------------------------------ TMA producer
+    if (start_ok && lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(B.q_full, C::NQ * C::Q_BYTES);
+      for (int q = 0; q < C::NQ; ++q)
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(smem + C::OFF_Q + q * C::Q_BYTES + kb * (BM * 128), &tm_q, B.q_full, kb * 64,
+                      qrow0 + q * BM, head);
+      int issued = 0;
+      for (int idx = 0; idx < 2 * nmax; ++idx) {
+        const int slot = idx % C::STAGES, use = idx / C::STAGES;
+        if (use > 0 && !mbar_wait(B.kv_empty + slot, (use - 1) & 1, ctx, 10)) break;
+        mbar_arrive_expect_tx(B.kv_full + slot, C::TILE_BYTES);
+        uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
+        const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, kb * 64, (idx >> 1) * BN, head);
+        issued = idx + 1;
+      }
+      // drain: every copy this thread started must land before the CTA may exit
+      ErrCtx nctx = ctx;
+      int no_abort = 0;
+      nctx.abort = &no_abort;
+      mbar_wait(B.q_full, 0, nctx, 11);
+      for (int idx = issued - 1; idx >= 0 && idx >= issued - C::STAGES; --idx)
+        mbar_wait(B.kv_full + idx % C::STAGES, (idx / C::STAGES) & 1, nctx, 12);
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (start_ok && lane == 0) {
+      const uint32_t idesc_qk = make_idesc_f16(BM, BN, BF16, false, false);
+      const uint32_t idesc_pv = make_idesc_f16(BM, D, BF16, false, true);
+      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+      const uint32_t ring = smem_u32(smem + C::OFF_RING);
+      auto slot_of = [&](int idx) { return idx % C::STAGES; };
+      auto wait_full = [&](int idx) {
+        return mbar_wait(B.kv_full + slot_of(idx), (idx / C::STAGES) & 1, ctx, 20);
+      };
+      // S = Q_q K^T into TMEM columns s_col
+      auto issue_qk = [&](int q, int kidx, uint32_t s_col) {
+        const uint32_t kt = ring + slot_of(kidx) * C::TILE_BYTES;
+        const uint32_t qt = q_base + q * C::Q_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int k0 = kk * 16;
+          const uint32_t off = (k0 / 64) * (BM * 128) + (k0 % 64) * 2;
+          const uint32_t offk = (k0 / 64) * (BN * 128) + (k0 % 64) * 2;
+          umma_ss(tbase + s_col, make_sdesc_sw128(qt + off, 16, 1024), make_sdesc_sw128(kt + offk, 16, 1024),
+                  idesc_qk, kk > 0);
+        }
+      };
+      // O += P V with P (16-bit, packed pairs) in TMEM columns [p_col, p_col + 64)
+      auto issue_pv = [&](uint32_t o_col, uint32_t p_col, int vidx, bool acc) {
+        const uint32_t vt = ring + slot_of(vidx) * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts(tbase + o_col, tbase + p_col + kk * 8, make_sdesc_sw128(vt + kk * 2048, BN * 128, 1024),
+                  idesc_pv, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(B.q_full, 0, ctx, 21);
+      if (ok) tc_fence_after();
+      if constexpr (C::NQ == 2) {
+        if (ok && nmax > 0) {
+          ok = wait_full(0);
+          if (ok) {
+            tc_fence_after();
+            if (nq[0] > 0) { issue_qk(0, 0, C::S_COL0); umma_commit(B.s_full + 0); }
+            if (nq[1] > 0) { issue_qk(1, 0, C::S_COL1); umma_commit(B.s_full + 1); }
+            umma_commit(B.kv_empty + slot_of(0));
+          }
+        }
+        for (int j = 0; ok && j < nmax; ++j) {
+          const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+          if (!(ok = wait_full(vidx))) break;
+          if (j < nq[0]) {
+            if (!(ok = mbar_wait(B.p_full + 0, j & 1, ctx, 22))) break;
+            tc_fence_after();
+            issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
+          }
+          if (j + 1 < nmax) {
+            if (!(ok = wait_full(kidx))) break;
+            tc_fence_after();
+          }
+          if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); umma_commit(B.s_full + 0); }
+          if (j < nq[1]) {
+            if (!(ok = mbar_wait(B.p_full + 1, j & 1, ctx, 23))) break;
+            tc_fence_after();
+            issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
+          }
+          umma_commit(B.kv_empty + slot_of(vidx));
+          if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); umma_commit(B.s_full + 1); }
+          if (j + 1 < nmax) umma_commit(B.kv_empty + slot_of(kidx));
+          if (j == nq[0] - 1) umma_commit(B.o_full + 0);
+          if (j == nq[1] - 1) umma_commit(B.o_full + 1);
+        }
+      } else {
+        // NQ == 1: S double-buffered in columns 0 / 128, O at 256
+        const int nb = nq[0];
+        if (ok && nb > 0) {
+          for (int j = 0; ok && j < 2 && j < nb; ++j) {
+            if (!(ok = wait_full(2 * j))) break;
+            tc_fence_after();
+            issue_qk(0, 2 * j, j ? C::S_COL1 : C::S_COL0);
+            umma_commit(B.s_full + j);
+            umma_commit(B.kv_empty + slot_of(2 * j));
+          }
+        }
+        for (int j = 0; ok && j < nb; ++j) {
+          const int vidx = 2 * j + 1;
+          const uint32_t buf = (j & 1) ? C::S_COL1 : C::S_COL0;
+          if (!(ok = wait_full(vidx))) break;
+          if (!(ok = mbar_wait(B.p_full + 0, j & 1, ctx, 24))) break;
+          tc_fence_after();
+          issue_pv(C::O_COL0, buf, vidx, j > 0);
+          umma_commit(B.pv_done);
+          umma_commit(B.kv_empty + slot_of(vidx));
+          if (j + 2 < nb) {
+            const int kidx = 2 * (j + 2);
+            if (!(ok = wait_full(kidx))) break;
+            tc_fence_after();
+            issue_qk(0, kidx, buf);
+            umma_commit(B.s_full + (j & 1));
+            umma_commit(B.kv_empty + slot_of(kidx));
+          }
+          if (j == nb - 1) umma_commit(B.o_full + 0);
+        }
+      }
+      // drain: all MMAs complete before TMEM is released
+      ErrCtx nctx = ctx;
+      int no_abort = 0;
+      nctx.abort = &no_abort;
+      umma_commit(B.drain);
+      mbar_wait(B.drain, 0, nctx, 25);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int q = warp >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_base = quarter * 32;
+    const int rit = quarter * 32 + lane;
+    const int row = qrow0 + q * BM + rit;
+    const int nb = nq[q];
+    const uint32_t o_col = q ? C::O_COL1 : C::O_COL0;
+    float m = -INFINITY;  // reference maximum, log2 units (scores * tau * log2 e)
+    float l = 0.f;
+    bool ok = start_ok;
+    for (int j = 0; ok && j < nb; ++j) {
+      uint32_t s_col;
+      uint64_t* sbar;
+      uint32_t sparity;
+      if constexpr (C::NQ == 2) {
+        s_col = q ? C::S_COL1 : C::S_COL0;
+        sbar = B.s_full + q;
+        sparity = j & 1;
+      } else {
+        s_col = (j & 1) ? C::S_COL1 : C::S_COL0;
+        sbar = B.s_full + (j & 1);
+        sparity = (j >> 1) & 1;
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(sbar, sparity, ctx, 30 + q));
+      if (!ok) break;
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tbase, lane_base, s_col + c * 32), r);
+        tmem_wait_ld();
+        reg_fence(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+      }
+      // mask: keys past N, and (causal) keys after this row
+      int limit = n - j * BN;
+      if (causal) limit = min(limit, row - j * BN + 1);
+      if (limit < BN) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c >= limit) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_blk = mx * scale_log2;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m == -INFINITY) {
+        m = m_blk;  // first visible block of this row: O is written fresh (or is still zero)
+        alpha = 0.f;
+      } else if (m_blk > m + kRescaleThreshold) {
+        alpha = ex2(m - m_blk);
+        m = m_blk;
+        rescale = true;
+      }
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      float sum = 0.f;
+#pragma unroll
+      for (int h = 0; h < BN / 64; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(s[h * 64 + 2 * i], scale_log2, neg_m));
+          const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], scale_log2, neg_m));
+          sum += p0 + p1;
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        tmem_st32(tmem_addr(tbase, lane_base, s_col + h * 32), pk);
+      }
+      l = l * alpha + sum;
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O row *= alpha; O is stable: the PV of block j-1 completed before S_j
+        // (NQ = 2: same issuing thread, in order) or pv_done says so (NQ = 1).
+        if constexpr (C::NQ == 1) {
+          ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done, (j - 1) & 1, ctx, 34));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const float a = rescale ? alpha : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          const uint32_t ta = tmem_addr(tbase, lane_base, o_col + c * 32);
+          tmem_ld32(ta, r);
+          tmem_wait_ld();
+          reg_fence(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+          tmem_st32(ta, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(B.p_full + q);
+    }
+    // epilogue: O / l -> global (16-bit), L = (m + log2 l) ln 2
+    if (ok && nb > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(B.o_full + q, 0, ctx, 40 + q));
+      if (ok) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem_addr(tbase, lane_base, o_col + c * 32), r);
+          tmem_wait_ld();
+          reg_fence(r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+          if (row < n) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (row < n) lse[(int64_t)head * n + row] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        if (counter && rit == 0) atomicAdd(counter, (unsigned long long)nb);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_d(const FwdArgs& a) {
+  using C = FwdCfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, a.bh, BN) ||
+      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, a.bh, BN))
+    return cudaErrorInvalidValue;
+  auto kern = fwd_tc_kernel<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
+  const float scale_log2 = a.scale * 1.4426950408889634f;
+  kern<<<(unsigned)(a.bh * tiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles,
+                                                                     scale_log2, a.causal, a.err, a.counter);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool fwd_tc_supported(int dtype, int d) {
+  return (dtype == DT_BF16 || dtype == DT_FP16) && (d == 64 || d == 128 || d == 256);
+}
+
+cudaError_t launch_fwd_tc(const FwdArgs& a) {
+  const bool bf = a.dtype == DT_BF16;
+  switch (a.d) {
+    case 64: return bf ? launch_fwd_d<64, true>(a) : launch_fwd_d<64, false>(a);
+    case 128: return bf ? launch_fwd_d<128, true>(a) : launch_fwd_d<128, false>(a);
+    case 256: return bf ? launch_fwd_d<256, true>(a) : launch_fwd_d<256, false>(a);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,68 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fa {
+
+enum Dtype : int { DT_BF16 = 0, DT_FP16 = 1, DT_FP32 = 2 };
+
+// Rows of the padded per-head statistics and of the fp32 dQ accumulator.
+inline int64_t padded_rows(int64_t n) { return (n + 127) / 128 * 128; }
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int bh;  // B*H
+  int n;
+  int d;
+  float scale;
+  int causal;
+  int dtype;
+  unsigned long long* err;      // device error word
+  unsigned long long* counter;  // device count of processed (query tile, key tile) pairs
+  cudaStream_t stream;
+};
+
+// Backward workspace, carved from one caller buffer of fa_bwd_workspace_size bytes:
+//   delta  [bh][npad]     fp32  D_i = sum_k dO_ik O_ik (0 on padding rows)
+//   lse2   [bh][npad]     fp32  L_i * log2(e) (+inf on padding rows)
+//   dq_acc [bh][npad][d]  fp32  accumulated dS K (before the factor tau)
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;
+  float* lse2;
+  float* dq_acc;
+  int bh;
+  int n;
+  int d;
+  float scale;
+  int causal;
+  int dtype;
+  unsigned long long* err;
+  unsigned long long* counter;
+  cudaStream_t stream;
+};
+
+bool fwd_tc_supported(int dtype, int d);
+bool bwd_tc_supported(int dtype, int d);
+
+cudaError_t launch_fwd_tc(const FwdArgs& a);
+cudaError_t launch_fwd_simt(const FwdArgs& a);
+cudaError_t launch_bwd_pre(const BwdArgs& a);
+cudaError_t launch_bwd_tc(const BwdArgs& a);
+cudaError_t launch_bwd_simt(const BwdArgs& a);
+cudaError_t launch_dq_convert(const BwdArgs& a);
+
+}  // namespace fa

@@ -1,0 +1,143 @@
+/*
+ * fa.h — C ABI of the exact tiled attention library for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is exact scaled-dot-product attention computed tile by tile with an
+ * online softmax, so the N x N score matrix S and probability matrix P never reach
+ * device memory:
+ *
+ *   forward   O = softmax(scale * Q K^T [+ causal mask]) V,   L_i = m_i + ln l_i
+ *   backward  dQ, dK, dV of f = sum(O o dO), recomputing S and P block by block from
+ *             Q, K and L, with D_i = sum_k dO_ik O_ik precomputed
+ *
+ * Sources (page title, section): "Lecture 8 · GPU Performance & FlashAttention"
+ * (CS324 notes) §5.1 standard attention, §5.2 online softmax, §5.3 tiled forward and
+ * causal block skipping, §5.4 recomputing backward and the D identity, §8.1 FA2 work
+ * split; "FlashAttention and GPU memory" (world.lapla.si explainer) §07–§09.
+ *
+ * Conventions shared by every entry point
+ *   Layout    Q, K, V, O, dO, dQ, dK, dV: contiguous row-major [B][H][N][d] of the
+ *             element type `dtype` (one N x d matrix per head). L: fp32 [B][H][N],
+ *             natural-log units. Keys and queries have the same length N.
+ *   Causal    causal != 0 masks key j for query i when j > i (top-left aligned).
+ *   Memory    All pointers are DEVICE pointers owned by the caller; the library keeps no
+ *             per-call allocation and never allocates anything N x N. Every pointer
+ *             must be 16-byte aligned. Buffers must not overlap, except that the
+ *             library only reads Q, K, V, O, dO and L.
+ *   Streams   `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *             asynchronous: they validate, enqueue kernels on `stream` and return.
+ *   Errors    Invalid arguments return an error and launch nothing. Device-side
+ *             failures (a bounded wait that timed out) are recorded in a library error
+ *             word and reported by fa_check_device_error. No C++ exception crosses
+ *             this interface. fa_last_error_message() describes the last failure of
+ *             the calling thread.
+ *   Paths     bf16/fp16 with d in {64, 128, 256} (forward) or {64, 128} (backward)
+ *             run the tensor-core kernels (TMA, tcgen05 MMAs accumulating in tensor
+ *             memory); fp32, and any other d in [1, 256], run CUDA-core kernels that
+ *             compute in fp32.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1, FA_FP32 = 2 } fa_dtype;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, scale not finite and > 0 */
+  FA_ERR_UNSUPPORTED = 2, /* dtype or head dimension outside what any kernel handles */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  FA_ERR_TIMEOUT = 4,     /* a kernel's bounded wait expired (reported by fa_check_device_error) */
+  FA_ERR_DEVICE = 5       /* another device-side check failed (reported by fa_check_device_error) */
+} fa_status;
+
+/*
+ * Forward pass ("Lecture 8" §5.3; FA2 order §8.1).
+ *   Q, K, V   in:  [B][H][N][d] dtype
+ *   O         out: [B][H][N][d] dtype, softmax(scale Q K^T [+mask]) V
+ *   L         out: [B][H][N] fp32, row log-sum-exp of the (masked) scaled scores
+ *   B, H, N   >= 0 (an empty problem returns FA_OK without launching); d in [1, 256]
+ *   scale     the factor tau on Q K^T, finite and > 0 (usually 1/sqrt(d))
+ * Launches one kernel.
+ */
+FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: per head, with Np = N rounded up to 128,
+ * D [Np] fp32, L*log2(e) [Np] fp32 and an fp32 dQ accumulator [Np][d].
+ * Returns 0 for invalid sizes.
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass with recomputation ("Lecture 8" §5.4): the three stages below in order.
+ *   Q, K, V, O, dO  in:  [B][H][N][d] dtype (O from fa_fwd)
+ *   L               in:  [B][H][N] fp32 from fa_fwd
+ *   dQ, dK, dV      out: [B][H][N][d] dtype
+ *   workspace       scratch of at least fa_bwd_workspace_size(B, H, N, d) bytes, 16-byte
+ *                   aligned, owned by the caller; its contents on entry do not matter.
+ * Launches three kernels (preprocess, main, dQ conversion).
+ */
+FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
+                 void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * Stage 1 of fa_bwd: D_i = sum_k dO_ik O_ik (the N x d identity that replaces the N x N
+ * row sum of P o dP, "Lecture 8" §5.4), L_i log2(e) for the exp2-domain recomputation,
+ * and a zeroed dQ accumulator, all into `workspace`.
+ */
+FA_API fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* L, void* workspace, size_t workspace_bytes,
+                            int B, int H, int N, int d, fa_dtype dtype, void* stream);
+
+/*
+ * Stage 2 of fa_bwd: recompute S and P block by block and produce dK, dV (written) and
+ * the unscaled dQ sum (accumulated in `workspace`). Needs stage 1 on the same workspace.
+ */
+FA_API fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
+                      void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                      fa_dtype dtype, void* stream);
+
+/* Stage 3 of fa_bwd: dQ = scale * (dQ accumulator), converted to dtype. */
+FA_API fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void* dQ, int B, int H, int N, int d,
+                            float scale, fa_dtype dtype, void* stream);
+
+/*
+ * Synchronises `stream` and reports device-side failures of earlier calls on the
+ * current device: FA_ERR_CUDA for a CUDA error, FA_ERR_TIMEOUT / FA_ERR_DEVICE for a
+ * failure a kernel recorded. The recorded failure is cleared.
+ */
+FA_API fa_status fa_check_device_error(void* stream);
+
+/*
+ * Diagnostic: number of (query tile, key tile) pairs of 128 x 128 the tensor-core
+ * kernels (and of 32 x 32 the CUDA-core forward) processed on the current device since
+ * the last reset. Synchronises `stream`; reset != 0 clears the counter afterwards.
+ */
+FA_API fa_status fa_tile_counter(void* stream, unsigned long long* value, int reset);
+
+/* Whether the given pass ("fwd" = 0, "bwd" = 1) runs on tensor cores for dtype and d. */
+FA_API int fa_uses_tensor_cores(int pass, fa_dtype dtype, int d);
+
+/* Static text for a status code. */
+FA_API const char* fa_status_string(fa_status status);
+
+/* Description of the last failure on the calling thread ("" if none). */
+FA_API const char* fa_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,112 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side argument checks (no GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_tiled_attention_07_gb300 import build as b
+
+    path = b.build()
+    assert os.path.exists(path)
+    return ctypes.CDLL(path)
+
+
+def _declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return re.findall(r"FA_API\s+[\w\s\*]*?\b(fa_\w+)\s*\(", txt)
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared_symbols())
+    for required in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check_device_error", "fa_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_symbol():
+    from exact_tiled_attention_07_gb300 import binding
+
+    assert set(binding.EXPORTED_SYMBOLS) == set(_declared_symbols())
+    for name in _declared_symbols():
+        assert callable(getattr(binding, name))
+
+
+def test_status_strings(lib):
+    lib.fa_status_string.restype = ctypes.c_char_p
+    assert lib.fa_status_string(0) == b"ok"
+    assert b"timed out" in lib.fa_status_string(4)
+    assert lib.fa_status_string(99) == b"unknown status"
+
+
+def test_workspace_size_is_linear_in_n(lib):
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    ws = lambda b, h, n, d: lib.fa_bwd_workspace_size(b, h, n, d)
+    # D + L*log2e + fp32 dQ accumulator over N rounded up to 128: nothing N x N
+    assert ws(1, 1, 128, 64) == 128 * 4 * 66
+    assert ws(2, 3, 129, 128) == 6 * 256 * 4 * 130
+    assert ws(8, 16, 4096, 128) == 8 * 16 * 4096 * 4 * 130
+    assert ws(1, 8, 65536, 64) < 65536 * 65536  # vs. one N x N byte matrix
+    assert ws(1, 1, 16, 0) == 0 and ws(1, 1, 16, 300) == 0
+
+
+def test_invalid_arguments_are_rejected_without_launching(lib):
+    vp = ctypes.c_void_p
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                           ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+    lib.fa_last_error_message.restype = ctypes.c_char_p
+    good = vp(0x10000)
+    # empty problems succeed and launch nothing
+    assert lib.fa_fwd(None, None, None, None, None, 0, 4, 128, 64, 0.125, 0, 0, None) == 0
+    assert lib.fa_fwd(None, None, None, None, None, 2, 4, 0, 64, 0.125, 0, 0, None) == 0
+    # null / misaligned pointers
+    assert lib.fa_fwd(None, good, good, good, good, 1, 1, 128, 64, 0.125, 0, 0, None) == 1
+    assert b"null" in lib.fa_last_error_message()
+    assert lib.fa_fwd(vp(0x10008), good, good, good, good, 1, 1, 128, 64, 0.125, 0, 0, None) == 1
+    assert b"aligned" in lib.fa_last_error_message()
+    # sizes, dtype, head dim, scale
+    assert lib.fa_fwd(good, good, good, good, good, -1, 1, 128, 64, 0.125, 0, 0, None) == 1
+    assert lib.fa_fwd(good, good, good, good, good, 1, 1, 128, 512, 0.125, 0, 0, None) == 2
+    assert lib.fa_fwd(good, good, good, good, good, 1, 1, 128, 64, 0.125, 0, 7, None) == 2
+    assert lib.fa_fwd(good, good, good, good, good, 1, 1, 128, 64, float("nan"), 0, 0, None) == 1
+    assert lib.fa_fwd(good, good, good, good, good, 1, 1, 128, 64, -1.0, 0, 0, None) == 1
+
+
+def test_backward_workspace_too_small_is_rejected(lib):
+    vp = ctypes.c_void_p
+    lib.fa_bwd.argtypes = [vp] * 10 + [ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+    lib.fa_last_error_message.restype = ctypes.c_char_p
+    g = vp(0x10000)
+    st = lib.fa_bwd(g, g, g, g, g, g, g, g, g, g, 1024, 1, 1, 128, 64, 0.125, 0, 0, None)
+    assert st == 1 and b"workspace" in lib.fa_last_error_message()
+
+
+def test_kernel_selection(lib):
+    lib.fa_uses_tensor_cores.argtypes = [ctypes.c_int] * 3
+    for d in (64, 128, 256):
+        assert lib.fa_uses_tensor_cores(0, 0, d) == 1  # bf16 forward
+        assert lib.fa_uses_tensor_cores(0, 1, d) == 1  # fp16 forward
+        assert lib.fa_uses_tensor_cores(0, 2, d) == 0  # fp32: CUDA cores
+    assert lib.fa_uses_tensor_cores(1, 0, 128) == 1 and lib.fa_uses_tensor_cores(1, 0, 256) == 0
+    assert lib.fa_uses_tensor_cores(0, 0, 96) == 0
+
+
+def test_oracle_is_not_imported_by_the_product():
+    pkg = os.path.join(ROOT, "exact_tiled_attention_07_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", txt, re.M), f
+                assert "oracle/" not in txt, f
