@@ -1,0 +1,414 @@
+"""Benchmark: attention forward + backward TFLOP/s on GB300 through the C ABI.
+
+One step = the whole hot path over one batch: fa_fwd, then the three backward stages
+(fa_bwd_preprocess, fa_bwd_main, fa_bwd_dq_convert).  Default workload: the causal LM
+shape B=8, H=16, N=4096, d=128, bf16 (FLOPs: forward 4·B·H·N²·d, backward 2.5x, halved
+for causal).  Inputs are larger than L2 (each [B,H,N,d] tensor is 134 MB).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU oracle (the
+reference arm of this build) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_tiled_attention_07_gb300.inputs import WORKLOADS, Workload, attention_flops, make_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "causal_lm_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "exact_tiled_attention_07_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, if taken on the current sources."""
+    digest = source_digest()
+    for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        with open(p) as f:
+            for line in f:
+                # machine-readable line: "traffic: <kernel_key> <workload> <bytes_per_launch> sources=<digest>"
+                if line.startswith("traffic:"):
+                    parts = line.split()
+                    if len(parts) >= 5 and parts[1] == kernel_key and parts[4] == f"sources={digest}":
+                        return parts[2], float(parts[3])
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            cols = [c.strip() for c in ln.split(",")]
+            if len(cols) < 9:
+                continue
+            try:
+                sm.append(float(cols[1]))
+                smax.append(float(cols[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, cols[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (the reference of this build) and the cpu_baseline leg
+# ---------------------------------------------------------------------------
+
+
+def oracle_heads(w: Workload, target_s: float, max_heads: int):
+    """Run the fp64 oracle (forward + backward) on whole heads until ~target_s of compute.
+
+    Returns (heads, seconds of oracle compute); input generation is not timed.
+    """
+    import oracle
+    from exact_tiled_attention_07_gb300.inputs import to_float64
+
+    one = w.with_shape(B=1, H=1)
+    heads, elapsed = 0, 0.0
+    while heads < max_heads and (heads == 0 or elapsed < target_s):
+        x = make_inputs(one.with_shape(seed=w.seed + heads))
+        x64 = {k: to_float64(v, w.dtype) for k, v in x.items()}
+        t0 = time.perf_counter()
+        oracle.attn_fwd64(x64["q"], x64["k"], x64["v"], w.scale, w.causal)
+        if not w.fwd_only:
+            oracle.attn_bwd64(x64["q"], x64["k"], x64["v"], x64["do"], w.scale, w.causal)
+        elapsed += time.perf_counter() - t0
+        heads += 1
+    return heads, elapsed
+
+
+def oracle_sample(w: Workload, target_s: float = 12.0, max_heads: int = 16):
+    """The cpu_baseline leg: the oracle as it stands, on whole heads of the workload (~target_s)."""
+    heads, elapsed = oracle_heads(w, target_s, max_heads)
+    pass_ = "fwd" if w.fwd_only else "fwd+bwd"
+    flops = attention_flops(1, 1, w.N, w.d, w.causal, pass_) * heads
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.H} heads ({w.N}x{w.d}, {pass_}), numpy fp64, {elapsed:.1f} s"}
+
+
+def run_reference(args, w: Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_heads(w, 0.0, 1)
+    times = [oracle_heads(w, 0.0, 1)[1] for _ in range(args.steps)]
+    pass_ = "fwd" if w.fwd_only else "fwd+bwd"
+    flops = attention_flops(1, 1, w.N, w.d, w.causal, pass_)
+    value = flops * len(times) / sum(times) / 1e12
+    cpu = {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+           "sample": f"1 of {w.B * w.H} heads per step ({w.N}x{w.d}, {pass_}), numpy fp64"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w), "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w: Workload):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype, "causal": w.causal,
+            "passes": "fwd" if w.fwd_only else "fwd+bwd",
+            "l2": "inputs larger than L2 (no flush)" if w.B * w.H * w.N * w.d * 2 > 129e6 else "L2 flushed"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+
+def _dev_tensor(stored, dtype, device):
+    import torch
+
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(stored).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(stored))
+    return t.pin_memory().to(device, non_blocking=False), t.pin_memory()
+
+
+def run_gpu(args, w: Workload):
+    import torch
+
+    from exact_tiled_attention_07_gb300 import binding
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load_library()
+
+    # every rank owns an independent shard of the same shape (weak scaling, no exchange)
+    x = make_inputs(w.with_shape(seed=w.seed + 1000 * rank), with_do=not w.fwd_only)
+    dev, pinned = {}, {}
+    for k_, v_ in x.items():
+        dev[k_], pinned[k_] = _dev_tensor(v_, w.dtype, device)
+    del x
+    q, k, v = dev["q"], dev["k"], dev["v"]
+    do = dev.get("do")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device)
+    if not w.fwd_only:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(binding.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    scale, causal = w.scale, w.causal
+    names = ["fwd"] if w.fwd_only else ["fwd", "bwd_pre", "bwd_main", "bwd_dq_convert"]
+
+    def launch(i, causal_=causal):
+        if i == 0:
+            binding.fa_fwd(q, k, v, o, lse, scale, causal_)
+        elif i == 1:
+            binding.fa_bwd_preprocess(o, do, lse, ws)
+        elif i == 2:
+            binding.fa_bwd_main(q, k, v, do, dk, dv, ws, scale, causal_)
+        else:
+            binding.fa_bwd_dq_convert(ws, dq, scale)
+
+    def step(evs=None):
+        for i in range(len(names)):
+            if evs is not None:
+                evs[i].record(stream)
+            launch(i)
+        if evs is not None:
+            evs[len(names)].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    binding.fa_check_device_error()
+
+    # ---------------- timed region: K steps, per-kernel events on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        t_start.record(stream)
+        for s_ in range(args.steps):
+            step(ev[s_])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    binding.fa_check_device_error()
+    total_ms = t_start.elapsed_time(t_end)
+    per_kernel = {nm: sum(ev[s_][i].elapsed_time(ev[s_][i + 1]) for s_ in range(args.steps)) / args.steps
+                  for i, nm in enumerate(names)}
+    if dist:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    pass_ = "fwd" if w.fwd_only else "fwd+bwd"
+    flops_rank = attention_flops(w.B, w.H, w.N, w.d, w.causal, pass_)
+    value = flops_rank * world / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    # ---------------- roofline of the dominant kernel
+    kflops = {"fwd": attention_flops(w.B, w.H, w.N, w.d, w.causal, "fwd"),
+              "bwd_main": attention_flops(w.B, w.H, w.N, w.d, w.causal, "bwd")}
+    dom = max((nm for nm in per_kernel if nm in kflops), key=lambda nm: per_kernel[nm])
+    achieved = kflops[dom] / (per_kernel[dom] * 1e-3) / 1e12
+    _, traffic = profiled_traffic(dom)
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": achieved / peak_sus, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
+                "share_of_step": per_kernel[dom] / ms_per_step}
+
+    # ---------------- end to end: pinned host buffers -> device, the C-ABI calls, results -> host
+    h2d = sum(pinned[k_].numel() * pinned[k_].element_size() for k_ in pinned)
+    outs = [o, lse] + ([] if w.fwd_only else [dq, dk, dv])
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    ins = [(dev[k_], pinned[k_]) for k_ in pinned]
+
+    def e2e_step():
+        for d_, h_ in ins:
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(host_out, outs):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e_s.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_s.elapsed_time(e_e) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": flops_rank * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    # ---------------- per-pass figures, including the non-causal variant of the same shape
+    targets = None
+    if not args.no_targets:
+        targets = {}
+        variants = [(causal, "causal" if causal else "noncausal")]
+        if causal:
+            variants.append((False, "noncausal"))
+        for cz, tag in variants:
+            passes = [("fwd", [0])] + ([] if w.fwd_only else [("bwd", [1, 2, 3])])
+            for pname, idxs in passes:
+                reps = max(3, min(args.steps, 10))
+                for _ in range(2):
+                    for i in idxs:
+                        launch(i, cz)
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                for _ in range(reps):
+                    for i in idxs:
+                        launch(i, cz)
+                b_.record(stream)
+                torch.cuda.synchronize()
+                ms = a_.elapsed_time(b_) / reps
+                fl = attention_flops(w.B, w.H, w.N, w.d, cz, pname)
+                tf = fl / (ms * 1e-3) / 1e12
+                targets[f"{tag}_{pname}"] = {"ms": ms, "tflops": tf, "pct_of_burst_peak": 100 * tf / peak_burst,
+                                             "pct_of_sustained_peak": 100 * tf / peak_sus}
+        binding.fa_check_device_error()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(w)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": workload_config(w),
+                "pct_of_peak": {"sustained": 100 * value / world / peak_sus, "burst": 100 * value / world / peak_burst,
+                                "source": peak_src},
+                "kernels_ms": per_kernel, "gpu_launches": len(names) * args.steps, "roofline": roofline,
+                "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu, "targets": targets}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-targets", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()
