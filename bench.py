@@ -80,7 +80,7 @@ def profiled_traffic(kernel_key):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms; summary() keeps the timed window."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -96,7 +96,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, FileNotFoundError):
@@ -105,7 +105,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -117,25 +117,28 @@ class ClockSampler:
             if self.thread:
                 self.thread.join(timeout=2)
 
-    def summary(self):
-        sm, smax, reasons = [], [], set()
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and active throttle reasons over samples inside [t0, t1] (wall clock)."""
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        parsed = []
+        for ts, ln in self.lines:
             cols = [c.strip() for c in ln.split(",")]
             if len(cols) < 9:
                 continue
             try:
-                sm.append(float(cols[1]))
-                smax.append(float(cols[2]))
+                parsed.append((ts, float(cols[1]), float(cols[2]), cols[5:9]))
             except ValueError:
                 continue
-            for nm, v in zip(names, cols[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
+        window = [p for p in parsed if t0 is None or (t0 <= p[0] <= t1 + 0.1)]
+        note = "samples inside the timed region"
+        if not window and parsed:
+            window = parsed
+            note = "no sample fell inside the timed region; all samples of the run"
+        if not window:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = sorted({nm for p in window for nm, v in zip(names, p[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(p[1] for p in window), "sm_max_mhz": max(p[2] for p in window),
+                "reasons": reasons, "samples": len(window), "note": note}
 
 
 # ---------------------------------------------------------------------------
@@ -278,12 +281,14 @@ def run_gpu(args, w: Workload):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        time.sleep(0.3)
+        time.sleep(0.5)  # let the sampler start
+        wall0 = time.time()
         t_start.record(stream)
         for s_ in range(args.steps):
             step(ev[s_])
         t_end.record(stream)
         torch.cuda.synchronize()
+        wall1 = time.time()
     if dist:
         dist.barrier()
     binding.fa_check_device_error()
@@ -386,7 +391,7 @@ def run_gpu(args, w: Workload):
                 "pct_of_peak": {"sustained": 100 * value / world / peak_sus, "burst": 100 * value / world / peak_burst,
                                 "source": peak_src},
                 "kernels_ms": per_kernel, "gpu_launches": len(names) * args.steps, "roofline": roofline,
-                "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu, "targets": targets}
+                "e2e": e2e, "clocks": clocks.summary(wall0, wall1), "cpu_baseline": cpu, "targets": targets}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -395,8 +400,8 @@ def run_gpu(args, w: Workload):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -9,18 +9,24 @@
 // with D_i = sum_k dO_ik O_ik precomputed by the preprocess kernel (the §5.4 identity).
 //
 // One CTA owns a 128-key tile of one head for its whole life: K_j, V_j stay in shared
-// memory and the dK_j, dV_j accumulators stay in TMEM, while 128-row query tiles
-// (Q_i, dO_i, L_i, D_i) stream through a two-stage TMA ring.  Working transposed puts keys on
-// TMEM lanes, so one thread owns one key row: P^T and dS^T need no cross-thread reduction,
-// P^T goes back into TMEM as the A operand of dV += P^T dO, and dS^T goes to shared memory
-// where the same swizzled bytes serve as the K-major A operand of dK += dS^T Q and as the
-// MN-major A operand of dQ = dS K.  The per-tile dQ_i partial (TMEM, reusing the dP^T
-// columns) is drained by a second warpgroup and added into the fp32 accumulator in global
-// memory with vector atomics.
+// memory and the dK_j, dV_j accumulators stay in TMEM, while query tiles (Q_i, dO_i, L_i,
+// D_i) stream through a two-stage TMA ring.  Working transposed puts keys on TMEM lanes, so
+// one thread owns one key row: P^T and dS^T need no cross-thread reduction.  P^T goes back
+// into TMEM as the A operand of dV += P^T dO; dS^T goes to shared memory, where the same
+// swizzled bytes feed dK += dS^T Q and the dQ GEMM.
 //
-// TMEM columns: [0,128) S^T / P^T, [128,256) dP^T then dQ_i, [256,256+d) dV, [256+d,256+2d) dK.
-// Causal: a key tile only meets query tiles at or after its diagonal (whole tiles in the
-// future are skipped, §5.3) and only the diagonal pair is masked element-wise.
+// dQ partials are summed over key tiles in an fp32 accumulator in global memory.  A second
+// warpgroup drains each partial from TMEM into a shared-memory staging tile and one thread
+// adds the tile to global memory with a TMA bulk reduction (whole 128-byte lines, no
+// per-element atomics).  Two shapes of the dQ GEMM keep every TMEM region separate, so no
+// GEMM waits for another region to be drained:
+//   d = 64:  128 queries per step, dQ = dS K   (M = 128 queries, N = 64)
+//   d = 128:  64 queries per step, dQ^T = K^T dS^T (M = 128 = d, N = 64 queries)
+//
+// Issue order per step i (one thread): dP_i, dV_i, S_{i+1}, dK_i, dQ_i, so the softmax-side
+// work on step i+1's scores overlaps the tensor core's dK_i and dQ_i.
+// Causal: a key tile only meets query tiles that reach its diagonal (whole tiles in the
+// future are skipped, §5.3) and only pairs crossing the diagonal are masked element-wise.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cmath>
@@ -33,27 +39,36 @@
 namespace fa {
 namespace {
 
-constexpr int BM = 128;  // query rows per step
 constexpr int BN = 128;  // key rows per CTA
 
 template <int D>
 struct BwdCfg {
+  static constexpr bool DQT = (D == 128);        // dQ^T = K^T dS^T (TMEM lanes = d)
+  static constexpr int BM = DQT ? 64 : 128;      // query rows per step
   static constexpr int KB = D / 64;
-  static constexpr int TILE_BYTES = BN * D * 2;  // K, V, Q_i, dO_i tiles (128 rows each)
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int QT_BYTES = BM * D * 2;
   static constexpr int DS_BYTES = BN * BM * 2;
-  static constexpr int THREADS = 320;             // WG0 compute, WG1 dQ drain, TMA warp, MMA warp
+  static constexpr int STG_BYTES = BM * D * 4;
+  static constexpr int THREADS = 320;            // WG0 P/dS, WG1 dQ drain, TMA warp, MMA warp
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + TILE_BYTES;
-  static constexpr int OFF_Q = OFF_V + TILE_BYTES;           // [2] stages
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;      // [2] stages
-  static constexpr int OFF_DS = OFF_DO + 2 * TILE_BYTES;
-  static constexpr int OFF_VEC = OFF_DS + DS_BYTES;          // [2] stages x (L2[128], D[128]) fp32
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;       // [2] stages
+  static constexpr int OFF_DO = OFF_Q + 2 * QT_BYTES;  // [2] stages
+  static constexpr int OFF_DS = OFF_DO + 2 * QT_BYTES;
+  static constexpr int OFF_STG = OFF_DS + DS_BYTES;    // [2] staging tiles
+  static constexpr int OFF_VEC = OFF_STG + 2 * STG_BYTES;  // [2] stages x (L2[BM], D[BM]) fp32
   static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * BM * 4;
   static constexpr int NBAR = 16;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
-  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
+  // TMEM columns
+  static constexpr uint32_t COL_S = 0;
+  static constexpr uint32_t COL_DP = BM;
+  static constexpr uint32_t COL_DQ = 2 * BM;
+  static constexpr uint32_t COL_DV = DQT ? 256 : 320;
+  static constexpr uint32_t COL_DK = 384;
 };
 
 enum BwdBar {
@@ -70,7 +85,7 @@ enum BwdBar {
   B_DRAIN = 12,
 };
 
-template <int D, bool BF16>
+template <int D>
 __device__ __forceinline__ void store_row16(void* base, int64_t row, const uint32_t (&pk)[16], int chunk) {
   uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(base) + row * D * 2 + chunk * 64);
 #pragma unroll
@@ -81,10 +96,11 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const float* __restrict__ lse2, const float* __restrict__ delta, float* __restrict__ dq_acc,
-                  void* __restrict__ dk_out, void* __restrict__ dv_out, int n, int npad, int ktiles,
-                  float scale, int causal, unsigned long long* err, unsigned long long* counter) {
+                  const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
+                  const float* __restrict__ delta, void* __restrict__ dk_out, void* __restrict__ dv_out, int n,
+                  int npad, int ktiles, float scale, int causal, unsigned long long* err) {
   using C = BwdCfg<D>;
+  constexpr int BM = C::BM;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -94,10 +110,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const ErrCtx ctx{err, abort_flag};
 
   const int head = blockIdx.x / ktiles;
-  const int kt = blockIdx.x - head * ktiles;  // heavy (early) key tiles first under causal
+  const int kt = blockIdx.x - head * ktiles;  // early key tiles carry the most causal work: launched first
   const int k0 = kt * BN;
   const int qtiles = (n + BM - 1) / BM;
-  const int i_start = causal ? kt : 0;  // BM == BN: query tile kt holds the diagonal
+  const int i_start = causal ? kt * (BN / BM) : 0;  // first query tile reaching this key tile's diagonal
   const int nsteps = qtiles - i_start;
   const float scale_log2 = scale * 1.4426950408889634f;
 
@@ -136,7 +152,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar + B_KV, 2 * C::TILE_BYTES);
+      mbar_arrive_expect_tx(bar + B_KV, 2 * C::KV_BYTES);
       for (int kb = 0; kb < C::KB; ++kb) {
         tma_load_3d(smem + C::OFF_K + kb * (BN * 128), &tm_k, bar + B_KV, kb * 64, k0, head);
         tma_load_3d(smem + C::OFF_V + kb * (BN * 128), &tm_v, bar + B_KV, kb * 64, k0, head);
@@ -147,10 +163,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (use > 0 && !mbar_wait(bar + B_QD_EMPTY + s, (use - 1) & 1, ctx, 110)) break;
         const int q0 = (i_start + i) * BM;
         uint64_t* fb = bar + B_QD_FULL + s;
-        mbar_arrive_expect_tx(fb, 2 * C::TILE_BYTES + 2 * BM * 4);
+        mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + 2 * BM * 4);
         for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(smem + C::OFF_Q + s * C::TILE_BYTES + kb * (BM * 128), &tm_q, fb, kb * 64, q0, head);
-          tma_load_3d(smem + C::OFF_DO + s * C::TILE_BYTES + kb * (BM * 128), &tm_do, fb, kb * 64, q0, head);
+          tma_load_3d(smem + C::OFF_Q + s * C::QT_BYTES + kb * (BM * 128), &tm_q, fb, kb * 64, q0, head);
+          tma_load_3d(smem + C::OFF_DO + s * C::QT_BYTES + kb * (BM * 128), &tm_do, fb, kb * 64, q0, head);
         }
         float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + s * 2 * BM;
         bulk_load(vec, lse2 + (int64_t)head * npad + q0, BM * 4, fb);
@@ -161,66 +177,81 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       int no_abort = 0;
       nctx.abort = &no_abort;
       mbar_wait(bar + B_KV, 0, nctx, 111);
-      for (int i = issued - 1; i >= 0 && i >= issued - 2; --i) mbar_wait(bar + B_QD_FULL + (i & 1), (i >> 1) & 1, nctx, 112);
+      for (int i = issued - 1; i >= 0 && i >= issued - 2; --i)
+        mbar_wait(bar + B_QD_FULL + (i & 1), (i >> 1) & 1, nctx, 112);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
     if (start_ok && lane == 0) {
-      const uint32_t idesc_s = make_idesc_f16(BN, BM, BF16, false, false);   // S^T, dP^T: M=keys, N=queries
-      const uint32_t idesc_kv = make_idesc_f16(BN, D, BF16, false, true);    // dV, dK: M=keys, N=d
-      const uint32_t idesc_q = make_idesc_f16(BM, D, BF16, true, true);      // dQ: M=queries (MN-major A)
+      const uint32_t idesc_s = make_idesc_f16(BN, BM, BF16, false, false);  // S^T, dP^T: M = keys, N = queries
+      const uint32_t idesc_kv = make_idesc_f16(BN, D, BF16, false, true);   // dV, dK: M = keys, N = d
+      const uint32_t idesc_q = C::DQT ? make_idesc_f16(D, BM, BF16, true, true)    // dQ^T: M = d, N = queries
+                                      : make_idesc_f16(BM, D, BF16, true, true);   // dQ: M = queries, N = d
       const uint32_t ks = smem_u32(smem + C::OFF_K), vs = smem_u32(smem + C::OFF_V);
       const uint32_t dss = smem_u32(smem + C::OFF_DS);
+      auto qs_of = [&](int s) { return smem_u32(smem + C::OFF_Q + s * C::QT_BYTES); };
+      auto dos_of = [&](int s) { return smem_u32(smem + C::OFF_DO + s * C::QT_BYTES); };
+      // K-major operand rows of 128 bytes in 64-column blocks: offset of K-slice kk (16 wide)
+      auto kmaj = [](int kk, int rows) { return (uint32_t)((kk * 16 / 64) * (rows * 128) + (kk * 16 % 64) * 2); };
+      // scores S^T = K Q_i^T and dP^T = V dO_i^T (A: 128 keys x d, B: BM queries x d, both K-major)
+      auto issue_scores = [&](uint32_t a, uint32_t b, uint32_t col) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tbase + col, make_sdesc_sw128(a + kmaj(kk, BN), 16, 1024), make_sdesc_sw128(b + kmaj(kk, BM), 16, 1024),
+                  idesc_s, kk > 0);
+      };
       bool ok = mbar_wait(bar + B_KV, 0, ctx, 120);
+      if (ok && nsteps > 0) {
+        ok = mbar_wait(bar + B_QD_FULL + 0, 0, ctx, 121);
+        if (ok) {
+          tc_fence_after();
+          issue_scores(ks, qs_of(0), C::COL_S);
+          umma_commit(bar + B_S_FULL);
+        }
+      }
       for (int i = 0; ok && i < nsteps; ++i) {
         const int s = i & 1;
-        const uint32_t qs = smem_u32(smem + C::OFF_Q + s * C::TILE_BYTES);
-        const uint32_t dos = smem_u32(smem + C::OFF_DO + s * C::TILE_BYTES);
-        if (!(ok = mbar_wait(bar + B_QD_FULL + s, (i >> 1) & 1, ctx, 121))) break;
-        tc_fence_after();
-        // S^T = K Q_i^T
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk * 16 / 64) * (BN * 128) + (kk * 16 % 64) * 2;
-          umma_ss(tbase + C::COL_S, make_sdesc_sw128(ks + off, 16, 1024), make_sdesc_sw128(qs + off, 16, 1024),
-                  idesc_s, kk > 0);
-        }
-        umma_commit(bar + B_S_FULL);
-        // dP^T = V dO_i^T (its columns held dQ_{i-1}: wait until that was read out)
-        if (i > 0) {
-          if (!(ok = mbar_wait(bar + B_DQ_FREE, (i - 1) & 1, ctx, 122))) break;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk * 16 / 64) * (BN * 128) + (kk * 16 % 64) * 2;
-          umma_ss(tbase + C::COL_DP, make_sdesc_sw128(vs + off, 16, 1024), make_sdesc_sw128(dos + off, 16, 1024),
-                  idesc_s, kk > 0);
-        }
+        const uint32_t qs = qs_of(s), dos = dos_of(s);
+        // dP^T_i (its columns were read out by WG0 before ds_ready(i-1))
+        issue_scores(vs, dos, C::COL_DP);
         umma_commit(bar + B_DP_FULL);
-        // dV += P^T dO_i (P^T from TMEM, K = queries)
+        // dV += P^T dO_i (P^T from TMEM, K = queries; dO_i as MN-major B)
         if (!(ok = mbar_wait(bar + B_P_READY, i & 1, ctx, 123))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           umma_ts(tbase + C::COL_DV, tbase + C::COL_S + kk * 8, make_sdesc_sw128(dos + kk * 2048, BM * 128, 1024),
                   idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_i (dS^T K-major in smem)
+        // S^T_{i+1}: overwrites P^T_i only after dV_i has read it (same issuing thread, in order)
+        if (i + 1 < nsteps) {
+          if (!(ok = mbar_wait(bar + B_QD_FULL + (s ^ 1), ((i + 1) >> 1) & 1, ctx, 121))) break;
+          tc_fence_after();
+          issue_scores(ks, qs_of(s ^ 1), C::COL_S);
+          umma_commit(bar + B_S_FULL);
+        }
+        // dK += dS^T Q_i (dS^T K-major in smem, Q_i MN-major)
         if (!(ok = mbar_wait(bar + B_DS_READY, i & 1, ctx, 124))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t off = (kk * 16 / 64) * (BN * 128) + (kk * 16 % 64) * 2;
-          umma_ss(tbase + C::COL_DK, make_sdesc_sw128(dss + off, 16, 1024),
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_ss(tbase + C::COL_DK, make_sdesc_sw128(dss + kmaj(kk, BN), 16, 1024),
                   make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024), idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
         umma_commit(bar + B_QD_EMPTY + s);
-        // dQ_i = dS K_j (dS read MN-major from the same buffer, K_j MN-major), into the dP^T columns
+        // dQ partial (previous one drained from TMEM first)
+        if (i > 0) {
+          if (!(ok = mbar_wait(bar + B_DQ_FREE, (i - 1) & 1, ctx, 122))) break;
+          tc_fence_after();
+        }
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ss(tbase + C::COL_DP, make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024),
-                  make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024), idesc_q, kk > 0);
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t kdesc = make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024);   // K as MN-major (d contiguous)
+          const uint64_t sdesc = make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024);  // dS^T as MN-major (queries contiguous)
+          if constexpr (C::DQT)
+            umma_ss(tbase + C::COL_DQ, kdesc, sdesc, idesc_q, kk > 0);
+          else
+            umma_ss(tbase + C::COL_DQ, sdesc, kdesc, idesc_q, kk > 0);
+        }
         umma_commit(bar + B_DQ_FULL);
       }
       if (ok) umma_commit(bar + B_ACC_FULL);
@@ -250,7 +281,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, i & 1, ctx, 130));
       if (!ok) break;
       tc_fence_after();
-      float p[BM];
+      // queries q0 + qc with qc < mask_below are in the past of this key (causal diagonal)
+      const int mask_below = causal ? key - q0 : 0;
+      // P^T row (this key against the BM queries), kept as packed 16-bit pairs: the same
+      // rounded values feed dV += P^T dO and dS = P o (dP - D)
+      uint32_t pk[BM / 2];
 #pragma unroll
       for (int c = 0; c < BM / 32; ++c) {
         uint32_t r[32];
@@ -258,26 +293,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tmem_wait_ld();
         reg_fence(r);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) p[c * 32 + t] = __uint_as_float(r[t]);
-      }
-      // queries q0 + c with c < mask_below are in the past of this key (causal diagonal)
-      const int mask_below = causal ? key - q0 : 0;
+        for (int t = 0; t < 32; t += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(l2v + c * 32 + t);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float e[4];
 #pragma unroll
-      for (int c = 0; c < BM; ++c) {
-        const float e = ex2(fmaf(p[c], scale_log2, -l2v[c]));
-        p[c] = (key_ok && c >= mask_below) ? e : 0.f;
+          for (int u = 0; u < 4; ++u) {
+            const int qc = c * 32 + t + u;
+            const float x = ex2(fmaf(__uint_as_float(r[t + u]), scale_log2, -lv[u]));
+            e[u] = (key_ok && qc >= mask_below) ? x : 0.f;
+          }
+          pk[(c * 32 + t) / 2] = pack2<BF16>(e[0], e[1]);
+          pk[(c * 32 + t) / 2 + 1] = pack2<BF16>(e[2], e[3]);
+        }
       }
 #pragma unroll
       for (int h = 0; h < BM / 64; ++h) {
-        uint32_t pk[32];
+        uint32_t w[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) pk[t] = pack2<BF16>(p[h * 64 + 2 * t], p[h * 64 + 2 * t + 1]);
-        tmem_st32(tmem_addr(tbase, lane_base, C::COL_S + h * 32), pk);
+        for (int t = 0; t < 32; ++t) w[t] = pk[h * 32 + t];
+        tmem_st32(tmem_addr(tbase, lane_base, C::COL_S + h * 32), w);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + B_P_READY);
-      // dS^T = P^T o (dP^T - D)
+      // dS^T = P^T o (dP^T - D); dp_full(i) also means the MMAs of step i-1 that read dS^T are done
       ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DP_FULL, i & 1, ctx, 131));
       if (!ok) break;
       tc_fence_after();
@@ -287,13 +327,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + c * 32), r);
         tmem_wait_ld();
         reg_fence(r);
-        uint32_t pk[16];
+        uint32_t dsk[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int qa = c * 32 + 2 * t;
-          const float d0 = p[qa] * (__uint_as_float(r[2 * t]) - dvec[qa]);
-          const float d1 = p[qa + 1] * (__uint_as_float(r[2 * t + 1]) - dvec[qa + 1]);
-          pk[t] = pack2<BF16>(d0, d1);
+        for (int t = 0; t < 16; t += 2) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dvec + c * 32 + 2 * t);
+          const float2 p01 = unpack2<BF16>(pk[c * 16 + t]);
+          const float2 p23 = unpack2<BF16>(pk[c * 16 + t + 1]);
+          dsk[t] = pack2<BF16>(p01.x * (__uint_as_float(r[2 * t]) - d4.x), p01.y * (__uint_as_float(r[2 * t + 1]) - d4.y));
+          dsk[t + 1] = pack2<BF16>(p23.x * (__uint_as_float(r[2 * t + 2]) - d4.z),
+                                   p23.y * (__uint_as_float(r[2 * t + 3]) - d4.w));
         }
         // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
         uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
@@ -301,7 +343,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int u = 0; u < 4; ++u) {
           const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
           *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+              make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
         }
       }
       fence_proxy_async_smem();
@@ -328,46 +370,73 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
             for (int t = 0; t < 16; ++t)
               pk[t] = pack2<BF16>(__uint_as_float(r[2 * t]) * f, __uint_as_float(r[2 * t + 1]) * f);
-            if (key_ok) store_row16<D, BF16>(dst, (int64_t)head * n + key, pk, c);
+            if (key_ok) store_row16<D>(dst, (int64_t)head * n + key, pk, c);
           }
         }
-        if (counter && rit == 0) atomicAdd(counter, (unsigned long long)nsteps);
       }
     } else if (ok && nsteps == 0 && key_ok) {
       // no query meets this key tile: zero gradients (not reachable for square causal masks)
       uint32_t pk[16] = {};
       for (int c = 0; c < D / 32; ++c) {
-        store_row16<D, BF16>(dk_out, (int64_t)head * n + key, pk, c);
-        store_row16<D, BF16>(dv_out, (int64_t)head * n + key, pk, c);
+        store_row16<D>(dk_out, (int64_t)head * n + key, pk, c);
+        store_row16<D>(dv_out, (int64_t)head * n + key, pk, c);
       }
     }
   } else if (warp < 8) {
-    // ------------------------------------------------------------------ WG1: drain dQ_i partials
+    // ------------------------------------------------------------------ WG1: drain dQ partials
+    // TMEM lane = d index (DQT) or query row; the partial goes to a staging tile in the layout
+    // of the dQ accumulator's tensor map and one thread adds it to global memory (TMA reduce).
     const uint32_t lane_base = (warp & 3) * 32;
-    const int rit = (warp & 3) * 32 + lane;  // query row within the tile
+    const int rr = (warp & 3) * 32 + lane;
+    const bool leader = (warp == 4 && lane == 0);
     bool ok = start_ok;
     for (int i = 0; ok && i < nsteps; ++i) {
       const int q0 = (i_start + i) * BM;
       ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, i & 1, ctx, 140));
       if (!ok) break;
       tc_fence_after();
-      float acc[D];
+      uint32_t v[64];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + c * 32), r);
+        tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + c * 32), r);
         tmem_wait_ld();
         reg_fence(r);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) acc[c * 32 + t] = __uint_as_float(r[t]);
+        for (int t = 0; t < 32; ++t) v[c * 32 + t] = r[t];
       }
       tc_fence_before();
       mbar_arrive(bar + B_DQ_FREE);
-      float4* dst = reinterpret_cast<float4*>(dq_acc + ((int64_t)head * npad + q0 + rit) * D);
+      uint8_t* stg = smem + C::OFF_STG + (i & 1) * C::STG_BYTES;
+      if (leader) bulk_wait_group_read<1>();  // the reduction that last used this tile has read it
+      named_bar_sync(1, 128);
+      if constexpr (C::DQT) {
+        // [BM queries][D] fp32, row-major: column rr (this thread's d) of each query row
+        float* st = reinterpret_cast<float*>(stg) + rr;
 #pragma unroll
-      for (int c = 0; c < D / 4; ++c)
-        atomicAdd(dst + c, make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]));
+        for (int q = 0; q < BM; ++q) st[q * D] = __uint_as_float(v[q]);
+      } else {
+        // [128 queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns; row rr
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          uint8_t* bx = stg + (j >> 3) * (BM * 128) + rr * 128;
+          *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ (uint32_t)(rr & 7)) << 4)) =
+              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (leader) {
+        if constexpr (C::DQT) {
+          tma_reduce_add_3d(&tm_dq, stg, 0, q0, head);
+        } else {
+          tma_reduce_add_3d(&tm_dq, stg, 0, q0, head);
+          tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, head);
+        }
+        bulk_commit_group();
+      }
     }
+    if (leader) bulk_wait_group<0>();  // every reduction issued here has completed
   }
 
   tc_fence_before();
@@ -381,19 +450,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 template <int D, bool BF16>
 cudaError_t launch_bwd_d(const BwdArgs& a) {
   using C = BwdCfg<D>;
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, a.bh, BN) ||
+  const int npad = (int)padded_rows(a.n);
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, C::BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, a.bh, BN) ||
       !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, a.bh, BN) ||
-      !make_tmap_16bit_3d(&tdo, a.dout, BF16, D, a.n, a.bh, BM))
+      !make_tmap_16bit_3d(&tdo, a.dout, BF16, D, a.n, a.bh, C::BM) ||
+      !make_tmap_f32_3d(&tdq, a.dq_acc, D, npad, a.bh, C::DQT ? D : 32, C::BM, !C::DQT))
     return cudaErrorInvalidValue;
   auto kern = bwd_tc_kernel<D, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int ktiles = (a.n + BN - 1) / BN;
-  const int npad = (int)padded_rows(a.n);
-  kern<<<(unsigned)(a.bh * ktiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, tdo, a.lse2, a.delta, a.dq_acc, a.dk,
-                                                                      a.dv, a.n, npad, ktiles, a.scale, a.causal,
-                                                                      a.err, a.counter);
+  kern<<<(unsigned)(a.bh * ktiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq, a.lse2, a.delta, a.dk, a.dv,
+                                                                      a.n, npad, ktiles, a.scale, a.causal, a.err);
   return cudaGetLastError();
 }
 

@@ -38,4 +38,20 @@ inline bool make_tmap_16bit_3d(CUtensorMap* map, const void* base, bool bf16, ui
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a [heads][rows][cols] row-major fp32 array, boxes of box_cols x box_rows,
+// optionally with the 128-byte swizzle (then box_cols * 4 must be 128).
+inline bool make_tmap_f32_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t heads,
+                             uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, heads};
+  cuuint64_t strides[2] = {cols * 4, cols * rows * 4};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa

@@ -121,9 +121,10 @@ FA_API fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes
 FA_API fa_status fa_check_device_error(void* stream);
 
 /*
- * Diagnostic: number of (query tile, key tile) pairs of 128 x 128 the tensor-core
- * kernels (and of 32 x 32 the CUDA-core forward) processed on the current device since
- * the last reset. Synchronises `stream`; reset != 0 clears the counter afterwards.
+ * Diagnostic: number of (query tile, key tile) pairs the forward kernels processed on the
+ * current device since the last reset (128 x 128 tiles on the tensor-core path, 32 x 32 on
+ * the CUDA-core path); skipped causal tiles are not counted. Synchronises `stream`;
+ * reset != 0 clears the counter afterwards.
  */
 FA_API fa_status fa_tile_counter(void* stream, unsigned long long* value, int reset);
 
