@@ -19,18 +19,20 @@ __all__ = [
     "FAError", "library_path", "load_library", "DTYPE_CODES",
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
-    "fa_last_error_message", "attention_forward", "attention_backward", "EXPORTED_SYMBOLS",
+    "fa_last_error_message", "fa_bwd_noalloc", "attention_forward", "attention_backward", "EXPORTED_SYMBOLS",
+    "NOALLOC_SCRATCH_BYTES",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_FILE = "libfa_gb300.so"
 
 FA_OK = 0
+NOALLOC_SCRATCH_BYTES = 64 << 20  # FA_BWD_NOALLOC_SCRATCH_BYTES in include/fa.h
 DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 EXPORTED_SYMBOLS = (
     "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
-    "fa_last_error_message",
+    "fa_last_error_message", "fa_bwd_noalloc",
 )
 
 _lib = None
@@ -67,6 +69,7 @@ def load_library():
         lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, i, vp]
         lib.fa_bwd_main.argtypes = [vp] * 7 + [sz, i, i, i, i, f, i, i, vp]
         lib.fa_bwd_dq_convert.argtypes = [vp, sz, vp, i, i, i, i, f, i, vp]
+        lib.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, f, i, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
         lib.fa_uses_tensor_cores.argtypes = [i, i, i]
@@ -74,7 +77,7 @@ def load_library():
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_error_message.argtypes = []
         lib.fa_last_error_message.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
+        for name in ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
                      "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -162,6 +165,14 @@ def fa_bwd_dq_convert(workspace, dQ, scale, stream=None):
     B, H, N, d = _shape4(dQ)
     _check(load_library().fa_bwd_dq_convert(_p(workspace), workspace.numel() * workspace.element_size(), _p(dQ),
                                             B, H, N, d, float(scale), _dt(dQ), _stream(stream)))
+
+
+def fa_bwd_noalloc(Q, K, V, O, dO, L, dQ, dK, dV, scale, causal, stream=None):
+    """fa_bwd with the library's static device scratch instead of a workspace (no allocation)."""
+    B, H, N, d = _shape4(Q)
+    _same(Q, K, V, O, dO, dQ, dK, dV)
+    _check(load_library().fa_bwd_noalloc(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV), B, H, N,
+                                         d, float(scale), int(bool(causal)), _dt(Q), _stream(stream)))
 
 
 def fa_check_device_error(stream=None):

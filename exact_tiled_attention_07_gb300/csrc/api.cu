@@ -116,6 +116,15 @@ fa_status carve(BwdArgs* a, void* ws, size_t ws_bytes, int B, int H, int N, int 
 }
 
 }  // namespace
+
+int set_last_error(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
 }  // namespace fa
 
 using namespace fa;

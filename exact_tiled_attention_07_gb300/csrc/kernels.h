@@ -55,6 +55,10 @@ struct BwdArgs {
   cudaStream_t stream;
 };
 
+// Records the calling thread's last error message (read by fa_last_error_message) and
+// returns `status`.
+int set_last_error(int status, const char* fmt, ...);
+
 bool fwd_tc_supported(int dtype, int d);
 bool bwd_tc_supported(int dtype, int d);
 

@@ -114,6 +114,32 @@ FA_API fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes
                             float scale, fa_dtype dtype, void* stream);
 
 /*
+ * Backward pass for callers that cannot allocate device memory: the same computation and
+ * arguments as fa_bwd, without `workspace`. (The pages have no counterpart of this entry
+ * point; it exists for the library's callers.)
+ *
+ * Some callers cannot provide a workspace: code inside a host application that owns every
+ * device allocation (a plugin or runtime with its own memory pool), or a latency-bound
+ * loop that cannot afford cudaMalloc's implicit device synchronisation. This entry point
+ * takes its scratch from a static device array of FA_BWD_NOALLOC_SCRATCH_BYTES that the
+ * library holds on every GPU where it is loaded, until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Limit     fa_bwd_workspace_size(B, H, N, d) must not exceed FA_BWD_NOALLOC_SCRATCH_BYTES;
+ *             larger problems return FA_ERR_INVALID_ARG and launch nothing.
+ *   Set-up    The first call on a device looks up the array's device address
+ *             (cudaGetSymbolAddress) with that device current; make that first call
+ *             before any stream capture.
+ *   Sharing   Every call uses the same array and leaves its contents behind; each call
+ *             re-initialises what it reads. Calls whose kernels overlap on the GPU
+ *             (different streams or host threads) race on the array: serialise them.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64ull << 20)
+FA_API fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale,
+                                int causal, fa_dtype dtype, void* stream);
+
+/*
  * Synchronises `stream` and reports device-side failures of earlier calls on the
  * current device: FA_ERR_CUDA for a CUDA error, FA_ERR_TIMEOUT / FA_ERR_DEVICE for a
  * failure a kernel recorded. The recorded failure is cleared.
