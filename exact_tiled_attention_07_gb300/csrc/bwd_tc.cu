@@ -10,7 +10,7 @@
 //
 // One CTA owns a 128-key tile of one head for its whole life: K_j, V_j stay in shared
 // memory and the dK_j, dV_j accumulators stay in TMEM, while query tiles (Q_i, dO_i, L_i,
-// D_i) stream through a two-stage TMA ring.  Working transposed puts keys on TMEM lanes, so
+// D_i) stream through a three-stage TMA ring.  Working transposed puts keys on TMEM lanes, so
 // one thread owns one key row: P^T and dS^T need no cross-thread reduction.  P^T goes back
 // into TMEM as the A operand of dV += P^T dO; dS^T goes to shared memory, where the same
 // swizzled bytes feed dK += dS^T Q and the dQ GEMM.
@@ -55,12 +55,13 @@ struct BwdCfg {
   static constexpr int MMA_WARP = 9;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;       // [2] stages
-  static constexpr int OFF_DO = OFF_Q + 2 * QT_BYTES;  // [2] stages
-  static constexpr int OFF_DS = OFF_DO + 2 * QT_BYTES;
-  static constexpr int OFF_STG = OFF_DS + DS_BYTES;    // [2] staging tiles
-  static constexpr int OFF_VEC = OFF_STG + 2 * STG_BYTES;  // [2] stages x (L2[BM], D[BM]) fp32
-  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * BM * 4;
+  static constexpr int QSTAGES = 3;                          // query-tile ring depth
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;                 // [QSTAGES]
+  static constexpr int OFF_DO = OFF_Q + QSTAGES * QT_BYTES;      // [QSTAGES]
+  static constexpr int OFF_DS = OFF_DO + QSTAGES * QT_BYTES;
+  static constexpr int OFF_STG = OFF_DS + DS_BYTES;              // dQ staging tile
+  static constexpr int OFF_VEC = OFF_STG + STG_BYTES;            // [QSTAGES] x (L2[BM], D[BM]) fp32
+  static constexpr int OFF_BAR = OFF_VEC + QSTAGES * 2 * BM * 4;
   static constexpr int NBAR = 16;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   // TMEM columns
@@ -73,16 +74,16 @@ struct BwdCfg {
 
 enum BwdBar {
   B_KV = 0,
-  B_QD_FULL = 1,   // [2]
-  B_QD_EMPTY = 3,  // [2]
-  B_S_FULL = 5,
-  B_DP_FULL = 6,
-  B_P_READY = 7,
-  B_DS_READY = 8,
-  B_DQ_FULL = 9,
-  B_DQ_FREE = 10,
-  B_ACC_FULL = 11,
-  B_DRAIN = 12,
+  B_QD_FULL = 1,   // [3]
+  B_QD_EMPTY = 4,  // [3]
+  B_S_FULL = 7,
+  B_DP_FULL = 8,
+  B_P_READY = 9,
+  B_DS_READY = 10,
+  B_DQ_FULL = 11,
+  B_DQ_FREE = 12,
+  B_ACC_FULL = 13,
+  B_DRAIN = 14,
 };
 
 template <int D>
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if ((smem_u32(smem) & 1023u) != 0) report_error(err, DERR_BAD_SMEM_ALIGN, 1);
     *abort_flag = (smem_u32(smem) & 1023u) != 0;
     mbar_init(bar + B_KV, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::QSTAGES; ++s) {
       mbar_init(bar + B_QD_FULL + s, 1);
       mbar_init(bar + B_QD_EMPTY + s, 1);
     }
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       int issued = 0;
       for (int i = 0; i < nsteps; ++i) {
-        const int s = i & 1, use = i >> 1;
+        const int s = i % C::QSTAGES, use = i / C::QSTAGES;
         if (use > 0 && !mbar_wait(bar + B_QD_EMPTY + s, (use - 1) & 1, ctx, 110)) break;
         const int q0 = (i_start + i) * BM;
         uint64_t* fb = bar + B_QD_FULL + s;
@@ -177,13 +178,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       int no_abort = 0;
       nctx.abort = &no_abort;
       mbar_wait(bar + B_KV, 0, nctx, 111);
-      for (int i = issued - 1; i >= 0 && i >= issued - 2; --i)
-        mbar_wait(bar + B_QD_FULL + (i & 1), (i >> 1) & 1, nctx, 112);
+      for (int i = issued - 1; i >= 0 && i >= issued - C::QSTAGES; --i)
+        mbar_wait(bar + B_QD_FULL + i % C::QSTAGES, (i / C::QSTAGES) & 1, nctx, 112);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
-    if (start_ok && lane == 0) {
+    // The whole warp runs this loop converged, so the smem descriptors are warp-uniform;
+    // one elected lane issues every MMA and commit (a commit tracks its own lane's MMAs).
+    if (start_ok) {
+      const bool leader = elect_one_sync();
       const uint32_t idesc_s = make_idesc_f16(BN, BM, BF16, false, false);  // S^T, dP^T: M = keys, N = queries
       const uint32_t idesc_kv = make_idesc_f16(BN, D, BF16, false, true);   // dV, dK: M = keys, N = d
       const uint32_t idesc_q = C::DQT ? make_idesc_f16(D, BM, BF16, true, true)    // dQ^T: M = d, N = queries
@@ -192,73 +196,115 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint32_t dss = smem_u32(smem + C::OFF_DS);
       auto qs_of = [&](int s) { return smem_u32(smem + C::OFF_Q + s * C::QT_BYTES); };
       auto dos_of = [&](int s) { return smem_u32(smem + C::OFF_DO + s * C::QT_BYTES); };
+      auto wait = [&](uint64_t* b, uint32_t parity, uint32_t site) {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, ctx, site));
+      };
+      auto commit = [&](uint64_t* b) {
+        if (leader) umma_commit(b);
+        __syncwarp();
+      };
       // K-major operand rows of 128 bytes in 64-column blocks: offset of K-slice kk (16 wide)
       auto kmaj = [](int kk, int rows) { return (uint32_t)((kk * 16 / 64) * (rows * 128) + (kk * 16 % 64) * 2); };
       // scores S^T = K Q_i^T and dP^T = V dO_i^T (A: 128 keys x d, B: BM queries x d, both K-major)
       auto issue_scores = [&](uint32_t a, uint32_t b, uint32_t col) {
+        uint64_t ad[D / 16], bd[D / 16];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tbase + col, make_sdesc_sw128(a + kmaj(kk, BN), 16, 1024), make_sdesc_sw128(b + kmaj(kk, BM), 16, 1024),
-                  idesc_s, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          ad[kk] = make_sdesc_sw128(a + kmaj(kk, BN), 16, 1024);
+          bd[kk] = make_sdesc_sw128(b + kmaj(kk, BM), 16, 1024);
+        }
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + col, ad[kk], bd[kk], idesc_s, kk > 0);
+        }
+        __syncwarp();
       };
-      bool ok = mbar_wait(bar + B_KV, 0, ctx, 120);
+      bool ok = wait(bar + B_KV, 0, 120);
       if (ok && nsteps > 0) {
-        ok = mbar_wait(bar + B_QD_FULL + 0, 0, ctx, 121);
+        ok = wait(bar + B_QD_FULL + 0, 0, 121);
         if (ok) {
           tc_fence_after();
           issue_scores(ks, qs_of(0), C::COL_S);
-          umma_commit(bar + B_S_FULL);
+          commit(bar + B_S_FULL);
         }
       }
       for (int i = 0; ok && i < nsteps; ++i) {
-        const int s = i & 1;
+        const int s = i % C::QSTAGES;
+        const int s1 = (i + 1) % C::QSTAGES;
         const uint32_t qs = qs_of(s), dos = dos_of(s);
-        // dP^T_i (its columns were read out by WG0 before ds_ready(i-1))
+        // dP^T_i (its columns were read out by the P/dS warps before ds_ready(i-1))
         issue_scores(vs, dos, C::COL_DP);
-        umma_commit(bar + B_DP_FULL);
+        commit(bar + B_DP_FULL);
         // dV += P^T dO_i (P^T from TMEM, K = queries; dO_i as MN-major B)
-        if (!(ok = mbar_wait(bar + B_P_READY, i & 1, ctx, 123))) break;
-        tc_fence_after();
+        {
+          uint64_t bd[BM / 16];
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts(tbase + C::COL_DV, tbase + C::COL_S + kk * 8, make_sdesc_sw128(dos + kk * 2048, BM * 128, 1024),
-                  idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
-        // S^T_{i+1}: overwrites P^T_i only after dV_i has read it (same issuing thread, in order)
-        if (i + 1 < nsteps) {
-          if (!(ok = mbar_wait(bar + B_QD_FULL + (s ^ 1), ((i + 1) >> 1) & 1, ctx, 121))) break;
+          for (int kk = 0; kk < BM / 16; ++kk) bd[kk] = make_sdesc_sw128(dos + kk * 2048, BM * 128, 1024);
+          if (!(ok = wait(bar + B_P_READY, i & 1, 123))) break;
           tc_fence_after();
-          issue_scores(ks, qs_of(s ^ 1), C::COL_S);
-          umma_commit(bar + B_S_FULL);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < BM / 16; ++kk)
+              umma_ts(tbase + C::COL_DV, tbase + C::COL_S + kk * 8, bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          __syncwarp();
+        }
+        // S^T_{i+1}: overwrites P^T_i only after dV_i has read it (same issuing lane, in order)
+        if (i + 1 < nsteps) {
+          if (!(ok = wait(bar + B_QD_FULL + s1, ((i + 1) / C::QSTAGES) & 1, 121))) break;
+          tc_fence_after();
+          issue_scores(ks, qs_of(s1), C::COL_S);
+          commit(bar + B_S_FULL);
         }
         // dK += dS^T Q_i (dS^T K-major in smem, Q_i MN-major)
-        if (!(ok = mbar_wait(bar + B_DS_READY, i & 1, ctx, 124))) break;
-        tc_fence_after();
+        {
+          uint64_t ad[BM / 16], bd[BM / 16];
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ss(tbase + C::COL_DK, make_sdesc_sw128(dss + kmaj(kk, BN), 16, 1024),
-                  make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024), idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar + B_QD_EMPTY + s);
-        // dQ partial (previous one drained from TMEM first)
-        if (i > 0) {
-          if (!(ok = mbar_wait(bar + B_DQ_FREE, (i - 1) & 1, ctx, 122))) break;
+          for (int kk = 0; kk < BM / 16; ++kk) {
+            ad[kk] = make_sdesc_sw128(dss + kmaj(kk, BN), 16, 1024);
+            bd[kk] = make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024);
+          }
+          if (!(ok = wait(bar + B_DS_READY, i & 1, 124))) break;
           tc_fence_after();
-        }
+          if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t kdesc = make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024);   // K as MN-major (d contiguous)
-          const uint64_t sdesc = make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024);  // dS^T as MN-major (queries contiguous)
-          if constexpr (C::DQT)
-            umma_ss(tbase + C::COL_DQ, kdesc, sdesc, idesc_q, kk > 0);
-          else
-            umma_ss(tbase + C::COL_DQ, sdesc, kdesc, idesc_q, kk > 0);
+            for (int kk = 0; kk < BM / 16; ++kk)
+              umma_ss(tbase + C::COL_DK, ad[kk], bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          __syncwarp();
         }
-        umma_commit(bar + B_DQ_FULL);
+        commit(bar + B_QD_EMPTY + s);
+        // dQ partial (the previous one drained from TMEM first)
+        {
+          uint64_t kd[BN / 16], sd[BN / 16];
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            kd[kk] = make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024);   // K as MN-major (d contiguous)
+            sd[kk] = make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024);  // dS^T as MN-major (queries contiguous)
+          }
+          if (i > 0) {
+            if (!(ok = wait(bar + B_DQ_FREE, (i - 1) & 1, 122))) break;
+            tc_fence_after();
+          }
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              if constexpr (C::DQT)
+                umma_ss(tbase + C::COL_DQ, kd[kk], sd[kk], idesc_q, kk > 0);
+              else
+                umma_ss(tbase + C::COL_DQ, sd[kk], kd[kk], idesc_q, kk > 0);
+            }
+          }
+          __syncwarp();
+        }
+        commit(bar + B_DQ_FULL);
       }
-      if (ok) umma_commit(bar + B_ACC_FULL);
+      if (ok) commit(bar + B_ACC_FULL);
+      // drain: all MMAs complete before TMEM is released
       ErrCtx nctx = ctx;
       int no_abort = 0;
       nctx.abort = &no_abort;
-      umma_commit(bar + B_DRAIN);
+      commit(bar + B_DRAIN);
       mbar_wait(bar + B_DRAIN, 0, nctx, 125);
     }
     __syncwarp();
@@ -272,12 +318,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t sw = (uint32_t)(rit & 7);
     bool ok = start_ok;
     for (int i = 0; ok && i < nsteps; ++i) {
-      const int s = i & 1;
+      const int s = i % C::QSTAGES;
       const int q0 = (i_start + i) * BM;
       const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
       const float* dvec = l2v + BM;
       // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (i >> 1) & 1, ctx, 133));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (i / C::QSTAGES) & 1, ctx, 133));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, i & 1, ctx, 130));
       if (!ok) break;
       tc_fence_after();
@@ -287,10 +333,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // rounded values feed dV += P^T dO and dS = P o (dP - D)
       uint32_t pk[BM / 2];
 #pragma unroll
-      for (int c = 0; c < BM / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + c * 32), r);
-        tmem_wait_ld();
+      for (int g = 0; g < BM / 64; ++g) {  // 64 columns per batch of TMEM loads
+      uint32_t sr[2][32];
+      tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + g * 64), sr[0]);
+      tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + g * 64 + 32), sr[1]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = g * 2 + cc;
+        uint32_t(&r)[32] = sr[cc];
         reg_fence(r);
 #pragma unroll
         for (int t = 0; t < 32; t += 4) {
@@ -307,6 +358,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           pk[(c * 32 + t) / 2 + 1] = pack2<BF16>(e[2], e[3]);
         }
       }
+      }
 #pragma unroll
       for (int h = 0; h < BM / 64; ++h) {
         uint32_t w[32];
@@ -322,10 +374,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < BM / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + c * 32), r);
-        tmem_wait_ld();
+      for (int g = 0; g < BM / 64; ++g) {  // 64 columns per batch of TMEM loads
+      uint32_t dr[2][32];
+      tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + g * 64), dr[0]);
+      tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + g * 64 + 32), dr[1]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = g * 2 + cc;
+        uint32_t(&r)[32] = dr[cc];
         reg_fence(r);
         uint32_t dsk[16];
 #pragma unroll
@@ -345,6 +402,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
               make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
         }
+      }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -395,20 +453,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, i & 1, ctx, 140));
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[64];
+      uint32_t vr[2][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + c * 32), r);
-        tmem_wait_ld();
-        reg_fence(r);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) v[c * 32 + t] = r[t];
-      }
+      for (int c = 0; c < 2; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + c * 32), vr[c]);
+      tmem_wait_ld();
+      reg_fence(vr[0]);
+      reg_fence(vr[1]);
+      const uint32_t* v = &vr[0][0];
       tc_fence_before();
       mbar_arrive(bar + B_DQ_FREE);
-      uint8_t* stg = smem + C::OFF_STG + (i & 1) * C::STG_BYTES;
-      if (leader) bulk_wait_group_read<1>();  // the reduction that last used this tile has read it
+      uint8_t* stg = smem + C::OFF_STG;
+      if (leader) bulk_wait_group_read<0>();  // the previous reduction has finished reading the tile
       named_bar_sync(1, 128);
       if constexpr (C::DQT) {
         // [BM queries][D] fp32, row-major: column rr (this thread's d) of each query row

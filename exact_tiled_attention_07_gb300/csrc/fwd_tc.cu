@@ -181,53 +181,70 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
-    if (start_ok && lane == 0) {
+    // The whole warp runs this converged, so descriptors are warp-uniform; one elected lane
+    // issues every MMA and commit (a commit tracks the MMAs of its own lane).
+    if (start_ok) {
+      const bool leader = elect_one_sync();
       const uint32_t idesc_qk = make_idesc_f16(BM, BN, BF16, false, false);
       const uint32_t idesc_pv = make_idesc_f16(BM, D, BF16, false, true);
       const uint32_t q_base = smem_u32(smem + C::OFF_Q);
       const uint32_t ring = smem_u32(smem + C::OFF_RING);
       auto slot_of = [&](int idx) { return idx % C::STAGES; };
-      auto wait_full = [&](int idx) {
-        return mbar_wait(B.kv_full + slot_of(idx), (idx / C::STAGES) & 1, ctx, 20);
+      auto wait = [&](uint64_t* b, uint32_t parity, uint32_t site) {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, ctx, site));
+      };
+      auto wait_full = [&](int idx) { return wait(B.kv_full + slot_of(idx), (idx / C::STAGES) & 1, 20); };
+      auto commit = [&](uint64_t* b) {
+        if (leader) umma_commit(b);
+        __syncwarp();
       };
       // S = Q_q K^T into TMEM columns s_col
       auto issue_qk = [&](int q, int kidx, uint32_t s_col) {
         const uint32_t kt = ring + slot_of(kidx) * C::TILE_BYTES;
         const uint32_t qt = q_base + q * C::Q_BYTES;
+        uint64_t ad[D / 16], bd[D / 16];
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int k0 = kk * 16;
-          const uint32_t off = (k0 / 64) * (BM * 128) + (k0 % 64) * 2;
-          const uint32_t offk = (k0 / 64) * (BN * 128) + (k0 % 64) * 2;
-          umma_ss(tbase + s_col, make_sdesc_sw128(qt + off, 16, 1024), make_sdesc_sw128(kt + offk, 16, 1024),
-                  idesc_qk, kk > 0);
+          ad[kk] = make_sdesc_sw128(qt + (k0 / 64) * (BM * 128) + (k0 % 64) * 2, 16, 1024);
+          bd[kk] = make_sdesc_sw128(kt + (k0 / 64) * (BN * 128) + (k0 % 64) * 2, 16, 1024);
         }
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + s_col, ad[kk], bd[kk], idesc_qk, kk > 0);
+        }
+        __syncwarp();
       };
       // O += P V with P (16-bit, packed pairs) in TMEM columns [p_col, p_col + 64)
       auto issue_pv = [&](uint32_t o_col, uint32_t p_col, int vidx, bool acc) {
         const uint32_t vt = ring + slot_of(vidx) * C::TILE_BYTES;
+        uint64_t bd[BN / 16];
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ts(tbase + o_col, tbase + p_col + kk * 8, make_sdesc_sw128(vt + kk * 2048, BN * 128, 1024),
-                  idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BN / 16; ++kk) bd[kk] = make_sdesc_sw128(vt + kk * 2048, BN * 128, 1024);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_ts(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
       };
-      bool ok = mbar_wait(B.q_full, 0, ctx, 21);
+      bool ok = wait(B.q_full, 0, 21);
       if (ok) tc_fence_after();
       if constexpr (C::NQ == 2) {
         if (ok && nmax > 0) {
           ok = wait_full(0);
           if (ok) {
             tc_fence_after();
-            if (nq[0] > 0) { issue_qk(0, 0, C::S_COL0); umma_commit(B.s_full + 0); }
-            if (nq[1] > 0) { issue_qk(1, 0, C::S_COL1); umma_commit(B.s_full + 1); }
-            umma_commit(B.kv_empty + slot_of(0));
+            if (nq[0] > 0) { issue_qk(0, 0, C::S_COL0); commit(B.s_full + 0); }
+            if (nq[1] > 0) { issue_qk(1, 0, C::S_COL1); commit(B.s_full + 1); }
+            commit(B.kv_empty + slot_of(0));
           }
         }
         for (int j = 0; ok && j < nmax; ++j) {
           const int vidx = 2 * j + 1, kidx = 2 * j + 2;
           if (!(ok = wait_full(vidx))) break;
           if (j < nq[0]) {
-            if (!(ok = mbar_wait(B.p_full + 0, j & 1, ctx, 22))) break;
+            if (!(ok = wait(B.p_full + 0, j & 1, 22))) break;
             tc_fence_after();
             issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
           }
@@ -235,17 +252,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (!(ok = wait_full(kidx))) break;
             tc_fence_after();
           }
-          if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); umma_commit(B.s_full + 0); }
+          if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); commit(B.s_full + 0); }
           if (j < nq[1]) {
-            if (!(ok = mbar_wait(B.p_full + 1, j & 1, ctx, 23))) break;
+            if (!(ok = wait(B.p_full + 1, j & 1, 23))) break;
             tc_fence_after();
             issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
           }
-          umma_commit(B.kv_empty + slot_of(vidx));
-          if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); umma_commit(B.s_full + 1); }
-          if (j + 1 < nmax) umma_commit(B.kv_empty + slot_of(kidx));
-          if (j == nq[0] - 1) umma_commit(B.o_full + 0);
-          if (j == nq[1] - 1) umma_commit(B.o_full + 1);
+          commit(B.kv_empty + slot_of(vidx));
+          if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); commit(B.s_full + 1); }
+          if (j + 1 < nmax) commit(B.kv_empty + slot_of(kidx));
+          if (j == nq[0] - 1) commit(B.o_full + 0);
+          if (j == nq[1] - 1) commit(B.o_full + 1);
         }
       } else {
         // NQ == 1: S double-buffered in columns 0 / 128, O at 256
@@ -255,35 +272,35 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (!(ok = wait_full(2 * j))) break;
             tc_fence_after();
             issue_qk(0, 2 * j, j ? C::S_COL1 : C::S_COL0);
-            umma_commit(B.s_full + j);
-            umma_commit(B.kv_empty + slot_of(2 * j));
+            commit(B.s_full + j);
+            commit(B.kv_empty + slot_of(2 * j));
           }
         }
         for (int j = 0; ok && j < nb; ++j) {
           const int vidx = 2 * j + 1;
           const uint32_t buf = (j & 1) ? C::S_COL1 : C::S_COL0;
           if (!(ok = wait_full(vidx))) break;
-          if (!(ok = mbar_wait(B.p_full + 0, j & 1, ctx, 24))) break;
+          if (!(ok = wait(B.p_full + 0, j & 1, 24))) break;
           tc_fence_after();
           issue_pv(C::O_COL0, buf, vidx, j > 0);
-          umma_commit(B.pv_done);
-          umma_commit(B.kv_empty + slot_of(vidx));
+          commit(B.pv_done);
+          commit(B.kv_empty + slot_of(vidx));
           if (j + 2 < nb) {
             const int kidx = 2 * (j + 2);
             if (!(ok = wait_full(kidx))) break;
             tc_fence_after();
             issue_qk(0, kidx, buf);
-            umma_commit(B.s_full + (j & 1));
-            umma_commit(B.kv_empty + slot_of(kidx));
+            commit(B.s_full + (j & 1));
+            commit(B.kv_empty + slot_of(kidx));
           }
-          if (j == nb - 1) umma_commit(B.o_full + 0);
+          if (j == nb - 1) commit(B.o_full + 0);
         }
       }
       // drain: all MMAs complete before TMEM is released
       ErrCtx nctx = ctx;
       int no_abort = 0;
       nctx.abort = &no_abort;
-      umma_commit(B.drain);
+      commit(B.drain);
       mbar_wait(B.drain, 0, nctx, 25);
     }
     __syncwarp();
@@ -315,16 +332,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(sbar, sparity, ctx, 30 + q));
       if (!ok) break;
       tc_fence_after();
+      // whole S row: all TMEM loads in flight before one wait
+      uint32_t sr[BN / 32][32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, s_col + c * 32), sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
       float s[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tbase, lane_base, s_col + c * 32), r);
-        tmem_wait_ld();
-        reg_fence(r);
+      for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-      }
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
       // mask: keys past N, and (causal) keys after this row
       int limit = n - j * BN;
       if (causal) limit = min(limit, row - j * BN + 1);

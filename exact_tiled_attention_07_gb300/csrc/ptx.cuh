@@ -48,7 +48,17 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
-__device__ __forceinline__ bool elect_one() { return lane_id() == 0; }
+// One lane of a converged warp (elect.sync); the same lane every time the full warp calls it.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
+      "elect.sync rx|px, %1;\n\t"
+      "@px mov.s32 %0, 1;\n\t}"
+      : "+r"(pred)
+      : "r"(0xffffffffu));
+  return pred != 0;
+}
 
 // ---------------------------------------------------------------------------
 // mbarrier
