@@ -11,9 +11,10 @@
 // One CTA owns a 128-key tile of one head for its whole life: K_j, V_j stay in shared
 // memory and the dK_j, dV_j accumulators stay in TMEM, while query tiles (Q_i, dO_i, L_i,
 // D_i) stream through a three-stage TMA ring.  Working transposed puts keys on TMEM lanes, so
-// one thread owns one key row: P^T and dS^T need no cross-thread reduction.  P^T goes back
-// into TMEM as the A operand of dV += P^T dO; dS^T goes to shared memory, where the same
-// swizzled bytes feed dK += dS^T Q and the dQ GEMM.
+// one thread owns one key row: P^T and dS^T need no cross-thread reduction.  K_j, P^T and
+// dS^T sit in TMEM as A operands (S^T = K Q^T, dV += P^T dO, dK += dS^T Q), which spares
+// the shared-memory read of A that an all-smem MMA pays; dS^T also goes to shared memory
+// as an operand of the dQ GEMM.
 //
 // dQ partials are summed over key tiles in an fp32 accumulator in global memory.  A second
 // warpgroup drains each partial from TMEM into a shared-memory staging tile and one thread
@@ -64,10 +65,12 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_VEC + QSTAGES * 2 * BM * 4;
   static constexpr int NBAR = 16;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
-  // TMEM columns
-  static constexpr uint32_t COL_S = 0;
-  static constexpr uint32_t COL_DP = BM;
-  static constexpr uint32_t COL_DQ = 2 * BM;
+  // TMEM columns: K_j as a 16-bit A operand (d/2 columns), S^T (P^T over its first BM/2),
+  // dP^T (dS^T over its first BM/2), the dQ partial and the dV, dK accumulators
+  static constexpr uint32_t COL_K = DQT ? 0 : 448;
+  static constexpr uint32_t COL_S = DQT ? 64 : 0;
+  static constexpr uint32_t COL_DP = COL_S + BM;
+  static constexpr uint32_t COL_DQ = COL_DP + BM;
   static constexpr uint32_t COL_DV = DQT ? 256 : 320;
   static constexpr uint32_t COL_DK = 384;
 };
@@ -84,6 +87,7 @@ enum BwdBar {
   B_DQ_FREE = 12,
   B_ACC_FULL = 13,
   B_DRAIN = 14,
+  B_KT_READY = 15,  // K_j copied into TMEM
 };
 
 template <int D>
@@ -134,6 +138,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar + B_DQ_FREE, 128);
     mbar_init(bar + B_ACC_FULL, 1);
     mbar_init(bar + B_DRAIN, 1);
+    mbar_init(bar + B_KT_READY, 128);
     fence_barrier_init();
   }
   if (warp == C::MMA_WARP) {
@@ -205,26 +210,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       };
       // K-major operand rows of 128 bytes in 64-column blocks: offset of K-slice kk (16 wide)
       auto kmaj = [](int kk, int rows) { return (uint32_t)((kk * 16 / 64) * (rows * 128) + (kk * 16 % 64) * 2); };
-      // scores S^T = K Q_i^T and dP^T = V dO_i^T (A: 128 keys x d, B: BM queries x d, both K-major)
-      auto issue_scores = [&](uint32_t a, uint32_t b, uint32_t col) {
+      // dP^T = V dO_i^T (A: 128 keys x d, B: BM queries x d, both K-major in smem)
+      auto issue_dp = [&](uint32_t b) {
         uint64_t ad[D / 16], bd[D / 16];
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          ad[kk] = make_sdesc_sw128(a + kmaj(kk, BN), 16, 1024);
+          ad[kk] = make_sdesc_sw128(vs + kmaj(kk, BN), 16, 1024);
           bd[kk] = make_sdesc_sw128(b + kmaj(kk, BM), 16, 1024);
         }
         if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + col, ad[kk], bd[kk], idesc_s, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + C::COL_DP, ad[kk], bd[kk], idesc_s, kk > 0);
+        }
+        __syncwarp();
+      };
+      // S^T = K Q_i^T with K_j from TMEM (A) and Q_i K-major in smem (B)
+      auto issue_s = [&](uint32_t b) {
+        uint64_t bd[D / 16];
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) bd[kk] = make_sdesc_sw128(b + kmaj(kk, BM), 16, 1024);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) umma_ts(tbase + C::COL_S, tbase + C::COL_K + kk * 8, bd[kk], idesc_s, kk > 0);
         }
         __syncwarp();
       };
       bool ok = wait(bar + B_KV, 0, 120);
+      if (ok) ok = wait(bar + B_KT_READY, 0, 126);
       if (ok && nsteps > 0) {
         ok = wait(bar + B_QD_FULL + 0, 0, 121);
         if (ok) {
           tc_fence_after();
-          issue_scores(ks, qs_of(0), C::COL_S);
+          issue_s(qs_of(0));
           commit(bar + B_S_FULL);
         }
       }
@@ -232,8 +249,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int s = i % C::QSTAGES;
         const int s1 = (i + 1) % C::QSTAGES;
         const uint32_t qs = qs_of(s), dos = dos_of(s);
-        // dP^T_i (its columns were read out by the P/dS warps before ds_ready(i-1))
-        issue_scores(vs, dos, C::COL_DP);
+        // dP^T_i (its columns, holding dS^T_{i-1}, were last read by dK_{i-1}: same lane, in order)
+        issue_dp(dos);
         commit(bar + B_DP_FULL);
         // dV += P^T dO_i (P^T from TMEM, K = queries; dO_i as MN-major B)
         {
@@ -253,23 +270,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (i + 1 < nsteps) {
           if (!(ok = wait(bar + B_QD_FULL + s1, ((i + 1) / C::QSTAGES) & 1, 121))) break;
           tc_fence_after();
-          issue_scores(ks, qs_of(s1), C::COL_S);
+          issue_s(qs_of(s1));
           commit(bar + B_S_FULL);
         }
-        // dK += dS^T Q_i (dS^T K-major in smem, Q_i MN-major)
+        // dK += dS^T Q_i (dS^T 16-bit in TMEM over the dP^T columns, Q_i MN-major)
         {
-          uint64_t ad[BM / 16], bd[BM / 16];
+          uint64_t bd[BM / 16];
 #pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            ad[kk] = make_sdesc_sw128(dss + kmaj(kk, BN), 16, 1024);
-            bd[kk] = make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024);
-          }
+          for (int kk = 0; kk < BM / 16; ++kk) bd[kk] = make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024);
           if (!(ok = wait(bar + B_DS_READY, i & 1, 124))) break;
           tc_fence_after();
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
-              umma_ss(tbase + C::COL_DK, ad[kk], bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
+              umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + kk * 8, bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
           }
           __syncwarp();
         }
@@ -317,6 +331,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
     const uint32_t sw = (uint32_t)(rit & 7);
     bool ok = start_ok;
+    // K_j row -> TMEM (A operand of S^T = K Q^T): 16-byte chunks of the swizzled smem tile
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_KV, 0, ctx, 134));
+    if (ok) {
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb) {
+        const uint8_t* krow = smem + C::OFF_K + kb * (BN * 128) + rit * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 x = *reinterpret_cast<const uint4*>(krow + (((uint32_t)ch ^ sw) << 4));
+          w[4 * ch] = x.x;
+          w[4 * ch + 1] = x.y;
+          w[4 * ch + 2] = x.z;
+          w[4 * ch + 3] = x.w;
+        }
+        tmem_st32(tmem_addr(tbase, lane_base, C::COL_K + kb * 32), w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar + B_KT_READY);
+    }
     for (int i = 0; ok && i < nsteps; ++i) {
       const int s = i % C::QSTAGES;
       const int q0 = (i_start + i) * BM;
@@ -402,9 +437,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
               make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
         }
+        // and packed into TMEM over dP^T columns already read (A operand of dK += dS^T Q)
+        tmem_st16(tmem_addr(tbase, lane_base, C::COL_DP + c * 16), dsk);
       }
       }
       fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + B_DS_READY);
     }
