@@ -65,8 +65,9 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_key):
-    """DRAM bytes per launch of a kernel from a committed ncu summary, if taken on the current sources."""
+def profiled_traffic(kernel_key, workload):
+    """DRAM bytes per launch of a kernel on a workload from a committed ncu summary, if the
+    summary was taken on the current sources (else None)."""
     digest = source_digest()
     for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
         with open(p) as f:
@@ -74,9 +75,10 @@ def profiled_traffic(kernel_key):
                 # machine-readable line: "traffic: <kernel_key> <workload> <bytes_per_launch> sources=<digest>"
                 if line.startswith("traffic:"):
                     parts = line.split()
-                    if len(parts) >= 5 and parts[1] == kernel_key and parts[4] == f"sources={digest}":
-                        return parts[2], float(parts[3])
-    return None, None
+                    if (len(parts) >= 5 and parts[1] == kernel_key and parts[2] == workload
+                            and parts[4] == f"sources={digest}"):
+                        return float(parts[3])
+    return None
 
 
 class ClockSampler:
@@ -208,6 +210,27 @@ def workload_config(w: Workload):
 # ---------------------------------------------------------------------------
 
 
+def shard_workload(w: Workload, rank: int) -> Workload:
+    """Rank r's independent shard: the same shape, its own seed (weak scaling, no exchange)."""
+    return w.with_shape(seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest of each rank's value (one all-reduce of a scalar); x itself on one process."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the work all ranks did in one step over the slowest rank's step time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def _dev_tensor(stored, dtype, device):
     import torch
 
@@ -236,7 +259,7 @@ def run_gpu(args, w: Workload):
     binding.load_library()
 
     # every rank owns an independent shard of the same shape (weak scaling, no exchange)
-    x = make_inputs(w.with_shape(seed=w.seed + 1000 * rank), with_do=not w.fwd_only)
+    x = make_inputs(shard_workload(w, rank), with_do=not w.fwd_only)
     dev, pinned = {}, {}
     for k_, v_ in x.items():
         dev[k_], pinned[k_] = _dev_tensor(v_, w.dtype, device)
@@ -295,14 +318,11 @@ def run_gpu(args, w: Workload):
     total_ms = t_start.elapsed_time(t_end)
     per_kernel = {nm: sum(ev[s_][i].elapsed_time(ev[s_][i + 1]) for s_ in range(args.steps)) / args.steps
                   for i, nm in enumerate(names)}
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, device)
     ms_per_step = total_ms / args.steps
     pass_ = "fwd" if w.fwd_only else "fwd+bwd"
     flops_rank = attention_flops(w.B, w.H, w.N, w.d, w.causal, pass_)
-    value = flops_rank * world / (ms_per_step * 1e-3) / 1e12
+    value = aggregate_tflops(flops_rank, world, ms_per_step)
 
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -313,7 +333,7 @@ def run_gpu(args, w: Workload):
               "bwd_main": attention_flops(w.B, w.H, w.N, w.d, w.causal, "bwd")}
     dom = max((nm for nm in per_kernel if nm in kflops), key=lambda nm: per_kernel[nm])
     achieved = kflops[dom] / (per_kernel[dom] * 1e-3) / 1e12
-    _, traffic = profiled_traffic(dom)
+    traffic = profiled_traffic(dom, w.name)
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
                 "frac": achieved / peak_sus, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
@@ -345,11 +365,8 @@ def run_gpu(args, w: Workload):
     e_e.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e_s.elapsed_time(e_e) / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": flops_rank * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+    e2e_ms = max_over_ranks(e2e_ms, dist, device)
+    e2e = {"value": aggregate_tflops(flops_rank, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # ---------------- per-pass figures, including the non-causal variant of the same shape
