@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
                   const float* __restrict__ delta, void* __restrict__ dk_out, void* __restrict__ dv_out, int n,
-                  int npad, int ktiles, float scale, int causal, unsigned long long* err) {
+                  int npad, int bh_count, int ktiles, float scale, int causal, unsigned long long* err) {
   using C = BwdCfg<D>;
   constexpr int BM = C::BM;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -114,8 +114,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const ErrCtx ctx{err, abort_flag};
 
-  const int head = blockIdx.x / ktiles;
-  const int kt = blockIdx.x - head * ktiles;  // early key tiles carry the most causal work: launched first
+  // work item: head-major (CTAs running together share Q/dO in L2); causal: heaviest (first)
+  // key tiles first within groups of heads
+  int head, kt;
+  if (causal) {
+    grouped_work_item(blockIdx.x, bh_count, ktiles, &head, &kt);
+  } else {
+    head = blockIdx.x / ktiles;
+    kt = blockIdx.x - head * ktiles;
+  }
   const int k0 = kt * BN;
   const int qtiles = (n + BM - 1) / BM;
   const int i_start = causal ? kt * (BN / BM) : 0;  // first query tile reaching this key tile's diagonal
@@ -555,7 +562,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
   if (e != cudaSuccess) return e;
   const int ktiles = (a.n + BN - 1) / BN;
   kern<<<(unsigned)(a.bh * ktiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq, a.lse2, a.delta, a.dk, a.dv,
-                                                                      a.n, npad, ktiles, a.scale, a.causal, a.err);
+                                                                      a.n, npad, a.bh, ktiles, a.scale, a.causal, a.err);
   return cudaGetLastError();
 }
 

@@ -101,10 +101,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const ErrCtx ctx{err, abort_flag};
 
-  // work item: head-major so concurrently running CTAs share K/V in L2; heavy causal tiles first
-  const int head = blockIdx.x / tiles_per_head;
-  int tile = blockIdx.x - head * tiles_per_head;
-  if (causal) tile = tiles_per_head - 1 - tile;
+  // work item: head-major (CTAs running together share K/V in L2); causal: heaviest (last)
+  // query tiles first within groups of heads
+  int head, tile;
+  if (causal) {
+    int rank;
+    grouped_work_item(blockIdx.x, bh_count, tiles_per_head, &head, &rank);
+    tile = tiles_per_head - 1 - rank;
+  } else {
+    head = blockIdx.x / tiles_per_head;
+    tile = blockIdx.x - head * tiles_per_head;
+  }
   const int qrow0 = tile * (C::NQ * BM);
   const int nblocks = (n + BN - 1) / BN;
   int nq[2];

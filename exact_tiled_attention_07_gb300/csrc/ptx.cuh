@@ -60,7 +60,23 @@ __device__ __forceinline__ bool elect_one_sync() {
   return pred != 0;
 }
 
+// Work-item order for grids of (head, tile) CTAs whose work depends on the tile index.
+// Heads are taken in groups of kHeadGroup; inside a group, tiles go from the heaviest to the
+// lightest, all heads of the group per tile.  The block scheduler then runs a
+// longest-first list schedule per group while the CTAs running together touch at most a
+// group's heads, whose K/V (or Q/dO) stay in L2.  `heavy_rank` 0 is the heaviest tile.
+constexpr int kHeadGroup = 16;
+__device__ __forceinline__ void grouped_work_item(int bid, int heads, int tiles, int* head, int* heavy_rank) {
+  const int per_group = kHeadGroup * tiles;
+  const int g = bid / per_group;
+  const int r = bid - g * per_group;
+  const int gsize = min(kHeadGroup, heads - g * kHeadGroup);
+  *heavy_rank = r / gsize;
+  *head = g * kHeadGroup + (r - *heavy_rank * gsize);
+}
+
 // ---------------------------------------------------------------------------
+// mbarrier// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
