@@ -46,14 +46,19 @@ class Workload:
     seed: int = 0
     fwd_only: bool = False
     extra: dict = field(default_factory=dict)
+    Hkv: int = 0  # key/value heads (grouped-query attention); 0 means H
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
 
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv or self.H
+
     def with_shape(self, **kw) -> "Workload":
         fields = dict(name=self.name, B=self.B, H=self.H, N=self.N, d=self.d, dtype=self.dtype,
-                      causal=self.causal, dist=self.dist, seed=self.seed, fwd_only=self.fwd_only)
+                      causal=self.causal, dist=self.dist, seed=self.seed, fwd_only=self.fwd_only, Hkv=self.Hkv)
         fields.update(kw)
         return Workload(**fields)
 
@@ -103,21 +108,23 @@ def to_float64(stored: np.ndarray, dtype: str) -> np.ndarray:
 def make_inputs(w: Workload, with_do: bool = True) -> dict:
     """Draw Q, K, V (and dO) for workload ``w``; values already rounded to ``w.dtype``.
 
-    Returns a dict of storage arrays [B, H, N, d] under keys q, k, v, do.
+    Returns a dict of storage arrays under keys q, k, v, do: Q and dO [B, H, N, d], K and V
+    [B, H_kv, N, d] (H_kv = H unless the workload shares key/value heads).
     """
     rng = np.random.Generator(np.random.PCG64(w.seed))
     shape = (w.B, w.H, w.N, w.d)
+    kv_shape = (w.B, w.kv_heads, w.N, w.d)
     names = ["q", "k", "v"] + (["do"] if with_do else [])
     raw = {}
     for nm in names:
-        raw[nm] = rng.standard_normal(size=shape, dtype=np.float32)
+        raw[nm] = rng.standard_normal(size=kv_shape if nm in ("k", "v") else shape, dtype=np.float32)
     if w.dist == "normal_over_sqrt_d":
         f = np.float32(1.0 / math.sqrt(w.d))
         for nm in names:
             raw[nm] *= f
     elif w.dist == "normal_key_offset":
         # per-key additive score offset c_j ~ N(0, σ² = 4), carried by coordinate 0
-        c = rng.standard_normal(size=(w.B, w.H, w.N), dtype=np.float32) * np.float32(2.0)
+        c = rng.standard_normal(size=(w.B, w.kv_heads, w.N), dtype=np.float32) * np.float32(2.0)
         raw["q"][..., 0] = 1.0
         raw["k"][..., 0] = c * np.float32(math.sqrt(w.d))
     elif w.dist != "normal":

@@ -336,3 +336,61 @@ def test_planted_missing_tau_in_dk_fails_fd():
     _, dk, _, _ = oracle.attn_bwd64(q, k, v, do, 0.5, False)
     _, fk, _ = _fd_grads(q, k, v, do, 0.5, False)
     assert np.abs(dk / 0.5 - fk).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
+# grouped-query / multi-query attention
+# --------------------------------------------------------------------------
+
+from oracle import gqa as G  # noqa: E402
+
+
+def test_gqa_group_of_one_is_plain_attention():
+    rng = np.random.default_rng(21)
+    q, k, v, do = (rng.standard_normal((2, 3, 11, 4)) for _ in range(4))
+    for causal in (False, True):
+        o1, l1 = G.attn_fwd64_gqa(q, k, v, 0.6, causal)
+        o2, l2 = oracle.attn_fwd64(q, k, v, 0.6, causal)
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
+        g1 = G.attn_bwd64_gqa(q, k, v, do, 0.6, causal)
+        g2 = oracle.attn_bwd64(q, k, v, do, 0.6, causal)
+        for a, b in zip(g1, g2):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_gqa_heads_share_key_value_heads():
+    # query heads 0,1 read key/value head 0; heads 2,3 read head 1 (g = 2)
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((1, 4, 9, 3))
+    k, v = rng.standard_normal((1, 2, 9, 3)), rng.standard_normal((1, 2, 9, 3))
+    o, _ = G.attn_fwd64_gqa(q, k, v, 0.5, True)
+    for h in range(4):
+        kv = G.kv_head_of(h, 4, 2)
+        assert kv == h // 2
+        oh, _ = oracle.attn_fwd64(q[:, h:h + 1], k[:, kv:kv + 1], v[:, kv:kv + 1], 0.5, True)
+        np.testing.assert_allclose(o[:, h], oh[:, 0], atol=1e-15)
+    with pytest.raises(ValueError):
+        G.kv_head_of(0, 4, 3)
+
+
+@pytest.mark.parametrize("h,h_kv,causal", [(4, 2, False), (3, 1, True)])
+def test_gqa_backward_matches_finite_differences(h, h_kv, causal):
+    rng = np.random.default_rng(23 + h)
+    n, d = 5, 3
+    q, do = rng.standard_normal((1, h, n, d)), rng.standard_normal((1, h, n, d))
+    k, v = rng.standard_normal((1, h_kv, n, d)), rng.standard_normal((1, h_kv, n, d))
+    dq, dk, dv, _ = G.attn_bwd64_gqa(q, k, v, do, 0.7, causal)
+    fq, fk, fv = _fd_grads(q, k, v, do, 0.7, causal, fwd=G.attn_fwd64_gqa)
+    for a, b in ((dq, fq), (dk, fk), (dv, fv)):
+        assert np.abs(a - b).max() < 1e-8
+
+
+def test_planted_gqa_backward_without_group_sum_fails_fd():
+    rng = np.random.default_rng(29)
+    q, do = rng.standard_normal((1, 2, 4, 3)), rng.standard_normal((1, 2, 4, 3))
+    k, v = rng.standard_normal((1, 1, 4, 3)), rng.standard_normal((1, 1, 4, 3))
+    _, dk_e, _, _ = oracle.attn_bwd64(q, G.expand_kv(k, 2), G.expand_kv(v, 2), do, 0.7, False)
+    wrong = dk_e[:, :1]  # slip: only the first query head's contribution
+    _, fk, _ = _fd_grads(q, k, v, do, 0.7, False, fwd=G.attn_fwd64_gqa)
+    assert np.abs(wrong - fk).max() > 1e-3
