@@ -19,7 +19,8 @@ __all__ = [
     "FAError", "library_path", "load_library", "DTYPE_CODES",
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
-    "fa_last_error_message", "fa_bwd_noalloc", "attention_forward", "attention_backward", "EXPORTED_SYMBOLS",
+    "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "attention_forward",
+    "attention_backward", "EXPORTED_SYMBOLS",
     "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -32,7 +33,7 @@ DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 EXPORTED_SYMBOLS = (
     "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
-    "fa_last_error_message", "fa_bwd_noalloc",
+    "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa",
 )
 
 _lib = None
@@ -70,6 +71,8 @@ def load_library():
         lib.fa_bwd_main.argtypes = [vp] * 7 + [sz, i, i, i, i, f, i, i, vp]
         lib.fa_bwd_dq_convert.argtypes = [vp, sz, vp, i, i, i, i, f, i, vp]
         lib.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, f, i, i, vp]
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+        lib.fa_bwd_gqa.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
         lib.fa_uses_tensor_cores.argtypes = [i, i, i]
@@ -77,7 +80,8 @@ def load_library():
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_error_message.argtypes = []
         lib.fa_last_error_message.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
+        for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_noalloc", "fa_bwd_preprocess",
+                     "fa_bwd_main", "fa_bwd_dq_convert",
                      "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -131,6 +135,37 @@ def fa_fwd(Q, K, V, O, L, scale, causal, stream=None):
         raise ValueError("L must be a contiguous fp32 tensor of B*H*N elements")
     _check(load_library().fa_fwd(_p(Q), _p(K), _p(V), _p(O), _p(L), B, H, N, d, float(scale), int(bool(causal)),
                                  _dt(Q), _stream(stream)))
+
+
+def _kv_heads(Q, K, V, *kv_like):
+    """Key/value head count of K (grouped-query attention) after checking the shapes agree."""
+    B, H, N, d = _shape4(Q)
+    Bk, Hkv, Nk, dk = _shape4(K)
+    if (Bk, Nk, dk) != (B, N, d) or Hkv < 1 or H % Hkv:
+        raise ValueError("K must be [B, Hkv, N, d] with H a multiple of Hkv")
+    for t in (V,) + kv_like:
+        if t.shape != K.shape or t.dtype != Q.dtype or t.device != Q.device or not t.is_contiguous():
+            raise ValueError("K, V (and dK, dV) must share shape, dtype and device and be contiguous")
+    return Hkv
+
+
+def fa_fwd_gqa(Q, K, V, O, L, scale, causal, stream=None):
+    B, H, N, d = _shape4(Q)
+    Hkv = _kv_heads(Q, K, V)
+    _same(Q, O)
+    if L.dtype != torch.float32 or L.numel() != B * H * N or not L.is_contiguous():
+        raise ValueError("L must be a contiguous fp32 tensor of B*H*N elements")
+    _check(load_library().fa_fwd_gqa(_p(Q), _p(K), _p(V), _p(O), _p(L), B, H, Hkv, N, d, float(scale),
+                                     int(bool(causal)), _dt(Q), _stream(stream)))
+
+
+def fa_bwd_gqa(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, stream=None):
+    B, H, N, d = _shape4(Q)
+    Hkv = _kv_heads(Q, K, V, dK, dV)
+    _same(Q, O, dO, dQ)
+    _check(load_library().fa_bwd_gqa(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV),
+                                     _p(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+                                     float(scale), int(bool(causal)), _dt(Q), _stream(stream)))
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:
@@ -204,12 +239,15 @@ def fa_last_error_message() -> str:
 
 
 def attention_forward(q, k, v, causal=False, scale=None, stream=None):
-    """O, L = fa_fwd(q, k, v); outputs allocated on q's device."""
+    """O, L = fa_fwd(q, k, v) (fa_fwd_gqa when k, v have fewer heads than q); outputs on q's device."""
     B, H, N, d = _shape4(q)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    if k.shape[1] != H:
+        fa_fwd_gqa(q, k, v, o, lse, scale, causal, stream)
+    else:
+        fa_fwd(q, k, v, o, lse, scale, causal, stream)
     return o, lse
 
 
@@ -221,5 +259,8 @@ def attention_backward(q, k, v, o, do, lse, causal=False, scale=None, workspace=
     if workspace is None:
         nbytes = fa_bwd_workspace_size(B, H, N, d)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
-    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)
+    if k.shape[1] != H:
+        fa_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)
+    else:
+        fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)
     return dq, dk, dv

@@ -129,21 +129,77 @@ int set_last_error(int status, const char* fmt, ...) {
 
 using namespace fa;
 
-extern "C" {
+namespace {
 
-fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, void* stream) {
+// Query heads H share key/value heads Hkv (H a multiple of Hkv); Hkv == H is plain attention.
+fa_status check_heads(int H, int Hkv) {
+  if (Hkv < 1 || H % Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "H=%d query heads must be a positive multiple of Hkv=%d key/value heads", H, Hkv);
+  return FA_OK;
+}
+
+fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv, int N,
+                   int d, float scale, int causal, fa_dtype dtype, void* stream, const char* name) {
   bool empty;
   fa_status st = check_common(B, H, N, d, dtype, &empty);
   if (st != FA_OK || empty) return st;
-  if ((st = check_ptrs({Q, K, V, O, L}, "fa_fwd")) != FA_OK) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
+  if ((st = check_ptrs({Q, K, V, O, L}, name)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   DeviceSyms syms;
   if ((st = device_syms(&syms)) != FA_OK) return st;
   FwdArgs a{Q, K, V, O, L, B * H, N, d, scale, causal ? 1 : 0, (int)dtype, syms.err, syms.counter,
             static_cast<cudaStream_t>(stream)};
-  if (fwd_tc_supported(a.dtype, d)) return launched(launch_fwd_tc(a), "fa_fwd (tensor-core kernel)");
-  return launched(launch_fwd_simt(a), "fa_fwd (CUDA-core kernel)");
+  a.group = H / Hkv;
+  if (fwd_tc_supported(a.dtype, d)) return launched(launch_fwd_tc(a), "forward (tensor-core kernel)");
+  return launched(launch_fwd_simt(a), "forward (CUDA-core kernel)");
+}
+
+fa_status bwd_main_impl(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
+                        void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale,
+                        int causal, fa_dtype dtype, void* stream, const char* name) {
+  bool empty;
+  fa_status st = check_common(B, H, N, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
+  if ((st = check_ptrs({Q, K, V, dO, dK, dV, workspace}, name)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  BwdArgs a{};
+  if ((st = carve(&a, workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
+  DeviceSyms syms;
+  if ((st = device_syms(&syms)) != FA_OK) return st;
+  a.q = Q;
+  a.k = K;
+  a.v = V;
+  a.dout = dO;
+  a.dk = dK;
+  a.dv = dV;
+  a.bh = B * H;
+  a.n = N;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.dtype = (int)dtype;
+  a.err = syms.err;
+  a.counter = syms.counter;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.group = H / Hkv;
+  if (bwd_tc_supported(a.dtype, d)) return launched(launch_bwd_tc(a), "backward (tensor-core kernel)");
+  return launched(launch_bwd_simt(a), "backward (CUDA-core kernels)");
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream) {
+  return fwd_impl(Q, K, V, O, L, B, H, H, N, d, scale, causal, dtype, stream, "fa_fwd");
+}
+
+fa_status fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv, int N,
+                     int d, float scale, int causal, fa_dtype dtype, void* stream) {
+  return fwd_impl(Q, K, V, O, L, B, H, Hkv, N, d, scale, causal, dtype, stream, "fa_fwd_gqa");
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -174,32 +230,8 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* L, void*
 fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
                       fa_dtype dtype, void* stream) {
-  bool empty;
-  fa_status st = check_common(B, H, N, d, dtype, &empty);
-  if (st != FA_OK || empty) return st;
-  if ((st = check_ptrs({Q, K, V, dO, dK, dV, workspace}, "fa_bwd_main")) != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
-  BwdArgs a{};
-  if ((st = carve(&a, workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
-  DeviceSyms syms;
-  if ((st = device_syms(&syms)) != FA_OK) return st;
-  a.q = Q;
-  a.k = K;
-  a.v = V;
-  a.dout = dO;
-  a.dk = dK;
-  a.dv = dV;
-  a.bh = B * H;
-  a.n = N;
-  a.d = d;
-  a.scale = scale;
-  a.causal = causal ? 1 : 0;
-  a.dtype = (int)dtype;
-  a.err = syms.err;
-  a.counter = syms.counter;
-  a.stream = static_cast<cudaStream_t>(stream);
-  if (bwd_tc_supported(a.dtype, d)) return launched(launch_bwd_tc(a), "fa_bwd_main (tensor-core kernel)");
-  return launched(launch_bwd_simt(a), "fa_bwd_main (CUDA-core kernels)");
+  return bwd_main_impl(Q, K, V, dO, dK, dV, workspace, workspace_bytes, B, H, H, N, d, scale, causal, dtype, stream,
+                       "fa_bwd_main");
 }
 
 fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void* dQ, int B, int H, int N, int d,
@@ -221,19 +253,27 @@ fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void*
   return launched(launch_dq_convert(a), "fa_bwd_dq_convert");
 }
 
-fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
-                 void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, void* stream) {
+fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
+                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                     int N, int d, float scale, int causal, fa_dtype dtype, void* stream) {
   bool empty;
   fa_status st = check_common(B, H, N, d, dtype, &empty);
   if (st != FA_OK || empty) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if ((st = check_ptrs({Q, K, V, O, dO, L, dQ, dK, dV, workspace}, "fa_bwd")) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if ((st = fa_bwd_preprocess(O, dO, L, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK) return st;
-  if ((st = fa_bwd_main(Q, K, V, dO, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal, dtype, stream)) !=
-      FA_OK)
+  if ((st = bwd_main_impl(Q, K, V, dO, dK, dV, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, dtype,
+                          stream, "fa_bwd")) != FA_OK)
     return st;
   return fa_bwd_dq_convert(workspace, workspace_bytes, dQ, B, H, N, d, scale, dtype, stream);
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
+                 void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, void* stream) {
+  return fa_bwd_gqa(Q, K, V, O, dO, L, dQ, dK, dV, workspace, workspace_bytes, B, H, H, N, d, scale, causal, dtype,
+                    stream);
 }
 
 fa_status fa_check_device_error(void* stream) {

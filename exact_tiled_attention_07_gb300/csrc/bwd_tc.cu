@@ -8,7 +8,8 @@
 //     dK_j += dS^T Q_i,   dQ_i += dS K_j      (tau applied to dK here and to dQ on conversion)
 // with D_i = sum_k dO_ik O_ik precomputed by the preprocess kernel (the §5.4 identity).
 //
-// One CTA owns a 128-key tile of one head for its whole life: K_j, V_j stay in shared
+// One CTA owns a 128-key tile of one key/value head for its whole life (with grouped-query
+// attention it visits every query head of that key/value head): K_j, V_j stay in shared
 // memory and the dK_j, dV_j accumulators stay in TMEM, while query tiles (Q_i, dO_i, L_i,
 // D_i) stream through a three-stage TMA ring.  Working transposed puts keys on TMEM lanes, so
 // one thread owns one key row: P^T and dS^T need no cross-thread reduction.  K_j, P^T and
@@ -90,6 +91,14 @@ enum BwdBar {
   B_KT_READY = 15,  // K_j copied into TMEM
 };
 
+// advance a (query tile, query head) step cursor
+__device__ __forceinline__ void step_next(int& ii, int& g, int tiles_per_head) {
+  if (++ii == tiles_per_head) {
+    ii = 0;
+    ++g;
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void store_row16(void* base, int64_t row, const uint32_t (&pk)[16], int chunk) {
   uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(base) + row * D * 2 + chunk * 64);
@@ -103,7 +112,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
                   const float* __restrict__ delta, void* __restrict__ dk_out, void* __restrict__ dv_out, int n,
-                  int npad, int bh_count, int ktiles, float scale, int causal, unsigned long long* err) {
+                  int npad, int bh_count, int ktiles, float scale, int causal, int group, unsigned long long* err) {
   using C = BwdCfg<D>;
   constexpr int BM = C::BM;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -116,17 +125,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   // work item: head-major (CTAs running together share Q/dO in L2); causal: heaviest (first)
   // key tiles first within groups of heads
-  int head, kt;
+  int kvh, kt;  // key/value head and key tile of this CTA
   if (causal) {
-    grouped_work_item(blockIdx.x, bh_count, ktiles, &head, &kt);
+    grouped_work_item(blockIdx.x, bh_count, ktiles, &kvh, &kt);
   } else {
-    head = blockIdx.x / ktiles;
-    kt = blockIdx.x - head * ktiles;
+    kvh = blockIdx.x / ktiles;
+    kt = blockIdx.x - kvh * ktiles;
   }
   const int k0 = kt * BN;
   const int qtiles = (n + BM - 1) / BM;
   const int i_start = causal ? kt * (BN / BM) : 0;  // first query tile reaching this key tile's diagonal
-  const int nsteps = qtiles - i_start;
+  // steps: (query head of this key/value head's group, query tile) pairs; dK, dV sum over all
+  const int nsteps_head = qtiles - i_start;
+  const int nsteps = group * nsteps_head;
+  // each role walks the steps with a (query tile ii, query head g of the group) cursor, advanced
+  // by step_next (no integer division on the per-step path)
   const float scale_log2 = scale * 1.4426950408889634f;
 
   if (threadIdx.x == 0) {
@@ -167,23 +180,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(bar + B_KV, 2 * C::KV_BYTES);
       for (int kb = 0; kb < C::KB; ++kb) {
-        tma_load_3d(smem + C::OFF_K + kb * (BN * 128), &tm_k, bar + B_KV, kb * 64, k0, head);
-        tma_load_3d(smem + C::OFF_V + kb * (BN * 128), &tm_v, bar + B_KV, kb * 64, k0, head);
+        tma_load_3d(smem + C::OFF_K + kb * (BN * 128), &tm_k, bar + B_KV, kb * 64, k0, kvh);
+        tma_load_3d(smem + C::OFF_V + kb * (BN * 128), &tm_v, bar + B_KV, kb * 64, k0, kvh);
       }
       int issued = 0;
-      for (int i = 0; i < nsteps; ++i) {
+      for (int i = 0, ii = 0, g = 0; i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
         const int s = i % C::QSTAGES, use = i / C::QSTAGES;
         if (use > 0 && !mbar_wait(bar + B_QD_EMPTY + s, (use - 1) & 1, ctx, 110)) break;
-        const int q0 = (i_start + i) * BM;
+        const int q0 = (i_start + ii) * BM, qh = kvh * group + g;
         uint64_t* fb = bar + B_QD_FULL + s;
         mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + 2 * BM * 4);
         for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(smem + C::OFF_Q + s * C::QT_BYTES + kb * (BM * 128), &tm_q, fb, kb * 64, q0, head);
-          tma_load_3d(smem + C::OFF_DO + s * C::QT_BYTES + kb * (BM * 128), &tm_do, fb, kb * 64, q0, head);
+          tma_load_3d(smem + C::OFF_Q + s * C::QT_BYTES + kb * (BM * 128), &tm_q, fb, kb * 64, q0, qh);
+          tma_load_3d(smem + C::OFF_DO + s * C::QT_BYTES + kb * (BM * 128), &tm_do, fb, kb * 64, q0, qh);
         }
         float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + s * 2 * BM;
-        bulk_load(vec, lse2 + (int64_t)head * npad + q0, BM * 4, fb);
-        bulk_load(vec + BM, delta + (int64_t)head * npad + q0, BM * 4, fb);
+        bulk_load(vec, lse2 + (int64_t)qh * npad + q0, BM * 4, fb);
+        bulk_load(vec + BM, delta + (int64_t)qh * npad + q0, BM * 4, fb);
         issued = i + 1;
       }
       ErrCtx nctx = ctx;
@@ -359,9 +372,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar + B_KT_READY);
     }
-    for (int i = 0; ok && i < nsteps; ++i) {
+    for (int i = 0, ii = 0, g = 0; ok && i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
       const int s = i % C::QSTAGES;
-      const int q0 = (i_start + i) * BM;
+      const int q0 = (i_start + ii) * BM;
       const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
       const float* dvec = l2v + BM;
       // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
@@ -473,7 +486,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
             for (int t = 0; t < 16; ++t)
               pk[t] = pack2<BF16>(__uint_as_float(r[2 * t]) * f, __uint_as_float(r[2 * t + 1]) * f);
-            if (key_ok) store_row16<D>(dst, (int64_t)head * n + key, pk, c);
+            if (key_ok) store_row16<D>(dst, (int64_t)kvh * n + key, pk, c);
           }
         }
       }
@@ -481,8 +494,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // no query meets this key tile: zero gradients (not reachable for square causal masks)
       uint32_t pk[16] = {};
       for (int c = 0; c < D / 32; ++c) {
-        store_row16<D>(dk_out, (int64_t)head * n + key, pk, c);
-        store_row16<D>(dv_out, (int64_t)head * n + key, pk, c);
+        store_row16<D>(dk_out, (int64_t)kvh * n + key, pk, c);
+        store_row16<D>(dv_out, (int64_t)kvh * n + key, pk, c);
       }
     }
   } else if (warp < 8) {
@@ -493,8 +506,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int rr = (warp & 3) * 32 + lane;
     const bool leader = (warp == 4 && lane == 0);
     bool ok = start_ok;
-    for (int i = 0; ok && i < nsteps; ++i) {
-      const int q0 = (i_start + i) * BM;
+    for (int i = 0, ii = 0, g = 0; ok && i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
+      const int q0 = (i_start + ii) * BM;
       ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, i & 1, ctx, 140));
       if (!ok) break;
       tc_fence_after();
@@ -527,11 +540,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (leader) {
+        const int qh = kvh * group + g;
         if constexpr (C::DQT) {
-          tma_reduce_add_3d(&tm_dq, stg, 0, q0, head);
+          tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
         } else {
-          tma_reduce_add_3d(&tm_dq, stg, 0, q0, head);
-          tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, head);
+          tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
+          tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, qh);
         }
         bulk_commit_group();
       }
@@ -552,8 +566,9 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
   using C = BwdCfg<D>;
   const int npad = (int)padded_rows(a.n);
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, C::BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, a.bh, BN) ||
-      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, a.bh, BN) ||
+  const int bh_kv = a.bh / a.group;
+  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, C::BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) ||
+      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN) ||
       !make_tmap_16bit_3d(&tdo, a.dout, BF16, D, a.n, a.bh, C::BM) ||
       !make_tmap_f32_3d(&tdq, a.dq_acc, D, npad, a.bh, C::DQT ? D : 32, C::BM, !C::DQT))
     return cudaErrorInvalidValue;
@@ -561,8 +576,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int ktiles = (a.n + BN - 1) / BN;
-  kern<<<(unsigned)(a.bh * ktiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq, a.lse2, a.delta, a.dk, a.dv,
-                                                                      a.n, npad, a.bh, ktiles, a.scale, a.causal, a.err);
+  kern<<<(unsigned)(bh_kv * ktiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq, a.lse2, a.delta, a.dk, a.dv,
+                                                                      a.n, npad, bh_kv, ktiles, a.scale, a.causal, a.group, a.err);
   return cudaGetLastError();
 }
 

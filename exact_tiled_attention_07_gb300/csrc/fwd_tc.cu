@@ -80,7 +80,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, float* __restrict__ lse, int n,
-                  int bh_count, int tiles_per_head, float scale_log2, int causal, unsigned long long* err,
+                  int bh_count, int tiles_per_head, float scale_log2, int causal, int group, unsigned long long* err,
                   unsigned long long* counter) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     head = blockIdx.x / tiles_per_head;
     tile = blockIdx.x - head * tiles_per_head;
   }
+  const int kvhead = head / group;  // grouped-query attention: key/value head shared by `group` query heads
   const int qrow0 = tile * (C::NQ * BM);
   const int nblocks = (n + BN - 1) / BN;
   int nq[2];
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
         const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, kb * 64, (idx >> 1) * BN, head);
+          tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, kb * 64, (idx >> 1) * BN, kvhead);
         issued = idx + 1;
       }
       // drain: every copy this thread started must land before the CTA may exit
@@ -454,8 +455,9 @@ template <int D, bool BF16>
 cudaError_t launch_fwd_d(const FwdArgs& a) {
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, a.bh, BN) ||
-      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, a.bh, BN))
+  const int bh_kv = a.bh / a.group;
+  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) ||
+      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN))
     return cudaErrorInvalidValue;
   auto kern = fwd_tc_kernel<D, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -463,7 +465,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
   const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
   const float scale_log2 = a.scale * 1.4426950408889634f;
   kern<<<(unsigned)(a.bh * tiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles,
-                                                                     scale_log2, a.causal, a.err, a.counter);
+                                                                     scale_log2, a.causal, a.group, a.err, a.counter);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,7 @@ struct FwdArgs {
   const void* v;
   void* o;
   float* lse;
-  int bh;  // B*H
+  int bh;  // B*H (query heads)
   int n;
   int d;
   float scale;
@@ -25,6 +25,7 @@ struct FwdArgs {
   unsigned long long* err;      // device error word
   unsigned long long* counter;  // device count of processed (query tile, key tile) pairs
   cudaStream_t stream;
+  int group = 1;  // query heads per key/value head: K, V hold bh / group heads
 };
 
 // Backward workspace, carved from one caller buffer of fa_bwd_workspace_size bytes:
@@ -53,6 +54,7 @@ struct BwdArgs {
   unsigned long long* err;
   unsigned long long* counter;
   cudaStream_t stream;
+  int group = 1;  // query heads per key/value head: K, V, dK, dV hold bh / group heads
 };
 
 // Records the calling thread's last error message (read by fa_last_error_message) and

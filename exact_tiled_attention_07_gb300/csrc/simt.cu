@@ -61,7 +61,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) fwd_simt(const T* __restrict__ Q, const T* __restrict__ K,
                                                      const T* __restrict__ V, T* __restrict__ O,
                                                      float* __restrict__ L, int n, int d, float scale, int causal,
-                                                     int row_tiles, unsigned long long* counter) {
+                                                     int row_tiles, int group, unsigned long long* counter) {
   extern __shared__ float sm[];
   float* qs = sm;                       // [32][d]
   float* ks = qs + kRows * d;           // [32][d+1]
@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt(const T* __restrict__ Q, co
   const int bh = blockIdx.x / row_tiles;
   const int r0 = (blockIdx.x - bh * row_tiles) * kRows;
   const int64_t hoff = (int64_t)bh * n * d;
+  const int64_t kvoff = (int64_t)(bh / group) * n * d;  // key/value head of this query head
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_lane = (d + 31) / 32;
 
@@ -86,8 +87,8 @@ __global__ void __launch_bounds__(kThreads) fwd_simt(const T* __restrict__ Q, co
   unsigned long long tiles = 0;
   for (int k0 = 0; k0 < kend; k0 += kTile) {
     __syncthreads();
-    load_rows(ks, d + 1, K + hoff, k0, kTile, n, d);
-    load_rows(vs, d, V + hoff, k0, kTile, n, d);
+    load_rows(ks, d + 1, K + kvoff, k0, kTile, n, d);
+    load_rows(vs, d, V + kvoff, k0, kTile, n, d);
     __syncthreads();
     ++tiles;
 #pragma unroll
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt(const T* __restrict__ 
                                                           const float* __restrict__ lse2,
                                                           const float* __restrict__ delta, int npad, T* __restrict__ dK,
                                                           T* __restrict__ dV, int n, int d, float scale, int causal,
-                                                          int row_tiles) {
+                                                          int row_tiles, int group) {
   extern __shared__ float sm[];
   float* kb = sm;                        // [32][d] this block's key rows
   float* vb = kb + kRows * d;            // [32][d]
@@ -152,21 +153,24 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt(const T* __restrict__ 
   float* dos = qs + kTile * (d + 1);     // [32][d+1]
   float* ls = dos + kTile * (d + 1);     // [32]
   float* ds_ = ls + kTile;               // [32]
-  const int bh = blockIdx.x / row_tiles;
-  const int j0 = (blockIdx.x - bh * row_tiles) * kRows;
-  const int64_t hoff = (int64_t)bh * n * d;
+  const int kvh = blockIdx.x / row_tiles;  // key/value head; its query heads are kvh*group .. +group-1
+  const int j0 = (blockIdx.x - kvh * row_tiles) * kRows;
+  const int64_t kvoff = (int64_t)kvh * n * d;
   const float scale_log2 = scale * 1.4426950408889634f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_lane = (d + 31) / 32;
-  load_rows(kb, d, K + hoff, j0, kRows, n, d);
-  load_rows(vb, d, V + hoff, j0, kRows, n, d);
+  load_rows(kb, d, K + kvoff, j0, kRows, n, d);
+  load_rows(vb, d, V + kvoff, j0, kRows, n, d);
   float dk[4][kPerLane], dv[4][kPerLane];
 #pragma unroll
   for (int t = 0; t < 4; ++t)
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) dk[t][i] = dv[t][i] = 0.f;
   const int qstart = causal ? (j0 / kTile) * kTile : 0;
+  for (int g = 0; g < group; ++g)
   for (int q0 = qstart; q0 < n; q0 += kTile) {
+    const int bh = kvh * group + g;  // query head
+    const int64_t hoff = (int64_t)bh * n * d;
     __syncthreads();
     load_rows(qs, d + 1, Q + hoff, q0, kTile, n, d);
     load_rows(dos, d + 1, dO + hoff, q0, kTile, n, d);
@@ -213,8 +217,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt(const T* __restrict__ 
     for (int i = 0; i < kPerLane; ++i) {
       const int c = lane + 32 * i;
       if (i < per_lane && c < d) {
-        st(dK, hoff + (int64_t)key * d + c, dk[t][i] * scale);
-        st(dV, hoff + (int64_t)key * d + c, dv[t][i]);
+        st(dK, kvoff + (int64_t)key * d + c, dk[t][i] * scale);
+        st(dV, kvoff + (int64_t)key * d + c, dv[t][i]);
       }
     }
   }
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt(const T* __restrict__ Q,
                                                         const T* __restrict__ V, const T* __restrict__ dO,
                                                         const float* __restrict__ lse2, const float* __restrict__ delta,
                                                         int npad, float* __restrict__ dq_acc, int n, int d,
-                                                        float scale, int causal, int row_tiles) {
+                                                        float scale, int causal, int row_tiles, int group) {
   extern __shared__ float sm[];
   float* qs = sm;                     // [32][d]
   float* dos = qs + kRows * d;        // [32][d]
@@ -237,6 +241,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt(const T* __restrict__ Q,
   const int bh = blockIdx.x / row_tiles;
   const int r0 = (blockIdx.x - bh * row_tiles) * kRows;
   const int64_t hoff = (int64_t)bh * n * d;
+  const int64_t kvoff = (int64_t)(bh / group) * n * d;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_lane = (d + 31) / 32;
   const float scale_log2 = scale * 1.4426950408889634f;
@@ -254,8 +259,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt(const T* __restrict__ Q,
   const int kend = causal ? min(n, r0 + kRows) : n;
   for (int k0 = 0; k0 < kend; k0 += kTile) {
     __syncthreads();
-    load_rows(ks, d + 1, K + hoff, k0, kTile, n, d);
-    load_rows(vs, d + 1, V + hoff, k0, kTile, n, d);
+    load_rows(ks, d + 1, K + kvoff, k0, kTile, n, d);
+    load_rows(vs, d + 1, V + kvoff, k0, kTile, n, d);
     __syncthreads();
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -403,7 +408,7 @@ cudaError_t fwd_simt_t(const FwdArgs& a) {
   const int tiles = (a.n + kRows - 1) / kRows;
   const size_t smem = sizeof(float) * (size_t)(kRows * a.d + kTile * (a.d + 1) + kTile * a.d);
   return launch_smem(fwd_simt<T>, a.bh * tiles, smem, a.stream, (const T*)a.q, (const T*)a.k, (const T*)a.v,
-                     (T*)a.o, a.lse, a.n, a.d, a.scale, a.causal, tiles, a.counter);
+                     (T*)a.o, a.lse, a.n, a.d, a.scale, a.causal, tiles, a.group, a.counter);
 }
 
 template <typename T>
@@ -411,14 +416,14 @@ cudaError_t bwd_simt_t(const BwdArgs& a) {
   const int tiles = (a.n + kRows - 1) / kRows;
   const int npad = (int)padded_rows(a.n);
   const size_t smem1 = sizeof(float) * (size_t)(2 * kRows * a.d + 2 * kTile * (a.d + 1) + 2 * kTile);
-  cudaError_t e = launch_smem(bwd_dkdv_simt<T>, a.bh * tiles, smem1, a.stream, (const T*)a.q, (const T*)a.k,
+  cudaError_t e = launch_smem(bwd_dkdv_simt<T>, (a.bh / a.group) * tiles, smem1, a.stream, (const T*)a.q, (const T*)a.k,
                               (const T*)a.v, (const T*)a.dout, (const float*)a.lse2, (const float*)a.delta, npad,
-                              (T*)a.dk, (T*)a.dv, a.n, a.d, a.scale, a.causal, tiles);
+                              (T*)a.dk, (T*)a.dv, a.n, a.d, a.scale, a.causal, tiles, a.group);
   if (e != cudaSuccess) return e;
   const size_t smem2 = sizeof(float) * (size_t)(2 * kRows * a.d + 2 * kTile * (a.d + 1));
   return launch_smem(bwd_dq_simt<T>, a.bh * tiles, smem2, a.stream, (const T*)a.q, (const T*)a.k, (const T*)a.v,
                      (const T*)a.dout, (const float*)a.lse2, (const float*)a.delta, npad, a.dq_acc, a.n, a.d,
-                     a.scale, a.causal, tiles);
+                     a.scale, a.causal, tiles, a.group);
 }
 
 template <typename T>

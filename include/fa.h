@@ -74,6 +74,15 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
                  float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
+ * Forward pass with grouped-query / multi-query attention ("Lecture 8" §8.2): H query heads
+ * share Hkv key/value heads, query head h of a batch row reading key/value head
+ * h / (H / Hkv). K and V are [B][Hkv][N][d]; Q, O are [B][H][N][d]; L is [B][H][N].
+ * H must be a positive multiple of Hkv (Hkv == 1: multi-query; Hkv == H: fa_fwd).
+ */
+FA_API fa_status fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv,
+                            int N, int d, float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: per head, with Np = N rounded up to 128,
  * D [Np] fp32, L*log2(e) [Np] fp32 and an fp32 dQ accumulator [Np][d].
  * Returns 0 for invalid sizes.
@@ -92,6 +101,17 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
                  void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                  float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * Backward pass with grouped-query / multi-query attention: as fa_bwd, with K, V, dK, dV of
+ * Hkv heads ([B][Hkv][N][d]). dK and dV of a key/value head are the sums over the query heads
+ * that read it (the gradient of a shared operand). The workspace is the one of
+ * fa_bwd_workspace_size(B, H, N, d) (per query head). Launches three kernels.
+ */
+FA_API fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                            const float* L, void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                            int B, int H, int Hkv, int N, int d, float scale, int causal, fa_dtype dtype,
+                            void* stream);
 
 /*
  * Stage 1 of fa_bwd: D_i = sum_k dO_ik O_ik (the N x d identity that replaces the N x N

@@ -110,3 +110,13 @@ def test_oracle_is_not_imported_by_the_product():
                 txt = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", txt, re.M), f
                 assert "oracle/" not in txt, f
+
+
+def test_gqa_head_counts_are_validated(lib):
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, i, vp]
+    lib.fa_last_error_message.restype = ctypes.c_char_p
+    g = vp(0x10000)
+    assert lib.fa_fwd_gqa(g, g, g, g, g, 1, 4, 3, 128, 64, 0.125, 0, 0, None) == 1
+    assert b"multiple" in lib.fa_last_error_message()
+    assert lib.fa_fwd_gqa(g, g, g, g, g, 1, 4, 0, 128, 64, 0.125, 0, 0, None) == 1
