@@ -394,3 +394,52 @@ def test_planted_gqa_backward_without_group_sum_fails_fd():
     wrong = dk_e[:, :1]  # slip: only the first query head's contribution
     _, fk, _ = _fd_grads(q, k, v, do, 0.7, False, fwd=G.attn_fwd64_gqa)
     assert np.abs(wrong - fk).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
+# decoding over a long cache, split into pieces and merged (Flash-Decoding)
+# --------------------------------------------------------------------------
+
+from oracle import decode as DEC  # noqa: E402
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 40])
+def test_split_kv_merge_equals_whole_cache(splits):
+    rng = np.random.default_rng(31 + splits)
+    q = rng.standard_normal((2, 4, 3, 8))
+    k, v = rng.standard_normal((2, 2, 37, 8)) * 2, rng.standard_normal((2, 2, 37, 8))
+    o_ref, l_ref = DEC.decode_fwd64(q, k, v, 0.4)
+    o, lse = DEC.merge_splits64(DEC.split_kv_states64(q, k, v, 0.4, splits))
+    np.testing.assert_allclose(o, o_ref, atol=1e-14)
+    np.testing.assert_allclose(lse, l_ref, atol=1e-13)
+
+
+def test_decode_is_attention_over_the_whole_cache():
+    # one query row equal to the last row of a square problem: same output as that row
+    rng = np.random.default_rng(41)
+    q, k, v = (rng.standard_normal((1, 2, 20, 6)) for _ in range(3))
+    o_full, l_full = oracle.attn_fwd64(q, k, v, 0.5, False)
+    o, lse = DEC.decode_fwd64(q[:, :, -1:], k, v, 0.5)
+    np.testing.assert_allclose(o[:, :, 0], o_full[:, :, -1], atol=1e-15)
+    np.testing.assert_allclose(lse[:, :, 0], l_full[:, :, -1], atol=1e-15)
+    # a single cached key: O = V, L = τ q·k
+    o1, l1 = DEC.decode_fwd64(q[:, :, :3], k[:, :, :1], v[:, :, :1], 0.5)
+    np.testing.assert_array_equal(o1, np.broadcast_to(v[:, :, :1], o1.shape))
+    np.testing.assert_allclose(l1, 0.5 * (q[:, :, :3] @ k[:, :, 0, :, None])[..., 0], atol=1e-15)
+
+
+def test_split_bounds_cover_the_cache():
+    for nk, s in [(1, 1), (10, 3), (4097, 16), (5, 8)]:
+        b = DEC.split_bounds(nk, s)
+        assert b[0][0] == 0 and b[-1][1] == nk and len(b) == s
+        assert all(b[i][1] == b[i + 1][0] for i in range(s - 1))
+
+
+def test_planted_merge_without_rescale_fails():
+    rng = np.random.default_rng(43)
+    q = rng.standard_normal((1, 1, 1, 4))
+    k, v = rng.standard_normal((1, 1, 10, 4)) * 3, rng.standard_normal((1, 1, 10, 4))
+    (m1, l1, o1), (m2, l2, o2) = DEC.split_kv_states64(q, k, v, 1.0, 2)
+    wrong = (l1 * o1 + l2 * o2) / (l1 + l2)  # slip: partial states not brought to a common maximum
+    o_ref, _ = DEC.decode_fwd64(q, k, v, 1.0)
+    assert np.abs(wrong - o_ref).max() > 1e-3
