@@ -19,8 +19,8 @@ __all__ = [
     "FAError", "library_path", "load_library", "DTYPE_CODES",
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
-    "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "attention_forward",
-    "attention_backward", "EXPORTED_SYMBOLS",
+    "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
+    "attention_forward", "attention_backward", "attention_decode", "EXPORTED_SYMBOLS",
     "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -33,7 +33,7 @@ DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 EXPORTED_SYMBOLS = (
     "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
-    "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa",
+    "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
 )
 
 _lib = None
@@ -73,6 +73,9 @@ def load_library():
         lib.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, f, i, i, vp]
         lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
         lib.fa_bwd_gqa.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, vp]
+        lib.fa_decode_workspace_size.argtypes = [i] * 7
+        lib.fa_decode_workspace_size.restype = sz
+        lib.fa_decode.argtypes = [vp] * 5 + [i] * 6 + [f, i, i, vp, sz, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
         lib.fa_uses_tensor_cores.argtypes = [i, i, i]
@@ -80,7 +83,7 @@ def load_library():
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_error_message.argtypes = []
         lib.fa_last_error_message.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_bwd_noalloc", "fa_bwd_preprocess",
+        for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_bwd_noalloc", "fa_bwd_preprocess",
                      "fa_bwd_main", "fa_bwd_dq_convert",
                      "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
             getattr(lib, name).restype = ctypes.c_int
@@ -210,6 +213,24 @@ def fa_bwd_noalloc(Q, K, V, O, dO, L, dQ, dK, dV, scale, causal, stream=None):
                                          d, float(scale), int(bool(causal)), _dt(Q), _stream(stream)))
 
 
+def fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d, splits=0) -> int:
+    return int(load_library().fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d, int(splits)))
+
+
+def fa_decode(Q, K, V, O, L, scale, splits=0, workspace=None, stream=None):
+    """Decode: Q, O [B, H, Nq, d] against the cache K, V [B, Hkv, Nk, d]; L [B, H, Nq]."""
+    B, H, Nq, d = _shape4(Q)
+    Bk, Hkv, Nk, dk = _shape4(K)
+    if (Bk, dk) != (B, d) or V.shape != K.shape or V.dtype != Q.dtype or K.dtype != Q.dtype or not V.is_contiguous():
+        raise ValueError("K, V must be [B, Hkv, Nk, d] of Q's dtype")
+    _same(Q, O)
+    if L.dtype != torch.float32 or L.numel() != B * H * Nq or not L.is_contiguous():
+        raise ValueError("L must be a contiguous fp32 tensor of B*H*Nq elements")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().fa_decode(_p(Q), _p(K), _p(V), _p(O), _p(L), B, H, Hkv, Nq, Nk, d, float(scale), int(splits),
+                                    _dt(Q), _p(workspace), nbytes, _stream(stream)))
+
+
 def fa_check_device_error(stream=None):
     _check(load_library().fa_check_device_error(_stream(stream)))
 
@@ -264,3 +285,16 @@ def attention_backward(q, k, v, o, do, lse, causal=False, scale=None, workspace=
     else:
         fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)
     return dq, dk, dv
+
+
+def attention_decode(q, k, v, scale=None, splits=0, stream=None):
+    """O, L = fa_decode(q, k, v) for q [B, H, Nq, d] over the cache k, v [B, Hkv, Nk, d]."""
+    B, H, Nq, d = _shape4(q)
+    _, Hkv, Nk, _ = _shape4(k)
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    nbytes = fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d, splits)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+    fa_decode(q, k, v, o, lse, scale, splits, ws, stream)
+    return o, lse

@@ -276,6 +276,73 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                     stream);
 }
 
+// Effective number of cache splits: 0 or less picks automatically; never more than Nk.
+static int decode_splits(int B, int H, int Hkv, int Nq, int Nk, int splits) {
+  int s = splits > 0 ? splits : decode_auto_splits(B, H, Hkv, Nq, Nk);
+  if (s > Nk) s = Nk;
+  if (s > 4096) s = 4096;
+  return s < 1 ? 1 : s;
+}
+
+static fa_status check_decode(int B, int H, int Hkv, int Nq, int Nk, int d, fa_dtype dtype, bool* empty) {
+  *empty = false;
+  if (dtype != FA_BF16 && dtype != FA_FP16 && dtype != FA_FP32)
+    return fail(FA_ERR_UNSUPPORTED, "unknown dtype %d", (int)dtype);
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return fail(FA_ERR_INVALID_ARG, "negative size");
+  if (d != 64 && d != 128 && d != 256) return fail(FA_ERR_UNSUPPORTED, "decode supports d in {64, 128, 256}, got %d", d);
+  if ((int64_t)B * H * Nq == 0) {
+    *empty = true;
+    return FA_OK;
+  }
+  fa_status st = check_heads(H, Hkv);
+  if (st != FA_OK) return st;
+  if (Nk < 1) return fail(FA_ERR_INVALID_ARG, "decode needs at least one cached key (Nk=%d)", Nk);
+  if ((double)B * Hkv * Nk * d > 4.0e15 || (double)B * H * Nq * d > 4.0e15)
+    return fail(FA_ERR_INVALID_ARG, "problem too large");
+  return FA_OK;
+}
+
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, int splits) {
+  bool empty;
+  if (check_decode(B, H, Hkv, Nq, Nk, d, FA_BF16, &empty) != FA_OK || empty) return 0;
+  return decode_workspace_bytes(B, H, Nq, d, decode_splits(B, H, Hkv, Nq, Nk, splits));
+}
+
+fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv, int Nq,
+                    int Nk, int d, float scale, int splits, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  bool empty;
+  fa_status st = check_decode(B, H, Hkv, Nq, Nk, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if ((st = check_ptrs({Q, K, V, O, L}, "fa_decode")) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  DecodeArgs a{};
+  a.q = Q;
+  a.k = K;
+  a.v = V;
+  a.o = O;
+  a.lse = L;
+  a.b = B;
+  a.h = H;
+  a.hkv = Hkv;
+  a.nq = Nq;
+  a.nk = Nk;
+  a.d = d;
+  a.scale = scale;
+  a.splits = decode_splits(B, H, Hkv, Nq, Nk, splits);
+  a.dtype = (int)dtype;
+  a.stream = static_cast<cudaStream_t>(stream);
+  const size_t need = decode_workspace_bytes(B, H, Nq, d, a.splits);
+  if (need > 0) {
+    if (!workspace || !aligned16(workspace))
+      return fail(FA_ERR_INVALID_ARG, "fa_decode: %d splits need a 16-byte-aligned workspace", a.splits);
+    if (workspace_bytes < need)
+      return fail(FA_ERR_INVALID_ARG, "fa_decode: workspace of %zu bytes < %zu required", workspace_bytes, need);
+    a.ws = static_cast<float*>(workspace);
+  }
+  return launched(launch_decode(a), "fa_decode");
+}
+
 fa_status fa_check_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));

@@ -57,6 +57,24 @@ struct BwdArgs {
   int group = 1;  // query heads per key/value head: K, V, dK, dV hold bh / group heads
 };
 
+// Decode over a key/value cache: Q, O [b][h][nq][d], K, V [b][hkv][nk][d], L [b][h][nq].
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  float* ws;  // splits > 1: [b*h*nq][splits][d] split outputs, then [b*h*nq][splits] base-2 LSEs
+  int b, h, hkv, nq, nk, d;
+  float scale;
+  int splits;
+  int dtype;
+  cudaStream_t stream;
+};
+int decode_auto_splits(int b, int h, int hkv, int nq, int nk);
+size_t decode_workspace_bytes(int b, int h, int nq, int d, int splits);
+cudaError_t launch_decode(const DecodeArgs& a);
+
 // Records the calling thread's last error message (read by fa_last_error_message) and
 // returns `status`.
 int set_last_error(int status, const char* fmt, ...);

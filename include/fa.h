@@ -160,6 +160,28 @@ FA_API fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, con
                                 int causal, fa_dtype dtype, void* stream);
 
 /*
+ * Decode attention over a key/value cache with the cache split across thread blocks
+ * ("Lecture 8" §8.2: the cache is cut into pieces processed in parallel and the partial
+ * results are combined with the online-softmax merge of Exercise 3).
+ *   Q        in:  [B][H][Nq][d] dtype, the new query rows
+ *   K, V     in:  [B][Hkv][Nk][d] dtype, the cache (H a multiple of Hkv; query head h reads
+ *                 key/value head h / (H / Hkv))
+ *   O, L     out: [B][H][Nq][d] dtype and [B][H][Nq] fp32; every query row attends to all Nk
+ *                 cached keys (no mask)
+ *   d        64, 128 or 256; Nk >= 1
+ *   splits   number of cache pieces; <= 0 chooses automatically; capped at Nk
+ *   workspace  fa_decode_workspace_size(...) bytes for the same arguments (0 when there is a
+ *            single piece: then workspace may be NULL)
+ * Launches one kernel, plus one merge kernel when there is more than one piece. Runs on CUDA
+ * cores: the kernel reads each cached key and value once and is bound by HBM bandwidth.
+ */
+FA_API size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, int splits);
+FA_API fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv,
+                           int Nq, int Nk, int d, float scale, int splits, fa_dtype dtype, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream` and reports device-side failures/*
  * Synchronises `stream` and reports device-side failures of earlier calls on the
  * current device: FA_ERR_CUDA for a CUDA error, FA_ERR_TIMEOUT / FA_ERR_DEVICE for a
  * failure a kernel recorded. The recorded failure is cleared.

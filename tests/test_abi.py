@@ -120,3 +120,14 @@ def test_gqa_head_counts_are_validated(lib):
     assert lib.fa_fwd_gqa(g, g, g, g, g, 1, 4, 3, 128, 64, 0.125, 0, 0, None) == 1
     assert b"multiple" in lib.fa_last_error_message()
     assert lib.fa_fwd_gqa(g, g, g, g, g, 1, 4, 0, 128, 64, 0.125, 0, 0, None) == 1
+
+
+def test_decode_workspace_size_host_rules(lib):
+    lib.fa_decode_workspace_size.argtypes = [ctypes.c_int] * 7
+    lib.fa_decode_workspace_size.restype = ctypes.c_size_t
+    f = lib.fa_decode_workspace_size
+    assert f(1, 8, 2, 1, 100, 128, 1) == 0  # one piece: no workspace
+    assert f(2, 8, 2, 3, 1000, 64, 5) == 2 * 8 * 3 * 5 * 65 * 4
+    assert f(1, 8, 3, 1, 100, 128, 4) == 0  # heads do not divide: invalid
+    assert f(1, 8, 2, 1, 100, 96, 4) == 0  # unsupported head dim
+    assert f(1, 8, 2, 1, 1 << 20, 128, 0) > 0  # long cache: split automatically
