@@ -1,5 +1,6 @@
 // C ABI (include/fa.h): argument validation, workspace carving, kernel selection.
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -276,9 +277,11 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                     stream);
 }
 
-// Effective number of cache splits: 0 or less picks automatically; never more than Nk.
-static int decode_splits(int B, int H, int Hkv, int Nq, int Nk, int splits) {
-  int s = splits > 0 ? splits : decode_auto_splits(B, H, Hkv, Nq, Nk);
+// Effective number of cache splits: 0 or less picks automatically (for the kernel that runs);
+// never more than Nk.
+static int decode_splits(int B, int H, int Hkv, int Nq, int Nk, int d, int splits, bool tc) {
+  int s = splits > 0 ? splits
+                     : (tc ? decode_tc_auto_splits(B, H, Hkv, Nq, Nk, d) : decode_auto_splits(B, H, Hkv, Nq, Nk));
   if (s > Nk) s = Nk;
   if (s > 4096) s = 4096;
   return s < 1 ? 1 : s;
@@ -305,7 +308,9 @@ static fa_status check_decode(int B, int H, int Hkv, int Nq, int Nk, int d, fa_d
 size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, int splits) {
   bool empty;
   if (check_decode(B, H, Hkv, Nq, Nk, d, FA_BF16, &empty) != FA_OK || empty) return 0;
-  return decode_workspace_bytes(B, H, Nq, d, decode_splits(B, H, Hkv, Nq, Nk, splits));
+  // enough for either kernel (the size does not depend on the dtype)
+  const int s = std::max(decode_splits(B, H, Hkv, Nq, Nk, d, splits, true), decode_splits(B, H, Hkv, Nq, Nk, d, splits, false));
+  return decode_workspace_bytes(B, H, Nq, d, s);
 }
 
 fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv, int Nq,
@@ -329,9 +334,14 @@ fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float*
   a.nk = Nk;
   a.d = d;
   a.scale = scale;
-  a.splits = decode_splits(B, H, Hkv, Nq, Nk, splits);
+  const bool tc = decode_tc_supported((int)dtype, d, (int64_t)B * H * Nq);
+  a.splits = decode_splits(B, H, Hkv, Nq, Nk, d, splits, tc);
   a.dtype = (int)dtype;
   a.stream = static_cast<cudaStream_t>(stream);
+  DeviceSyms syms;
+  if ((st = device_syms(&syms)) != FA_OK) return st;
+  a.err = syms.err;
+  a.counter = syms.counter;
   const size_t need = decode_workspace_bytes(B, H, Nq, d, a.splits);
   if (need > 0) {
     if (!workspace || !aligned16(workspace))
@@ -340,7 +350,7 @@ fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float*
       return fail(FA_ERR_INVALID_ARG, "fa_decode: workspace of %zu bytes < %zu required", workspace_bytes, need);
     a.ws = static_cast<float*>(workspace);
   }
-  return launched(launch_decode(a), "fa_decode");
+  return launched(tc ? launch_decode_tc(a) : launch_decode(a), "fa_decode");
 }
 
 fa_status fa_check_device_error(void* stream) {

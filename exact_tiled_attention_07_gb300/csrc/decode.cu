@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(256) decode_merge(const float* __restrict__ ws
 #pragma unroll
   for (int e = 0; e < PL; ++e) acc[e] = 0.f;
   float den = 0.f;
+  // the splits' loads are independent: unrolled so several are in flight at once
+#pragma unroll 4
   for (int s = 0; s < splits; ++s) {
     const float ls = lr[s];
     const float w = (ls == -INFINITY) ? 0.f : ex2f(ls - mx);
@@ -308,9 +310,27 @@ cudaError_t launch_decode_t(const DecodeArgs& a) {
                                                        ws_o, ws_l, a.h, a.hkv, a.nq, a.nk, a.splits, row_blocks,
                                                        a.scale * 1.4426950408889634f);
   if ((e = cudaGetLastError()) != cudaSuccess || a.splits == 1) return e;
+  return launch_decode_merge(a);
+}
+
+template <typename T, int D>
+cudaError_t launch_merge_t(const DecodeArgs& a) {
+  const int64_t rows = (int64_t)a.b * a.h * a.nq;
+  const float* ws_o = a.ws;
+  const float* ws_l = a.ws + rows * a.splits * D;
   decode_merge<T, D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, a.stream>>>(ws_o, ws_l, (T*)a.o, a.lse, rows,
                                                                                   a.splits);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_merge_d(const DecodeArgs& a) {
+  switch (a.d) {
+    case 64: return launch_merge_t<T, 64>(a);
+    case 128: return launch_merge_t<T, 128>(a);
+    case 256: return launch_merge_t<T, 256>(a);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 template <typename T>
@@ -330,7 +350,7 @@ int decode_auto_splits(int b, int h, int hkv, int nq, int nk) {
   const int64_t base = (int64_t)b * hkv * rb;
   // about two full waves of two CTAs per SM on a 152-SM GB300, rounded down so the last wave
   // is not a small remainder
-  const int64_t target = 4 * 152;
+  const int64_t target = 4 * kSmCount;
   int64_t s = target / base;
   s = std::min<int64_t>(s, (nk + 255) / 256);  // at least ~256 keys per split
   s = std::min<int64_t>(std::max<int64_t>(s, 1), 128);
@@ -347,6 +367,14 @@ cudaError_t launch_decode(const DecodeArgs& a) {
     case DT_BF16: return launch_decode_d<__nv_bfloat16>(a);
     case DT_FP16: return launch_decode_d<__half>(a);
     default: return launch_decode_d<float>(a);
+  }
+}
+
+cudaError_t launch_decode_merge(const DecodeArgs& a) {
+  switch (a.dtype) {
+    case DT_BF16: return launch_merge_d<__nv_bfloat16>(a);
+    case DT_FP16: return launch_merge_d<__half>(a);
+    default: return launch_merge_d<float>(a);
   }
 }
 

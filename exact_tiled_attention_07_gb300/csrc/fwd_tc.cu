@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const int vidx = 2 * j + 1;
           const uint32_t buf = (j & 1) ? C::S_COL1 : C::S_COL0;
           if (!(ok = wait_full(vidx))) break;
-          if (!(ok = wait(B.p_full + 0, j & 1, 24))) break;
+          if (!(ok = wait(B.p_full + (j & 1), (j >> 1) & 1, 24))) break;
           tc_fence_after();
           issue_pv(C::O_COL0, buf, vidx, j > 0);
           commit(B.pv_done);
@@ -412,7 +412,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(B.p_full + q);
+      // NQ = 1: one barrier per S buffer; with a single one the softmax could finish blocks j
+      // and j + 1 while the MMA warp still waits for V_j, and its parity wait on phase j would
+      // then see phase j + 1
+      mbar_arrive(B.p_full + (C::NQ == 2 ? q : (j & 1)));
     }
     // epilogue: O / l -> global (16-bit), L = (m + log2 l) ln 2
     if (ok && nb > 0) {

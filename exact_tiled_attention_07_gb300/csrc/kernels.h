@@ -70,10 +70,18 @@ struct DecodeArgs {
   int splits;
   int dtype;
   cudaStream_t stream;
+  unsigned long long* err = nullptr;      // device error word (tensor-core path)
+  unsigned long long* counter = nullptr;  // device count of processed (row tile, key tile) pairs
 };
+// Streaming multiprocessors of a GB300, for sizing grids.
+constexpr int kSmCount = 152;
 int decode_auto_splits(int b, int h, int hkv, int nq, int nk);
+int decode_tc_auto_splits(int b, int h, int hkv, int nq, int nk, int d);
+bool decode_tc_supported(int dtype, int d, int64_t q_rows);
 size_t decode_workspace_bytes(int b, int h, int nq, int d, int splits);
-cudaError_t launch_decode(const DecodeArgs& a);
+cudaError_t launch_decode(const DecodeArgs& a);     // CUDA cores, any dtype
+cudaError_t launch_decode_tc(const DecodeArgs& a);  // tensor cores, bf16/fp16
+cudaError_t launch_decode_merge(const DecodeArgs& a);
 
 // Records the calling thread's last error message (read by fa_last_error_message) and
 // returns `status`.

@@ -75,3 +75,52 @@ def test_decode_workspace_rules(fa):
     o, lse = torch.empty_like(q), torch.empty((1, 8, 1), dtype=torch.float32, device="cuda")
     with pytest.raises(fa.FAError, match="workspace"):
         fa.fa_decode(q, k, k, o, lse, 0.1, splits=4, workspace=None)
+
+
+@pytest.mark.parametrize("h,hkv,nq,nk,splits", [(64, 1, 3, 1000, 0), (8, 2, 40, 300, 0), (8, 2, 40, 300, 2),
+                                                (16, 16, 1, 300, 10), (4, 1, 64, 129, 0), (8, 1, 5, 700, 0),
+                                                (16, 2, 8, 1000, 3), (8, 8, 1, 129, 2)])
+def test_decode_row_tiles_and_empty_pieces(fa, h, hkv, nq, nk, splits):
+    # group x Nq above 128 rows (several row tiles per key/value head), 33..64 rows (two
+    # copies of the rows on the tensor-core path) and <= 32 rows (four copies); more pieces
+    # than key tiles (empty pieces); a one-key last tile, alone in its piece, so that three
+    # of the four row copies see no key there
+    _check(fa, 2, h, hkv, nq, nk, 128, "bf16", splits, 400 + h + nq)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("nq", [1, 5, 20])
+def test_decode_row_copies_per_head_dim(fa, d, nq):
+    # 8 query heads on one key/value head: 8, 40 and 160 rows
+    _check(fa, 1, 8, 1, nq, 777, d, "fp16", 0, 700 + d + nq)
+
+
+def test_decode_visits_every_key_tile_once_per_row_tile(fa):
+    b, h, hkv, nq, nk, d = 2, 16, 4, 2, 1000, 64
+    x = _inputs(b, h, hkv, nq, nk, d, "bf16", 500)
+    dev = {k: to_device(v, "bf16") for k, v in x.items()}
+    fa.fa_tile_counter(reset=True)
+    fa.attention_decode(dev["q"], dev["k"], dev["v"], splits=3)
+    torch.cuda.synchronize()
+    rows = (h // hkv) * nq
+    assert fa.fa_tile_counter() == b * hkv * ((rows + 127) // 128) * ((nk + 127) // 128)
+
+
+def test_decode_long_cache_sampled_heads(fa):
+    # a decode step of the size the benchmark times (B 8, H 32, Hkv 8, Nk 32768, d 128),
+    # checked on sampled heads against attention over the whole cache
+    b, h, hkv, nq, nk, d = 8, 32, 8, 1, 32768, 128
+    x = _inputs(b, h, hkv, nq, nk, d, "bf16", 600)
+    dev = {k: to_device(v, "bf16") for k, v in x.items()}
+    o, lse = fa.attention_decode(dev["q"], dev["k"], dev["v"])
+    fa.fa_check_device_error()
+    go, gl = to_f64(o), to_f64(lse)
+    group = h // hkv
+    for bi, hi in [(0, 0), (0, 31), (3, 9), (7, 20), (5, 4)]:
+        kv = hi // group
+        o_ref, l_ref = DEC.decode_fwd64(to_float64(x["q"][bi:bi + 1, hi:hi + 1], "bf16"),
+                                        to_float64(x["k"][bi:bi + 1, kv:kv + 1], "bf16"),
+                                        to_float64(x["v"][bi:bi + 1, kv:kv + 1], "bf16"), d ** -0.5)
+        assert max_abs(go[bi, hi], o_ref[0, 0]) <= TOL_O_MAXABS
+        assert rel_rms(go[bi, hi], o_ref[0, 0]) <= TOL_O_RELRMS
+        assert max_abs(gl[bi, hi], l_ref[0, 0]) <= TOL_L_MAXABS
