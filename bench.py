@@ -1,7 +1,8 @@
 """Benchmark: attention forward + backward TFLOP/s on GB300 through the C ABI.
 
 One step = the whole hot path over one batch: fa_fwd, then the three backward stages
-(fa_bwd_preprocess, fa_bwd_main, fa_bwd_dq_convert).  Default workload: the causal LM
+(fa_bwd_preprocess, fa_bwd_main, fa_bwd_dq_convert).  The line also carries a split-KV
+decode measurement (``decode``: fa_decode over a 1.07 GB key/value cache, HBM-bound).  Default workload: the causal LM
 shape B=8, H=16, N=4096, d=128, bf16 (FLOPs: forward 4·B·H·N²·d, backward 2.5x, halved
 for causal).  Inputs are larger than L2 (each [B,H,N,d] tensor is 134 MB).
 
@@ -29,7 +30,14 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from exact_tiled_attention_07_gb300.inputs import WORKLOADS, Workload, attention_flops, make_inputs  # noqa: E402
+from exact_tiled_attention_07_gb300.inputs import (  # noqa: E402
+    DECODE_WORKLOADS,
+    WORKLOADS,
+    Workload,
+    attention_flops,
+    make_decode_inputs,
+    make_inputs,
+)
 
 METRIC = "attention fwd/bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "causal_lm_bf16"
@@ -241,6 +249,49 @@ def _dev_tensor(stored, dtype, device):
     return t.pin_memory().to(device, non_blocking=False), t.pin_memory()
 
 
+def measure_decode(binding, device, peaks, peak_src, reps=50):
+    """Split-KV decode over a key/value cache larger than L2: HBM bytes per second of one
+    fa_decode call (the partial kernel and the merge), against the measured HBM bandwidth."""
+    import torch
+
+    w = DECODE_WORKLOADS["decode_gqa_bf16"]
+    x = make_decode_inputs(w)
+    q, k, v = (_dev_tensor(x[n], w.dtype, device)[0] for n in ("q", "k", "v"))
+    del x
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=device)
+    nbytes = binding.fa_decode_workspace_size(w.B, w.H, w.Hkv, w.Nq, w.Nk, w.d, 0)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+    def call():
+        binding.fa_decode(q, k, v, o, lse, w.scale, 0, ws)
+
+    for _ in range(5):
+        call()
+    binding.fa_check_device_error()
+    stream = torch.cuda.current_stream()
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(2_000_000)  # the first calls are queued before the start event fires
+    a_.record(stream)
+    for _ in range(reps):
+        call()
+    b_.record(stream)
+    torch.cuda.synchronize()
+    binding.fa_check_device_error()
+    us = a_.elapsed_time(b_) / reps * 1e3
+    gbs = w.bytes_moved() / (us * 1e-6) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+            "dtype": w.dtype, "us_per_call": us, "calls": reps, "launches_per_call": 2,
+            "roofline": {"kernel": "decode_tc_kernel + decode_merge", "bound": "hbm", "achieved": gbs,
+                         "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": profiled_traffic("decode_tc", w.name),
+                         "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)",
+                         "algorithmic_bytes": w.bytes_moved()},
+            "l2": "cache of 1.07 GB, larger than L2 (no flush)"}
+
+
 def run_gpu(args, w: Workload):
     import torch
 
@@ -397,6 +448,10 @@ def run_gpu(args, w: Workload):
                                              "pct_of_sustained_peak": 100 * tf / peak_sus}
         binding.fa_check_device_error()
 
+    decode = None
+    if not args.no_decode:
+        decode = measure_decode(binding, device, peaks, peak_src)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(w)
@@ -408,7 +463,8 @@ def run_gpu(args, w: Workload):
                 "pct_of_peak": {"sustained": 100 * value / world / peak_sus, "burst": 100 * value / world / peak_burst,
                                 "source": peak_src},
                 "kernels_ms": per_kernel, "gpu_launches": len(names) * args.steps, "roofline": roofline,
-                "e2e": e2e, "clocks": clocks.summary(wall0, wall1), "cpu_baseline": cpu, "targets": targets}
+                "e2e": e2e, "clocks": clocks.summary(wall0, wall1), "cpu_baseline": cpu, "targets": targets,
+                "decode": decode}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -423,6 +479,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-targets", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]

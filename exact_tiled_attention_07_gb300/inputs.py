@@ -16,6 +16,12 @@ Workloads (shapes B, H, N, d; all scale τ = 1/√d):
   K[..., j, 0] = c_j·√d, so τ·q_i·k_j gains exactly c_j (stresses rescaling)
 * ``hd256_bf16``      4, 16, 16384, 256, bf16, non-causal, forward only, N(0,1)
 
+Decode workloads (``DECODE_WORKLOADS``: new query rows Q [B, H, Nq, d] against a key/value
+cache K, V [B, Hkv, Nk, d]):
+
+* ``decode_gqa_bf16`` 8, 32 query heads on 8 key/value heads, 1 new row, 32768 cached
+  keys, d = 128, bf16, N(0,1), seed 600 (a 1.07 GB cache, larger than L2)
+
 Random numbers come from numpy's PCG64 generator, drawn in float32 in the
 order Q, K, V, dO, then the key offsets.
 """
@@ -27,7 +33,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "round_to_dtype", "to_float64",
+__all__ = ["Workload", "WORKLOADS", "DecodeWorkload", "DECODE_WORKLOADS", "make_decode_inputs", "make_inputs", "round_to_dtype", "to_float64",
            "bf16_bits_from_f32", "f32_from_bf16_bits", "attention_flops"]
 
 DTYPES = ("fp32", "fp16", "bf16")
@@ -130,6 +136,43 @@ def make_inputs(w: Workload, with_do: bool = True) -> dict:
     elif w.dist != "normal":
         raise ValueError(f"unknown distribution {w.dist!r}")
     return {nm: round_to_dtype(a, w.dtype) for nm, a in raw.items()}
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    dtype: str = "bf16"
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def bytes_moved(self) -> int:
+        """Compulsory HBM bytes of one decode step: read Q, K, V; write O (dtype) and L (fp32)."""
+        e = 4 if self.dtype == "fp32" else 2
+        rows = self.B * self.H * self.Nq
+        return e * (2 * self.B * self.Hkv * self.Nk * self.d + 2 * rows * self.d) + 4 * rows
+
+
+DECODE_WORKLOADS = {
+    "decode_gqa_bf16": DecodeWorkload("decode_gqa_bf16", 8, 32, 8, 1, 32768, 128, "bf16", 600),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload) -> dict:
+    """Draw Q [B, H, Nq, d] and the cache K, V [B, Hkv, Nk, d], N(0,1), rounded to ``w.dtype``."""
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    out = {}
+    for name, shape in (("q", (w.B, w.H, w.Nq, w.d)), ("k", (w.B, w.Hkv, w.Nk, w.d)), ("v", (w.B, w.Hkv, w.Nk, w.d))):
+        out[name] = round_to_dtype(rng.standard_normal(shape, dtype=np.float32), w.dtype)
+    return out
 
 
 def attention_flops(B, H, N, d, causal, pass_="fwd"):

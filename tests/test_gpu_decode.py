@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 from oracle import decode as DEC
-from exact_tiled_attention_07_gb300.inputs import round_to_dtype, to_float64
+from exact_tiled_attention_07_gb300.inputs import DECODE_WORKLOADS, make_decode_inputs, round_to_dtype, to_float64
 from helpers import TOL_FP32, TOL_L_MAXABS, TOL_O_MAXABS, TOL_O_RELRMS, max_abs, rel_rms, to_device, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -107,10 +107,11 @@ def test_decode_visits_every_key_tile_once_per_row_tile(fa):
 
 
 def test_decode_long_cache_sampled_heads(fa):
-    # a decode step of the size the benchmark times (B 8, H 32, Hkv 8, Nk 32768, d 128),
-    # checked on sampled heads against attention over the whole cache
-    b, h, hkv, nq, nk, d = 8, 32, 8, 1, 32768, 128
-    x = _inputs(b, h, hkv, nq, nk, d, "bf16", 600)
+    # the decode step the benchmark times (B 8, H 32, Hkv 8, Nk 32768, d 128), in the launch
+    # configuration it uses, checked on sampled heads against attention over the whole cache
+    w = DECODE_WORKLOADS["decode_gqa_bf16"]
+    b, h, hkv, nq, nk, d = w.B, w.H, w.Hkv, w.Nq, w.Nk, w.d
+    x = make_decode_inputs(w)
     dev = {k: to_device(v, "bf16") for k, v in x.items()}
     o, lse = fa.attention_decode(dev["q"], dev["k"], dev["v"])
     fa.fa_check_device_error()
