@@ -443,3 +443,118 @@ def test_planted_merge_without_rescale_fails():
     wrong = (l1 * o1 + l2 * o2) / (l1 + l2)  # slip: partial states not brought to a common maximum
     o_ref, _ = DEC.decode_fwd64(q, k, v, 1.0)
     assert np.abs(wrong - o_ref).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) block quantisation and the attention it feeds
+# --------------------------------------------------------------------------
+
+from oracle import fp8 as F8  # noqa: E402
+
+
+def test_e4m3_value_set_from_the_format():
+    v = F8.e4m3_values()
+    assert len(v) == 127  # zero, 7 subnormals, 15 binades x 8 mantissas minus the NaN code
+    assert v[0] == 0 and v[1] == 2.0 ** -9 and v[7] == 7 * 2.0 ** -9 and v[8] == 2.0 ** -6
+    assert v[-1] == 448.0 and v[-2] == 416.0
+    assert np.all(np.diff(v) > 0)
+
+
+def test_e4m3_round_fixes_values_and_takes_ties_to_even():
+    v = F8.e4m3_values()
+    np.testing.assert_array_equal(F8.e4m3_round(v), v)
+    np.testing.assert_array_equal(F8.e4m3_round(-v[1:]), -v[1:])
+    mid = (v[:-1] + v[1:]) / 2
+    # codes ascend with the value and the mantissa is the code's low 3 bits: the even-index
+    # neighbour has the even mantissa
+    want = np.where(np.arange(len(mid)) % 2 == 0, v[:-1], v[1:])
+    np.testing.assert_array_equal(F8.e4m3_round(mid), want)
+    # just off the midpoints: the nearer neighbour
+    np.testing.assert_array_equal(F8.e4m3_round(mid * (1 - 1e-9)), v[:-1])
+    np.testing.assert_array_equal(F8.e4m3_round(mid * (1 + 1e-9)), v[1:])
+    # saturation (satfinite): everything above 448 is 448
+    np.testing.assert_array_equal(F8.e4m3_round([449.0, 470.0, 1e6, -1e6]), [448.0, 448.0, 448.0, -448.0])
+    assert F8.e4m3_round(2.0 ** -11) == 0.0 and F8.e4m3_round(3 * 2.0 ** -11) == 2.0 ** -9
+
+
+def test_e4m3_round_matches_the_torch_float8_conversion():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8 dtype in this torch")
+    rng = np.random.default_rng(71)
+    x = np.concatenate([rng.standard_normal(20000) * s for s in (1e-3, 0.05, 1.0, 30.0, 150.0)])
+    x = x[np.abs(x) <= 448.0]
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(F8.e4m3_round(x.astype(np.float32)), ref)
+
+
+def test_block_quantisation_scales_each_block_to_the_format_range():
+    rng = np.random.default_rng(72)
+    x = rng.standard_normal((2, 3, 300, 16)) * rng.uniform(0.01, 100, size=(2, 3, 1, 1))
+    codes, scales = F8.quantize_blocks(x)
+    assert scales.shape == (2, 3, 3) and scales.dtype == np.float32
+    for b in range(3):
+        blk = codes[:, :, b * 128:(b + 1) * 128]
+        np.testing.assert_array_equal(np.abs(blk).max(axis=(-2, -1)), 448.0)  # each block's amax maps to 448
+        np.testing.assert_array_equal(F8.e4m3_round(blk), blk)  # codes are E4M3 values
+        np.testing.assert_allclose(scales[..., b], np.abs(x[:, :, b * 128:(b + 1) * 128]).max(axis=(-2, -1)) / 448,
+                                   rtol=1e-7)
+    deq = F8.dequantize_blocks(codes, scales)
+    # E4M3 keeps 3 mantissa bits: relative error <= 2^-4 above the subnormal range
+    big = np.abs(x) >= np.repeat(scales, 128, axis=-1)[..., :300, None] * 2.0 ** -6
+    assert np.all(np.abs(deq - x)[big] <= 2.0 ** -4 * np.abs(x)[big] * (1 + 1e-6))
+    # zero block: scale 1, codes 0
+    z_codes, z_scales = F8.quantize_blocks(np.zeros((1, 1, 5, 8)))
+    assert z_scales[0, 0, 0] == 1.0 and not z_codes.any()
+
+
+def test_block_quantisation_beats_one_scale_per_tensor():
+    # blocks of very different magnitude (the case block quantisation is for): one scale for
+    # the whole tensor pushes the small blocks into the subnormal range
+    rng = np.random.default_rng(73)
+    mags = np.array([1e-3, 1.0, 50.0, 1e-2])
+    x = rng.standard_normal((1, 1, 512, 64)) * np.repeat(mags, 128)[None, None, :, None]
+    codes, scales = F8.quantize_blocks(x)
+    err_block = np.linalg.norm(F8.dequantize_blocks(codes, scales) - x) / np.linalg.norm(x)
+    c1, s1 = F8.quantize_blocks(x, block=512)  # one block = one scale for the tensor
+    small = x[..., :128, :]
+
+    def rel(deq):
+        return np.linalg.norm(deq[..., :128, :] - small) / np.linalg.norm(small)
+
+    # E4M3 rounding keeps every normal value within 2^-4 (RMS about 2^-3 / sqrt(12) = 0.036)
+    assert err_block < 0.036
+    assert rel(F8.dequantize_blocks(codes, scales)) < 0.036
+    assert rel(F8.dequantize_blocks(c1, s1, block=512)) > 5 * rel(F8.dequantize_blocks(codes, scales))
+
+
+def test_fp8_attention_is_attention_on_the_dequantised_inputs():
+    rng = np.random.default_rng(74)
+    # inputs that are E4M3 values with a block maximum of 448: scale 1, dequantisation exact
+    v = F8.e4m3_values()
+    q, k, vv = (rng.choice(np.concatenate([v, -v]), size=(1, 2, 130, 16)) for _ in range(3))
+    for t in (q, k, vv):
+        t[..., 0, 0] = 448.0
+        t[..., 128, 0] = 448.0
+    qc, qs = F8.quantize_blocks(q)
+    kc, ks = F8.quantize_blocks(k)
+    vc, vs = F8.quantize_blocks(vv)
+    assert np.all(qs == 1) and np.array_equal(qc, q)
+    o, lse = F8.attn_fwd64_fp8(qc, qs, kc, ks, vc, vs, 0.01, True)
+    o_ref, l_ref = oracle.attn_fwd64(q, k, vv, 0.01, True)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(lse, l_ref)
+
+
+def test_planted_truncating_e4m3_fails():
+    v = F8.e4m3_values()
+    mid = (v[:-1] + v[1:]) / 2
+
+    def truncating(x):  # slip: rounds toward zero instead of to nearest
+        a = np.abs(x)
+        _, fe = np.frexp(np.where(a > 0, a, 1.0))
+        ulp = 2.0 ** (np.maximum(fe - 1, -6) - 3)
+        return np.floor(a / ulp) * ulp
+
+    want = np.where(np.arange(len(mid)) % 2 == 0, v[:-1], v[1:])
+    assert not np.array_equal(truncating(mid), want)
