@@ -20,8 +20,8 @@ __all__ = [
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
-    "attention_forward", "attention_backward", "attention_decode", "EXPORTED_SYMBOLS",
-    "NOALLOC_SCRATCH_BYTES",
+    "fa_quantize_fp8", "fa_fwd_fp8", "attention_forward", "attention_backward", "attention_decode",
+    "attention_forward_fp8", "quantize_fp8", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +34,7 @@ EXPORTED_SYMBOLS = (
     "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
+    "fa_quantize_fp8", "fa_fwd_fp8",
 )
 
 _lib = None
@@ -76,6 +77,8 @@ def load_library():
         lib.fa_decode_workspace_size.argtypes = [i] * 7
         lib.fa_decode_workspace_size.restype = sz
         lib.fa_decode.argtypes = [vp] * 5 + [i] * 6 + [f, i, i, vp, sz, vp]
+        lib.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+        lib.fa_fwd_fp8.argtypes = [vp] * 8 + [i, i, i, i, f, i, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
         lib.fa_uses_tensor_cores.argtypes = [i, i, i]
@@ -83,7 +86,8 @@ def load_library():
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_error_message.argtypes = []
         lib.fa_last_error_message.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_bwd_noalloc", "fa_bwd_preprocess",
+        for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_quantize_fp8", "fa_fwd_fp8",
+                     "fa_bwd_noalloc", "fa_bwd_preprocess",
                      "fa_bwd_main", "fa_bwd_dq_convert",
                      "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
             getattr(lib, name).restype = ctypes.c_int
@@ -231,6 +235,36 @@ def fa_decode(Q, K, V, O, L, scale, splits=0, workspace=None, stream=None):
                                     _dt(Q), _p(workspace), nbytes, _stream(stream)))
 
 
+def fa_quantize_fp8(X, X8, scales, stream=None):
+    """Block quantisation of X [B, H, N, d] to E4M3 codes X8 (uint8, same shape) and
+    scales [B, H, ceil(N / 128)] fp32."""
+    B, H, N, d = _shape4(X)
+    if X8.dtype != torch.uint8 or tuple(X8.shape) != (B, H, N, d) or not X8.is_contiguous():
+        raise ValueError("X8 must be a contiguous uint8 tensor of X's shape")
+    nb = (N + 127) // 128
+    if scales.dtype != torch.float32 or scales.numel() != B * H * nb or not scales.is_contiguous():
+        raise ValueError(f"scales must be a contiguous fp32 tensor of B*H*ceil(N/128) = {B * H * nb} elements")
+    _check(load_library().fa_quantize_fp8(_p(X), _p(X8), _p(scales), B, H, N, d, _dt(X), _stream(stream)))
+
+
+def fa_fwd_fp8(Q8, K8, V8, q_scales, k_scales, v_scales, O, L, scale, causal, stream=None):
+    """Forward on E4M3 codes with block scales; O [B, H, N, d] bf16 or fp16, L [B, H, N] fp32."""
+    B, H, N, d = _shape4(Q8)
+    nb = (N + 127) // 128
+    for t in (Q8, K8, V8):
+        if t.dtype != torch.uint8 or tuple(t.shape) != (B, H, N, d) or not t.is_contiguous():
+            raise ValueError("Q8, K8, V8 must be contiguous uint8 tensors of one shape")
+    for t in (q_scales, k_scales, v_scales):
+        if t.dtype != torch.float32 or t.numel() != B * H * nb or not t.is_contiguous():
+            raise ValueError("block scales must be contiguous fp32 tensors of B*H*ceil(N/128) elements")
+    if tuple(O.shape) != (B, H, N, d) or not O.is_contiguous():
+        raise ValueError("O must be a contiguous [B, H, N, d] tensor")
+    if L.dtype != torch.float32 or L.numel() != B * H * N or not L.is_contiguous():
+        raise ValueError("L must be a contiguous fp32 tensor of B*H*N elements")
+    _check(load_library().fa_fwd_fp8(_p(Q8), _p(K8), _p(V8), _p(q_scales), _p(k_scales), _p(v_scales), _p(O), _p(L),
+                                     B, H, N, d, float(scale), int(bool(causal)), _dt(O), _stream(stream)))
+
+
 def fa_check_device_error(stream=None):
     _check(load_library().fa_check_device_error(_stream(stream)))
 
@@ -297,4 +331,24 @@ def attention_decode(q, k, v, scale=None, splits=0, stream=None):
     nbytes = fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d, splits)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
     fa_decode(q, k, v, o, lse, scale, splits, ws, stream)
+    return o, lse
+
+
+def quantize_fp8(x, stream=None):
+    """(codes, scales) = block quantisation of x [B, H, N, d] (one scale per 128 rows of a head)."""
+    B, H, N, d = _shape4(x)
+    x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+    sc = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=x.device)
+    fa_quantize_fp8(x, x8, sc, stream)
+    return x8, sc
+
+
+def attention_forward_fp8(q8, k8, v8, q_scales, k_scales, v_scales, scale=None, causal=False,
+                          out_dtype=torch.bfloat16, stream=None):
+    """O, L = fa_fwd_fp8(...) on E4M3 codes and their block scales."""
+    B, H, N, d = _shape4(q8)
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty((B, H, N, d), dtype=out_dtype, device=q8.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    fa_fwd_fp8(q8, k8, v8, q_scales, k_scales, v_scales, o, lse, scale, causal, stream)
     return o, lse

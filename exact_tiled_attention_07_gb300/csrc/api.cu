@@ -353,6 +353,52 @@ fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float*
   return launched(tc ? launch_decode_tc(a) : launch_decode(a), "fa_decode");
 }
 
+fa_status fa_quantize_fp8(const void* X, void* X8, float* scales, int B, int H, int N, int d, fa_dtype dtype,
+                          void* stream) {
+  bool empty;
+  fa_status st = check_common(B, H, N, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if (d != 64 && d != 128 && d != 256)
+    return fail(FA_ERR_UNSUPPORTED, "fa_quantize_fp8 supports d in {64, 128, 256}, got %d", d);
+  if ((st = check_ptrs({X, X8, scales}, "fa_quantize_fp8")) != FA_OK) return st;
+  QuantArgs a{X, X8, scales, B * H, N, d, (int)dtype, static_cast<cudaStream_t>(stream)};
+  return launched(launch_quantize_fp8(a), "fa_quantize_fp8");
+}
+
+fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, const float* q_scales, const float* k_scales,
+                     const float* v_scales, void* O, float* L, int B, int H, int N, int d, float scale, int causal,
+                     fa_dtype out_dtype, void* stream) {
+  if (out_dtype != FA_BF16 && out_dtype != FA_FP16)
+    return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8 writes O as bf16 or fp16, not dtype %d", (int)out_dtype);
+  bool empty;
+  fa_status st = check_common(B, H, N, d, out_dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if (!fwd_fp8_supported(d)) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8 supports d = 128, got %d", d);
+  if ((st = check_ptrs({Q8, K8, V8, q_scales, k_scales, v_scales, O, L}, "fa_fwd_fp8")) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  DeviceSyms syms;
+  if ((st = device_syms(&syms)) != FA_OK) return st;
+  Fp8FwdArgs a{};
+  a.q8 = Q8;
+  a.k8 = K8;
+  a.v8 = V8;
+  a.q_scales = q_scales;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
+  a.o = O;
+  a.lse = L;
+  a.bh = B * H;
+  a.n = N;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.out_dtype = (int)out_dtype;
+  a.err = syms.err;
+  a.counter = syms.counter;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launched(launch_fwd_fp8(a), "fa_fwd_fp8");
+}
+
 fa_status fa_check_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));

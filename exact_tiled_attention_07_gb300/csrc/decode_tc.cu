@@ -307,9 +307,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         for (int c = 0; c < COLS; ++c)
           if (c >= limit) s[c] = -INFINITY;
       }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < COLS; ++c) mx = fmaxf(mx, s[c]);
+      const float mx = row_max(s);
       const float m_blk = mx * scale_log2;
       float alpha = 1.f;
       bool rescale = false;
@@ -322,7 +320,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         rescale = true;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float sum = 0.f;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
       // this copy's P: 16-bit pairs, COLS / 2 TMEM columns from column col0 / 2 of the buffer
 #pragma unroll
       for (int h = 0; h < COLS / 32; ++h) {
@@ -331,11 +329,12 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2(fmaf(s[h * 32 + 2 * i], scale_log2, neg_m));
           const float p1 = ex2(fmaf(s[h * 32 + 2 * i + 1], scale_log2, neg_m));
-          sum += p0 + p1;
+          part[i & 3] += p0 + p1;
           pk[i] = pack2<BF16>(p0, p1);
         }
         tmem_st16(tmem_addr(tbase, lane_base, s_col + col0 / 2 + h * 16), pk);
       }
+      const float sum = (part[0] + part[1]) + (part[2] + part[3]);
       if constexpr (R > 1) {
         // the other copies' key columns contribute nothing to this copy's rows
         const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};

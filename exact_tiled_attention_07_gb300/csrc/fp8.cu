@@ -1,0 +1,516 @@
+// FP8 (E4M3) path: block quantisation, and the tensor-core forward on quantised Q, K, V.
+//
+// "Lecture 8 · GPU Performance & FlashAttention" §8.1 and "FlashAttention and GPU memory" §11:
+// the third generation runs attention in 8-bit floating point with block quantisation, one
+// scale per block of each tensor.  Here a block is 128 rows x d of one head (the tile the
+// kernel streams), its scale is amax / 448 (E4M3's largest finite value) and its codes are
+// E4M3(x / scale), rounded to nearest even; the scale and the quotient are fp32 divisions.
+//
+// fwd_fp8_kernel is the 16-bit forward's pipeline (two query tiles ping-ponging, TMA ring,
+// softmax in the exp2 domain with lazy rescaling) with 8-bit operands: S = Q8 K8^T and
+// O += P8 V8 are kind::f8f6f4 MMAs (K = 32 per instruction).  The block scales enter as
+//   S_ij = tau * sq(i) * sk(j) * (Q8 K8^T)_ij        (one factor per pair of tiles),
+//   O_i  = sum_j P_ij sv(j) V8_j / l_i,
+// with sv(j) folded into P before it is rounded to E4M3: P8 = E4M3(P * sv(j) / sv_max), where
+// sv_max is the head's largest V scale, so P8 <= 2^8 (the lazy-rescale bound) stays inside
+// E4M3's range, and the epilogue multiplies O by sv_max / l.  l sums the unrounded P.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace fa {
+namespace {
+
+constexpr float kE4m3Max = 448.0f;
+
+// ------------------------------------------------------------------------------ quantisation
+
+__device__ __forceinline__ void load8f(const float* p, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8f(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void load8f(const __half* p, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+// One CTA per 128-row block of one head: amax over the block, then the codes.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
+                                                           float* __restrict__ scales, int n, int nb) {
+  constexpr int G = 128 * D / 8 / 256;  // 8-element groups per thread in a full block
+  __shared__ float red[8];
+  const int blk = blockIdx.x % nb;
+  const int64_t head = blockIdx.x / nb;
+  const int r0 = blk * 128;
+  const int groups = min(128, n - r0) * D / 8;
+  const T* src = x + (head * n + r0) * D;
+  uint8_t* dst = x8 + (head * n + r0) * D;
+  float v[G][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int gi = threadIdx.x + g * 256;
+    if (gi < groups) {
+      load8f(src + (int64_t)gi * 8, v[g]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[g][i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[g][i]));
+  }
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+  const float s = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
+  if (threadIdx.x == 0) scales[head * nb + blk] = s;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int gi = threadIdx.x + g * 256;
+    if (gi < groups) {
+      float q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(v[g][i], s);
+      *reinterpret_cast<uint2*>(dst + (int64_t)gi * 8) =
+          make_uint2(pack4_e4m3(q[0], q[1], q[2], q[3]), pack4_e4m3(q[4], q[5], q[6], q[7]));
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_quantize_t(const QuantArgs& a) {
+  const int nb = (a.n + 127) / 128;
+  const unsigned grid = (unsigned)((int64_t)a.bh * nb);
+  switch (a.d) {
+    case 64:
+      quantize_fp8_kernel<T, 64><<<grid, 256, 0, a.stream>>>((const T*)a.x, (uint8_t*)a.x8, a.scales, a.n, nb);
+      break;
+    case 128:
+      quantize_fp8_kernel<T, 128><<<grid, 256, 0, a.stream>>>((const T*)a.x, (uint8_t*)a.x8, a.scales, a.n, nb);
+      break;
+    case 256:
+      quantize_fp8_kernel<T, 256><<<grid, 256, 0, a.stream>>>((const T*)a.x, (uint8_t*)a.x8, a.scales, a.n, nb);
+      break;
+    default:
+      return cudaErrorNotSupported;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------ forward
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per tile
+constexpr float kRescaleThreshold = 8.0f;
+
+// d = 128: one 128-byte row per tile row, so every tile is a single TMA box
+struct Fp8Cfg {
+  static constexpr int D = 128;
+  static constexpr int NQ = 2;
+  static constexpr int TILE_BYTES = 128 * D;  // 16 KB (Q, K or V tile)
+  static constexpr int STAGES = 12;
+  static constexpr int PRODUCER_WARP = 8;
+  static constexpr int MMA_WARP = 9;
+  static constexpr int THREADS = 320;
+  static constexpr int S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 384;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = NQ * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + STAGES * TILE_BYTES;
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 1;
+  static constexpr int OFF_RED = OFF_BAR + NBAR * 8 + 16;  // 8 floats: per-warp partial maxima
+  static constexpr int SMEM = OFF_RED + 8 * 4;
+};
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
+    fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ q_scales,
+                   const float* __restrict__ k_scales, const float* __restrict__ v_scales, void* __restrict__ out,
+                   float* __restrict__ lse, int n, int bh_count, int tiles_per_head, float scale_log2, int causal,
+                   int group, unsigned long long* err, unsigned long long* counter) {
+  using C = Fp8Cfg;
+  constexpr int D = C::D;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = bars + 1 + C::STAGES;
+  uint64_t* s_full = bars + 1 + 2 * C::STAGES;  // [2]
+  uint64_t* p_full = s_full + 2;                // [2]
+  uint64_t* o_full = p_full + 2;                // [2]
+  uint64_t* drain = o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  const ErrCtx ctx{err, abort_flag};
+
+  int head, tile;
+  if (causal) {
+    int rank;
+    grouped_work_item(blockIdx.x, bh_count, tiles_per_head, &head, &rank);
+    tile = tiles_per_head - 1 - rank;
+  } else {
+    head = blockIdx.x / tiles_per_head;
+    tile = blockIdx.x - head * tiles_per_head;
+  }
+  const int kvhead = head / group;
+  const int nblk = (n + BN - 1) / BN;  // 128-row blocks per head: key tiles and scale entries
+  const int qrow0 = tile * (C::NQ * BM);
+  int nq[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int first = qrow0 + q * BM;
+    if (first >= n) {
+      nq[q] = 0;
+    } else if (causal) {
+      nq[q] = min(nblk, (min(first + BM, n) - 1) / BN + 1);
+    } else {
+      nq[q] = nblk;
+    }
+  }
+  const int nmax = max(nq[0], nq[1]);
+
+  if (threadIdx.x == 0) {
+    if ((smem_u32(smem) & 1023u) != 0) report_error(err, DERR_BAD_SMEM_ALIGN, 0);
+    *abort_flag = (smem_u32(smem) & 1023u) != 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(s_full + q, 1);
+      mbar_init(p_full + q, 128);
+      mbar_init(o_full + q, 1);
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const bool start_ok = (*abort_flag == 0);
+
+  if (warp == C::PRODUCER_WARP) {
+    // ------------------------------------------------------------------ TMA producer
+    if (start_ok && lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(q_full, C::NQ * C::TILE_BYTES);
+      for (int q = 0; q < C::NQ; ++q)
+        tma_load_3d(smem + C::OFF_Q + q * C::TILE_BYTES, &tm_q, q_full, 0, qrow0 + q * BM, head);
+      int issued = 0;
+      for (int idx = 0; idx < 2 * nmax; ++idx) {
+        const int slot = idx % C::STAGES, use = idx / C::STAGES;
+        if (use > 0 && !mbar_wait(kv_empty + slot, (use - 1) & 1, ctx, 210)) break;
+        mbar_arrive_expect_tx(kv_full + slot, C::TILE_BYTES);
+        tma_load_3d(smem + C::OFF_RING + slot * C::TILE_BYTES, (idx & 1) ? &tm_v : &tm_k, kv_full + slot, 0,
+                    (idx >> 1) * BN, kvhead);
+        issued = idx + 1;
+      }
+      ErrCtx nctx = ctx;
+      int no_abort = 0;
+      nctx.abort = &no_abort;
+      mbar_wait(q_full, 0, nctx, 211);
+      for (int idx = issued - 1; idx >= 0 && idx >= issued - C::STAGES; --idx)
+        mbar_wait(kv_full + idx % C::STAGES, (idx / C::STAGES) & 1, nctx, 212);
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (start_ok) {
+      const bool leader = elect_one_sync();
+      // E4M3 is format code 0 in the A/B fields: the f16 descriptor layout with the f16 codes
+      const uint32_t idesc_qk = make_idesc_f16(BM, BN, false, false, false);
+      const uint32_t idesc_pv = make_idesc_f16(BM, D, false, false, true);
+      const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+      const uint32_t ring = smem_u32(smem + C::OFF_RING);
+      auto slot_of = [&](int idx) { return idx % C::STAGES; };
+      auto wait = [&](uint64_t* b, uint32_t parity, uint32_t site) {
+        return __all_sync(0xffffffffu, mbar_wait(b, parity, ctx, site));
+      };
+      auto wait_full = [&](int idx) { return wait(kv_full + slot_of(idx), (idx / C::STAGES) & 1, 220); };
+      auto commit = [&](uint64_t* b) {
+        if (leader) umma_commit(b);
+        __syncwarp();
+      };
+      // S = Q8_q K8^T: 32 bytes (32 elements) of the 128-byte rows per instruction
+      auto issue_qk = [&](int q, int kidx, uint32_t s_col) {
+        const uint32_t kt = ring + slot_of(kidx) * C::TILE_BYTES;
+        const uint32_t qt = q_base + q * C::TILE_BYTES;
+        uint64_t ad[D / 32], bd[D / 32];
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+          ad[kk] = make_sdesc_sw128(qt + kk * 32, 16, 1024);
+          bd[kk] = make_sdesc_sw128(kt + kk * 32, 16, 1024);
+        }
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) umma_ss_f8(tbase + s_col, ad[kk], bd[kk], idesc_qk, kk > 0);
+        }
+        __syncwarp();
+      };
+      // O += P8 V8: P8 (4 keys per TMEM column) in [p_col, p_col + 32); V8 MN-major, 32 keys
+      // (4 swizzle atoms of 8 rows) per instruction
+      auto issue_pv = [&](uint32_t o_col, uint32_t p_col, int vidx, bool acc) {
+        const uint32_t vt = ring + slot_of(vidx) * C::TILE_BYTES;
+        uint64_t bd[BN / 32];
+#pragma unroll
+        for (int kk = 0; kk < BN / 32; ++kk) bd[kk] = make_sdesc_sw128(vt + kk * 4096, BN * 128, 1024);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 32; ++kk)
+            umma_ts_f8(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+      };
+      bool ok = wait(q_full, 0, 221);
+      if (ok) tc_fence_after();
+      if (ok && nmax > 0) {
+        ok = wait_full(0);
+        if (ok) {
+          tc_fence_after();
+          if (nq[0] > 0) { issue_qk(0, 0, C::S_COL0); commit(s_full + 0); }
+          if (nq[1] > 0) { issue_qk(1, 0, C::S_COL1); commit(s_full + 1); }
+          commit(kv_empty + slot_of(0));
+        }
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+        if (!(ok = wait_full(vidx))) break;
+        if (j < nq[0]) {
+          if (!(ok = wait(p_full + 0, j & 1, 222))) break;
+          tc_fence_after();
+          issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
+        }
+        if (j + 1 < nmax) {
+          if (!(ok = wait_full(kidx))) break;
+          tc_fence_after();
+        }
+        if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); commit(s_full + 0); }
+        if (j < nq[1]) {
+          if (!(ok = wait(p_full + 1, j & 1, 223))) break;
+          tc_fence_after();
+          issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
+        }
+        commit(kv_empty + slot_of(vidx));
+        if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); commit(s_full + 1); }
+        if (j + 1 < nmax) commit(kv_empty + slot_of(kidx));
+        if (j == nq[0] - 1) commit(o_full + 0);
+        if (j == nq[1] - 1) commit(o_full + 1);
+      }
+      ErrCtx nctx = ctx;
+      int no_abort = 0;
+      nctx.abort = &no_abort;
+      commit(drain);
+      mbar_wait(drain, 0, nctx, 225);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int q = warp >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_base = quarter * 32;
+    const int rit = quarter * 32 + lane;
+    const int row = qrow0 + q * BM + rit;
+    const int nb = nq[q];
+    const uint32_t s_col = q ? C::S_COL1 : C::S_COL0;
+    const uint32_t o_col = q ? C::O_COL1 : C::O_COL0;
+    const float* ks = k_scales + (int64_t)kvhead * nblk;
+    const float* vs = v_scales + (int64_t)kvhead * nblk;
+    // the head's largest V scale (both warpgroups, one named barrier)
+    float svmax = 0.f;
+    for (int i = threadIdx.x; i < nblk; i += 256) svmax = fmaxf(svmax, vs[i]);
+    for (int o = 16; o > 0; o >>= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, o));
+    if (lane == 0) red[warp] = svmax;
+    named_bar_sync(1, 256);
+    svmax = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) svmax = fmaxf(svmax, red[w]);
+    const float inv_svmax = 1.f / svmax;
+    const int qblk = min((qrow0 + q * BM) / BM, nblk - 1);
+    const float sq_log2 = scale_log2 * q_scales[(int64_t)head * nblk + qblk];
+    float m = -INFINITY;
+    float l = 0.f;
+    bool ok = start_ok;
+    float sk_next = nb > 0 ? ks[0] : 0.f, sv_next = nb > 0 ? vs[0] : 0.f;
+    for (int j = 0; ok && j < nb; ++j) {
+      const float st = sq_log2 * sk_next;      // tau log2(e) sq sk: S units -> log2 units
+      const float pv = sv_next * inv_svmax;   // sv / sv_max, folded into P
+      if (j + 1 < nb) {
+        sk_next = ks[j + 1];
+        sv_next = vs[j + 1];
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full + q, j & 1, ctx, 230 + q));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[BN / 32][32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, s_col + c * 32), sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+      int limit = n - j * BN;
+      if (causal) limit = min(limit, row - j * BN + 1);
+      if (limit < BN) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c >= limit) s[c] = -INFINITY;
+      }
+      const float mx = row_max(s);
+      const float m_blk = mx * st;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m == -INFINITY) {
+        m = m_blk;
+        alpha = 0.f;
+      } else if (m_blk > m + kRescaleThreshold) {
+        alpha = ex2(m - m_blk);
+        m = m_blk;
+        rescale = true;
+      }
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = ex2(fmaf(s[4 * i], st, neg_m));
+        const float p1 = ex2(fmaf(s[4 * i + 1], st, neg_m));
+        const float p2 = ex2(fmaf(s[4 * i + 2], st, neg_m));
+        const float p3 = ex2(fmaf(s[4 * i + 3], st, neg_m));
+        part[i & 3] += (p0 + p1) + (p2 + p3);
+        pk[i] = pack4_e4m3(p0 * pv, p1 * pv, p2 * pv, p3 * pv);
+      }
+      const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+      tmem_st32(tmem_addr(tbase, lane_base, s_col), pk);
+      l = l * alpha + sum;
+      if (__any_sync(0xffffffffu, rescale)) {
+        const float a = rescale ? alpha : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          const uint32_t ta = tmem_addr(tbase, lane_base, o_col + c * 32);
+          tmem_ld32(ta, r);
+          tmem_wait_ld();
+          reg_fence(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+          tmem_st32(ta, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + q);
+    }
+    if (ok && nb > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(o_full + q, 0, ctx, 240 + q));
+      if (ok) {
+        tc_fence_after();
+        const float inv = l > 0.f ? svmax / l : 0.f;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem_addr(tbase, lane_base, o_col + c * 32), r);
+          tmem_wait_ld();
+          reg_fence(r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<OUT_BF16>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+          if (row < n) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (row < n) lse[(int64_t)head * n + row] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        if (counter && rit == 0) atomicAdd(counter, (unsigned long long)nb);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <bool OUT_BF16>
+cudaError_t launch_fwd_fp8_t(const Fp8FwdArgs& a) {
+  using C = Fp8Cfg;
+  CUtensorMap tq, tk, tv;
+  const int bh_kv = a.bh / a.group;
+  if (!make_tmap_8bit_3d(&tq, a.q8, C::D, a.n, a.bh, BM) || !make_tmap_8bit_3d(&tk, a.k8, C::D, a.n, bh_kv, BN) ||
+      !make_tmap_8bit_3d(&tv, a.v8, C::D, a.n, bh_kv, BN))
+    return cudaErrorInvalidValue;
+  auto kern = fwd_fp8_kernel<OUT_BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
+  kern<<<(unsigned)(a.bh * tiles), C::THREADS, C::SMEM, a.stream>>>(
+      tq, tk, tv, a.q_scales, a.k_scales, a.v_scales, a.o, a.lse, a.n, a.bh, tiles,
+      a.scale * 1.4426950408889634f, a.causal, a.group, a.err, a.counter);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_fp8(const QuantArgs& a) {
+  switch (a.dtype) {
+    case DT_BF16: return launch_quantize_t<__nv_bfloat16>(a);
+    case DT_FP16: return launch_quantize_t<__half>(a);
+    default: return launch_quantize_t<float>(a);
+  }
+}
+
+bool fwd_fp8_supported(int d) { return d == 128; }
+
+cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a) {
+  if (a.d != 128) return cudaErrorNotSupported;
+  return a.out_dtype == DT_BF16 ? launch_fwd_fp8_t<true>(a) : launch_fwd_fp8_t<false>(a);
+}
+
+}  // namespace fa

@@ -360,9 +360,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= limit) s[c] = -INFINITY;
       }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      const float mx = row_max(s);
       const float m_blk = mx * scale_log2;
       float alpha = 1.f;
       bool rescale = false;
@@ -375,7 +373,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         rescale = true;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float sum = 0.f;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
 #pragma unroll
       for (int h = 0; h < BN / 64; ++h) {
         uint32_t pk[32];
@@ -383,11 +381,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int i = 0; i < 32; ++i) {
           const float p0 = ex2(fmaf(s[h * 64 + 2 * i], scale_log2, neg_m));
           const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], scale_log2, neg_m));
-          sum += p0 + p1;
+          part[i & 3] += p0 + p1;
           pk[i] = pack2<BF16>(p0, p1);
         }
         tmem_st32(tmem_addr(tbase, lane_base, s_col + h * 32), pk);
       }
+      const float sum = (part[0] + part[1]) + (part[2] + part[3]);
       l = l * alpha + sum;
       if (__any_sync(0xffffffffu, rescale)) {
         // O row *= alpha; O is stable: the PV of block j-1 completed before S_j

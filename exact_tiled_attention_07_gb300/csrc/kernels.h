@@ -83,6 +83,40 @@ cudaError_t launch_decode(const DecodeArgs& a);     // CUDA cores, any dtype
 cudaError_t launch_decode_tc(const DecodeArgs& a);  // tensor cores, bf16/fp16
 cudaError_t launch_decode_merge(const DecodeArgs& a);
 
+// FP8 (E4M3) block quantisation: X [bh][n][d] (dtype) -> codes X8 [bh][n][d] (bytes) and one
+// fp32 scale per 128-row block, scales [bh][ceil(n / 128)].
+struct QuantArgs {
+  const void* x;
+  void* x8;
+  float* scales;
+  int bh, n, d, dtype;
+  cudaStream_t stream;
+};
+cudaError_t launch_quantize_fp8(const QuantArgs& a);
+
+// FP8 forward: Q8, K8, V8 [bh][n][d] E4M3 codes with block scales; O [bh][n][d] in out_dtype
+// (bf16 or fp16), L [bh][n] fp32.
+struct Fp8FwdArgs {
+  const void* q8;
+  const void* k8;
+  const void* v8;
+  const float* q_scales;
+  const float* k_scales;
+  const float* v_scales;
+  void* o;
+  float* lse;
+  int bh, n, d;
+  float scale;
+  int causal;
+  int out_dtype;
+  unsigned long long* err;
+  unsigned long long* counter;
+  cudaStream_t stream;
+  int group = 1;
+};
+bool fwd_fp8_supported(int d);
+cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a);
+
 // Records the calling thread's last error message (read by fa_last_error_message) and
 // returns `status`.
 int set_last_error(int status, const char* fmt, ...);

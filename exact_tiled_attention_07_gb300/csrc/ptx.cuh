@@ -219,6 +219,27 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// The same two products with 8-bit floating-point operands (kind::f8f6f4; E4M3 is format 0 in
+// the A/B format fields of the instruction descriptor, K = 32 per instruction).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async operation issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -300,6 +321,21 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint
   return base + (lane << 16) + col;
 }
 
+// Largest of N values (N a multiple of 4): four independent chains, then a tree, so the
+// reduction is not one long chain of dependent max instructions.
+template <int N>
+__device__ __forceinline__ float row_max(const float (&s)[N]) {
+  static_assert(N % 4 == 0, "row_max takes a multiple of 4 values");
+  float m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = s[i];
+#pragma unroll
+  for (int c = 4; c < N; c += 4)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], s[c + i]);
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
 // 2^x on the SFU (PTX ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -316,6 +352,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
   }
+}
+
+// Four fp32 values as E4M3 bytes (round to nearest even, saturating at +-448), v0 in the lowest
+// byte.  cvt...e4m3x2 puts its first source in the upper byte of the pair.
+__device__ __forceinline__ uint32_t pack4_e4m3(float v0, float v1, float v2, float v3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v1), "f"(v0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v3), "f"(v2));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
 template <bool BF16>

@@ -172,13 +172,47 @@ FA_API fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, con
  *   splits   number of cache pieces; <= 0 chooses automatically; capped at Nk
  *   workspace  fa_decode_workspace_size(...) bytes for the same arguments (0 when there is a
  *            single piece: then workspace may be NULL)
- * Launches one kernel, plus one merge kernel when there is more than one piece. Runs on CUDA
- * cores: the kernel reads each cached key and value once and is bound by HBM bandwidth.
+ * Launches one kernel, plus one merge kernel when there is more than one piece. bf16/fp16 run
+ * on the tensor cores (the rows sharing a key/value head form one 128-row tile), fp32 on CUDA
+ * cores; either way each cached key and value is read once and the call is bound by HBM
+ * bandwidth. The size fa_decode_workspace_size returns covers every dtype.
  */
 FA_API size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, int splits);
 FA_API fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv,
                            int Nq, int Nk, int d, float scale, int splits, fa_dtype dtype, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/*
+ * FP8 (E4M3) block quantisation ("Lecture 8" §8.1, "FlashAttention and GPU memory" §11: the
+ * third generation runs attention in 8-bit floating point with one scale per block).
+ *   X        in:  [B][H][N][d] dtype (bf16, fp16 or fp32)
+ *   X8       out: [B][H][N][d] bytes, E4M3 codes (1 sign, 4 exponent bits with bias 7,
+ *                 3 mantissa bits; largest finite value 448)
+ *   scales   out: [B][H][ceil(N / 128)] fp32; block b of a head is rows [128 b, 128 b + 128)
+ *   d        64, 128 or 256
+ * For each block, scale = amax / 448 (1 when the block is all zero) and
+ * code = E4M3(x / scale), rounded to nearest even and saturated at +-448; both divisions are
+ * fp32 divisions rounded to nearest. One kernel, one thread block per 128-row block.
+ */
+FA_API fa_status fa_quantize_fp8(const void* X, void* X8, float* scales, int B, int H, int N, int d, fa_dtype dtype,
+                                 void* stream);
+
+/*
+ * Forward attention on FP8 inputs with block scales (tensor cores, kind::f8f6f4).
+ *   Q8, K8, V8           in:  [B][H][N][d] E4M3 codes, as written by fa_quantize_fp8
+ *   q/k/v_scales         in:  [B][H][ceil(N / 128)] fp32 block scales
+ *   O                    out: [B][H][N][d] out_dtype (FA_BF16 or FA_FP16)
+ *   L                    out: [B][H][N] fp32, natural-log log-sum-exp of the scaled scores
+ *   d                    128
+ * Computes attention of the dequantised tensors (code x block scale): S = scale Q K^T (causal
+ * mask when causal != 0), O = softmax(S) V, L = m + ln l. The probabilities are rounded to
+ * E4M3 before the P V product (after multiplying by the key block's V scale over the head's
+ * largest V scale), so O carries E4M3's relative rounding of P (at most 2^-4 per element);
+ * L does not. Pointers 16-byte aligned; the same errors as fa_fwd.
+ */
+FA_API fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, const float* q_scales,
+                            const float* k_scales, const float* v_scales, void* O, float* L, int B, int H, int N,
+                            int d, float scale, int causal, fa_dtype out_dtype, void* stream);
 
 /*
  * Synchronises `stream` and reports device-side failures/*

@@ -48,3 +48,18 @@ TOL_O_RELRMS = 5e-3
 TOL_GRAD_RELRMS = 1e-2
 TOL_L_MAXABS = 1e-3
 TOL_FP32 = 1e-5
+
+# FP8 forward against attention on the dequantised inputs.  The kernel rounds P (scaled into
+# (0, 2^8]) to E4M3 before the P V product: each probability carries a relative error of at
+# most 2^-4 (3 mantissa bits, round to nearest), RMS 2^-3 / sqrt(12) ~ 0.036 for a uniformly
+# spread rounding error, so O's relative RMS error is about 0.036 and |error| of an element
+# is at most 2^-4 max|V| (the weights sum to one).  L does not involve the rounded P.
+TOL_FP8_O_RELRMS = 0.05
+TOL_FP8_O_MAXABS_OF_VMAX = 2.0 ** -4
+# L: S = Q8 K8^T is accumulated by the tensor core, whose sum of 8-bit products is not an
+# IEEE fp32 sum; the dot-product error bound |dS| <= k u sum|q_k k_k| with the unit roundoff u
+# of that accumulation gives an L error proportional to the row's largest |S|.  Read here as
+# |dL| <= 1e-3 + 2^-11 max_j |S_ij| (u about 2^-14, the measured relative error of L at large
+# scores being about 2^-13).
+TOL_FP8_L_OF_SMAX = 2.0 ** -11
+

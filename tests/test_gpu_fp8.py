@@ -1,0 +1,151 @@
+"""FP8 (E4M3) block quantisation and the FP8 forward through the C ABI, against the oracle."""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import fp8 as F8
+from helpers import (TOL_FP8_L_OF_SMAX, TOL_FP8_O_MAXABS_OF_VMAX, TOL_FP8_O_RELRMS, TOL_L_MAXABS, max_abs,
+                     rel_rms, to_device, to_f64)
+from exact_tiled_attention_07_gb300.inputs import round_to_dtype, to_float64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_tiled_attention_07_gb300 import binding, build
+
+    build.build()
+    return binding
+
+
+def _draw(shape, seed, spread=True):
+    """N(0,1) values, each 128-row block of a head scaled by its own factor in [1e-3, 1e2]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.standard_normal(shape, dtype=np.float32)
+    if spread:
+        nb = (shape[-2] + 127) // 128
+        f = np.exp(rng.uniform(np.log(1e-3), np.log(1e2), size=shape[:-2] + (nb,))).astype(np.float32)
+        x *= np.repeat(f, 128, axis=-1)[..., : shape[-2], None]
+    return x
+
+
+def _codes_to_bytes(codes):
+    """Oracle code values (exact E4M3 values) -> their bytes, by torch's float8 conversion."""
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("n", [1, 127, 128, 300])
+def test_quantize_codes_and_scales_are_bit_exact(fa, dtype, d, n):
+    x = round_to_dtype(_draw((2, 3, n, d), 10 + d + n), dtype)
+    x64 = to_float64(x, dtype)
+    codes, scales = F8.quantize_blocks(x64)
+    x8, sc = fa.quantize_fp8(to_device(x, dtype))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(sc.cpu().numpy(), scales)
+    np.testing.assert_array_equal(x8.cpu().numpy(), _codes_to_bytes(codes).numpy())
+
+
+def test_quantize_all_zero_block_and_saturation(fa):
+    x = np.zeros((1, 1, 256, 128), dtype=np.float32)
+    x[0, 0, 128:, :] = np.linspace(-3.0, 5.0, 128 * 128, dtype=np.float32).reshape(128, 128)
+    x8, sc = fa.quantize_fp8(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert sc[0, 0, 0].item() == 1.0 and not x8[0, 0, :128].any()
+    codes, scales = F8.quantize_blocks(x)
+    assert sc[0, 0, 1].item() == scales[0, 0, 1]
+    np.testing.assert_array_equal(x8.cpu().numpy(), _codes_to_bytes(codes).numpy())
+    # the block maximum maps to 448 = byte 0x7E
+    assert int(x8[0, 0, 255, 127].item()) == 0x7E
+
+
+def _fp8_case(b, h, n, seed, spread=True):
+    q, k, v = (_draw((b, h, n, 128), seed + i, spread) for i in range(3))
+    qc, qs = F8.quantize_blocks(q)
+    kc, ks = F8.quantize_blocks(k)
+    vc, vs = F8.quantize_blocks(v)
+    dev = [_codes_to_bytes(c).cuda() for c in (qc, kc, vc)] + [torch.from_numpy(s).cuda() for s in (qs, ks, vs)]
+    return (qc, qs, kc, ks, vc, vs), dev
+
+
+def _smax_rows(q, k, scale, causal, rows):
+    """max_j |S_ij| for the rows (b, h, i), S = scale q_i . k_j over the visible keys."""
+    out = []
+    for b, h, i in rows:
+        s_ = scale * (k[b, h] @ q[b, h, i])
+        out.append(np.abs(s_[: i + 1] if causal else s_).max())
+    return np.array(out)
+
+
+def _check_l(gl, l_ref, smax):
+    err = np.abs(np.asarray(gl, np.float64) - l_ref)
+    bound = TOL_L_MAXABS + TOL_FP8_L_OF_SMAX * smax
+    assert np.all(err <= bound), (err.max(), float(((err - TOL_L_MAXABS) / smax).max()))
+
+
+def _check_o(go, o_ref, vmax):
+    assert rel_rms(go, o_ref) <= TOL_FP8_O_RELRMS, rel_rms(go, o_ref)
+    assert max_abs(go, o_ref) <= TOL_FP8_O_MAXABS_OF_VMAX * vmax + 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [128, 129, 300, 1000])
+@pytest.mark.parametrize("out", ["bf16", "fp16"])
+def test_fp8_forward_matches_attention_on_dequantised_inputs(fa, causal, n, out):
+    host, dev = _fp8_case(2, 2, n, 50 + n + causal)
+    scale = 128 ** -0.5
+    odt = torch.bfloat16 if out == "bf16" else torch.float16
+    o, lse = fa.attention_forward_fp8(*dev[:3], *dev[3:], scale=scale, causal=causal, out_dtype=odt)
+    fa.fa_check_device_error()
+    o_ref, l_ref = F8.attn_fwd64_fp8(*host, scale, causal)
+    vmax = np.abs(F8.dequantize_blocks(host[4], host[5])).max()
+    _check_o(to_f64(o), o_ref, vmax)
+    rows = list(np.ndindex(2, 2, n))
+    deq = [F8.dequantize_blocks(host[2 * i], host[2 * i + 1]) for i in range(2)]
+    _check_l(to_f64(lse).reshape(-1), l_ref.reshape(-1), _smax_rows(deq[0], deq[1], scale, causal, rows))
+
+
+def test_fp8_forward_unit_scales_and_causal_tiles(fa):
+    # uniform magnitudes: every block scale close to the others; causal tile count T (T + 1) / 2
+    host, dev = _fp8_case(1, 3, 1000, 90, spread=False)
+    fa.fa_tile_counter(reset=True)
+    o, lse = fa.attention_forward_fp8(*dev[:3], *dev[3:], causal=True)
+    torch.cuda.synchronize()
+    t = (1000 + 127) // 128
+    assert fa.fa_tile_counter() == 3 * t * (t + 1) // 2
+    o_ref, l_ref = F8.attn_fwd64_fp8(*host, 128 ** -0.5, True)
+    _check_o(to_f64(o), o_ref, np.abs(F8.dequantize_blocks(host[4], host[5])).max())
+    assert max_abs(to_f64(lse), l_ref) <= TOL_L_MAXABS
+
+
+def test_fp8_forward_full_size_sampled_rows(fa):
+    # the causal LM shape (B 8, H 16, N 4096, d 128), sampled rows against the oracle
+    b, h, n = 8, 16, 4096
+    host, dev = _fp8_case(b, h, n, 123, spread=False)
+    o, lse = fa.attention_forward_fp8(*dev[:3], *dev[3:], causal=True)
+    fa.fa_check_device_error()
+    rng = np.random.default_rng(5)
+    samples = np.stack([rng.integers(0, b, 48), rng.integers(0, h, 48), rng.integers(0, n, 48)], axis=1)
+    samples = np.concatenate([samples, [[0, 0, 0], [7, 15, n - 1], [3, 4, 128], [5, 9, 127]]])
+    deq = [F8.dequantize_blocks(host[2 * i], host[2 * i + 1]) for i in range(3)]
+    o_ref, l_ref = oracle.attn_fwd64_rows(*deq, 128 ** -0.5, True, samples)
+    go, gl = to_f64(o), to_f64(lse)
+    got_o = np.stack([go[bb, hh, ii] for bb, hh, ii in samples])
+    got_l = np.array([gl[bb, hh, ii] for bb, hh, ii in samples])
+    _check_o(got_o, o_ref, np.abs(deq[2]).max())
+    _check_l(got_l, l_ref, _smax_rows(deq[0], deq[1], 128 ** -0.5, True, samples))
+
+
+def test_fp8_argument_checks(fa):
+    z = torch.zeros((1, 1, 128, 64), dtype=torch.uint8, device="cuda")
+    s = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(fa.FAError, match="d = 128"):
+        fa.attention_forward_fp8(z, z, z, s, s, s)
