@@ -446,6 +446,43 @@ def run_gpu(args, w: Workload):
                 tf = fl / (ms * 1e-3) / 1e12
                 targets[f"{tag}_{pname}"] = {"ms": ms, "tflops": tf, "pct_of_burst_peak": 100 * tf / peak_burst,
                                              "pct_of_sustained_peak": 100 * tf / peak_sus}
+        if w.d == 128 and w.dtype != "fp32":
+            # FP8 forward on block-quantised copies of the same inputs (quantised once, untimed);
+            # its peak is the bf16 peak x 2 (the nominal dense fp8 / bf16 ratio)
+            q8, qs = binding.quantize_fp8(q)
+            k8, ks = binding.quantize_fp8(k)
+            v8, vs = binding.quantize_fp8(v)
+            o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=device)
+            for cz, tag in variants:
+                reps = max(3, min(args.steps, 10))
+
+                def fp8_call():
+                    binding.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o8, lse, scale, cz)
+
+                for _ in range(2):
+                    fp8_call()
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                for _ in range(reps):
+                    fp8_call()
+                b_.record(stream)
+                torch.cuda.synchronize()
+                ms = a_.elapsed_time(b_) / reps
+                tf = attention_flops(w.B, w.H, w.N, w.d, cz, "fwd") / (ms * 1e-3) / 1e12
+                targets[f"{tag}_fwd_fp8"] = {"ms": ms, "tflops": tf, "pct_of_fp8_burst_peak": 100 * tf / (2 * peak_burst),
+                                             "pct_of_fp8_sustained_peak": 100 * tf / (2 * peak_sus)}
+            reps = max(3, min(args.steps, 10))
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            for _ in range(reps):
+                binding.fa_quantize_fp8(q, q8, qs)
+            b_.record(stream)
+            torch.cuda.synchronize()
+            ms = a_.elapsed_time(b_) / reps
+            qbytes = q.numel() * (q.element_size() + 1) + qs.numel() * 4
+            targets["quantize_fp8"] = {"ms": ms, "gbs": qbytes / (ms * 1e-3) / 1e9,
+                                       "frac_of_hbm": qbytes / (ms * 1e-3) / 1e9 / float(peaks.get("hbm_gbs", 6800.0))}
+            del q8, k8, v8, o8
         binding.fa_check_device_error()
 
     decode = None

@@ -12,7 +12,8 @@ Sources it restates (cited by page title and section):
   backward and the D identity, §5.7 causal block skipping, §8.1 FA2's deferred
   normalisation, §8.2 multi-query / grouped-query attention (``oracle/gqa.py``) and
   split-KV decoding with the state merge (``oracle/decode.py``), the FP8 forward with block
-  quantisation (``oracle/fp8.py``), Exercises 1 and 3.
+  quantisation (``oracle/fp8.py``), §5.7 block-sparse and sliding-window masks
+  (``oracle/masks.py``), Exercises 1 and 3.
 * "Stanford CS336 Lecture 5 close reading: GPUs ... Flash Attention", §7
   (the FA2-order forward loop).
 * "FlashAttention and GPU memory" (world.lapla.si explainer), §08 online
@@ -43,3 +44,5 @@ from .online_softmax import (  # noqa: F401
 from .gqa import kv_head_of, expand_kv, attn_fwd64_gqa, attn_bwd64_gqa  # noqa: F401,E402
 from .decode import decode_fwd64, split_kv_states64, merge_splits64, split_bounds  # noqa: F401,E402
 from .fp8 import e4m3_round, e4m3_values, quantize_blocks, dequantize_blocks, attn_fwd64_fp8  # noqa: F401,E402
+from .masks import (visible_mask, attn_fwd64_masked, attn_bwd64_masked, tiled_fwd_block_sparse,  # noqa: F401,E402
+                    blocks_visited)

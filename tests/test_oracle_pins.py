@@ -558,3 +558,140 @@ def test_planted_truncating_e4m3_fails():
 
     want = np.where(np.arange(len(mid)) % 2 == 0, v[:-1], v[1:])
     assert not np.array_equal(truncating(mid), want)
+
+
+# --------------------------------------------------------------------------
+# block-sparse and sliding-window masks (Lecture 8 §5.7, Proposition 4)
+# --------------------------------------------------------------------------
+
+from oracle import masks as MK  # noqa: E402
+
+
+def _qkv(seed, b=1, h=2, n=40, d=6):
+    rng = np.random.default_rng(seed)
+    return tuple(rng.standard_normal((b, h, n, d)) for _ in range(3))
+
+
+def test_mask_special_cases_reduce_to_the_known_masks():
+    n, blk = 40, 8
+    nb = n // blk
+    assert MK.visible_mask(n, block_mask=np.ones((nb, nb)), block=blk).all()
+    np.testing.assert_array_equal(MK.visible_mask(n, True, block_mask=np.tril(np.ones((nb, nb))), block=blk),
+                                  MK.visible_mask(n, True))
+    np.testing.assert_array_equal(MK.visible_mask(n, True, window=n), MK.visible_mask(n, True))
+    vis = MK.visible_mask(n, True, window=5)
+    np.testing.assert_array_equal(vis.sum(axis=1), np.minimum(np.arange(n) + 1, 5))
+    vis2 = MK.visible_mask(n, False, window=5)
+    np.testing.assert_array_equal(vis2.sum(axis=1), [min(i, 4) + min(n - 1 - i, 4) + 1 for i in range(n)])
+
+
+def test_masked_definition_agrees_with_the_standard_one():
+    q, k, v = _qkv(81)
+    n = q.shape[2]
+    for causal in (False, True):
+        o, lse = MK.attn_fwd64_masked(q, k, v, 0.4, MK.visible_mask(n, causal))
+        o_ref, l_ref = oracle.attn_fwd64(q, k, v, 0.4, causal)
+        np.testing.assert_allclose(o, o_ref, atol=1e-14)
+        np.testing.assert_allclose(lse, l_ref, atol=1e-14)
+
+
+def test_window_of_one_and_local_windows_in_closed_form():
+    q, k, v = _qkv(82)
+    n = q.shape[2]
+    o, lse = MK.attn_fwd64_masked(q, k, v, 0.7, MK.visible_mask(n, True, window=1))
+    np.testing.assert_allclose(o, v, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.7 * np.einsum("bhnd,bhnd->bhn", q, k), atol=1e-14)
+    # a causal window of w: row i is ordinary attention over keys i-w+1 .. i
+    w = 6
+    o, lse = MK.attn_fwd64_masked(q, k, v, 0.7, MK.visible_mask(n, True, window=w))
+    for i in (0, 3, 5, 6, 17, n - 1):
+        lo = max(0, i - w + 1)
+        s = 0.7 * k[0, 1, lo:i + 1] @ q[0, 1, i]
+        p = np.exp(s - s.max())
+        np.testing.assert_allclose(o[0, 1, i], p @ v[0, 1, lo:i + 1] / p.sum(), atol=1e-14)
+        np.testing.assert_allclose(lse[0, 1, i], s.max() + np.log(p.sum()), atol=1e-14)
+
+
+def test_block_diagonal_mask_is_independent_attention_per_block():
+    q, k, v = _qkv(83, n=48)
+    blk = 16
+    bm = np.eye(3)
+    o, lse = MK.attn_fwd64_masked(q, k, v, 0.3, MK.visible_mask(48, block_mask=bm, block=blk))
+    for c in range(3):
+        sl = slice(c * blk, (c + 1) * blk)
+        o_ref, l_ref = oracle.attn_fwd64(q[:, :, sl], k[:, :, sl], v[:, :, sl], 0.3, False)
+        np.testing.assert_allclose(o[:, :, sl], o_ref, atol=1e-14)
+        np.testing.assert_allclose(lse[:, :, sl], l_ref, atol=1e-14)
+
+
+def test_rows_with_no_visible_key():
+    q, k, v = _qkv(84, n=32)
+    bm = np.ones((4, 4))
+    bm[2, :] = 0  # query block 2 sees nothing
+    vis = MK.visible_mask(32, block_mask=bm, block=8)
+    o, lse = MK.attn_fwd64_masked(q, k, v, 0.5, vis)
+    assert np.all(o[:, :, 16:24] == 0) and np.all(lse[:, :, 16:24] == -np.inf)
+    rng = np.random.default_rng(85)
+    do = rng.standard_normal(q.shape)
+    dq, dk, dv = MK.attn_bwd64_masked(q, k, v, do, 0.5, vis)
+    assert np.all(dq[:, :, 16:24] == 0)
+    # those rows' dO reaches no key: changing it leaves dK, dV unchanged
+    do2 = do.copy()
+    do2[:, :, 16:24] += 3.0
+    _, dk2, dv2 = MK.attn_bwd64_masked(q, k, v, do2, 0.5, vis)
+    np.testing.assert_array_equal(dk, dk2)
+    np.testing.assert_array_equal(dv, dv2)
+
+
+def test_block_sparse_tiled_forward_equals_definition_and_visits_nonzero_blocks():
+    rng = np.random.default_rng(86)
+    n, blk = 70, 16
+    nb = (n + blk - 1) // blk
+    q, k, v = (rng.standard_normal((n, 8)) for _ in range(3))
+    for causal, window, dens in [(False, 0, 0.5), (True, 0, 0.6), (True, 20, 1.0), (False, 9, 0.7), (True, 0, 1.0)]:
+        bm = (rng.random((nb, nb)) < dens).astype(np.uint8)
+        bm[:, 0] = 1  # every row sees at least its first block unless the window removes it
+        vis = MK.visible_mask(n, causal, window, bm, blk)
+        o, lse, visited = MK.tiled_fwd_block_sparse(q, k, v, 0.45, vis, blk)
+        o_ref, l_ref = MK.attn_fwd64_masked(q[None, None], k[None, None], v[None, None], 0.45, vis)
+        np.testing.assert_allclose(o, o_ref[0, 0], atol=1e-13)
+        np.testing.assert_allclose(lse, l_ref[0, 0], atol=1e-13)
+        assert visited == MK.blocks_visited(n, causal, window, bm, blk).sum()
+    # the causal example of the page: 136 of 16 x 16 blocks
+    assert MK.blocks_visited(16 * 128, True).sum() == 136
+
+
+def test_masked_backward_against_finite_differences():
+    rng = np.random.default_rng(87)
+    n, d, blk = 10, 3, 4
+    q, k, v, do = (rng.standard_normal((1, 1, n, d)) for _ in range(4))
+    bm = np.array([[1, 0, 1], [1, 1, 0], [0, 1, 1]])
+    vis = MK.visible_mask(n, True, 4, bm, blk)
+    dq, dk, dv = MK.attn_bwd64_masked(q, k, v, do, 0.6, vis)
+
+    def f(q_, k_, v_):
+        return (MK.attn_fwd64_masked(q_, k_, v_, 0.6, vis)[0] * do).sum()
+
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            fp = f(args["q"], args["k"], args["v"])
+            args[name] = xm
+            fm = f(args["q"], args["k"], args["v"])
+            num[idx] = (fp - fm) / (2 * h)
+        np.testing.assert_allclose(g, num, atol=1e-8, rtol=1e-6)
+
+
+def test_planted_window_off_by_one_fails():
+    q, k, v = _qkv(88)
+    n = q.shape[2]
+    wrong = np.abs(np.arange(n)[:, None] - np.arange(n)[None, :]) <= 1  # slip: <= w instead of < w
+    wrong &= np.arange(n)[None, :] <= np.arange(n)[:, None]
+    o, _ = MK.attn_fwd64_masked(q, k, v, 0.7, wrong)
+    assert np.abs(o - v).max() > 1e-3  # the window-of-one closed form O = V catches it
