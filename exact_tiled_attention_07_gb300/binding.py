@@ -20,7 +20,7 @@ __all__ = [
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
-    "fa_quantize_fp8", "fa_fwd_fp8", "attention_forward", "attention_backward", "attention_decode",
+    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked", "attention_forward", "attention_backward", "attention_decode",
     "attention_forward_fp8", "quantize_fp8", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
-    "fa_quantize_fp8", "fa_fwd_fp8",
+    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked",
 )
 
 _lib = None
@@ -78,6 +78,8 @@ def load_library():
         lib.fa_decode_workspace_size.restype = sz
         lib.fa_decode.argtypes = [vp] * 5 + [i] * 6 + [f, i, i, vp, sz, vp]
         lib.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+        lib.fa_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, i, i, vp]
+        lib.fa_bwd_masked.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, vp, i, i, vp]
         lib.fa_fwd_fp8.argtypes = [vp] * 8 + [i, i, i, i, f, i, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
@@ -87,6 +89,7 @@ def load_library():
         lib.fa_last_error_message.argtypes = []
         lib.fa_last_error_message.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_quantize_fp8", "fa_fwd_fp8",
+                     "fa_fwd_masked", "fa_bwd_masked",
                      "fa_bwd_noalloc", "fa_bwd_preprocess",
                      "fa_bwd_main", "fa_bwd_dq_convert",
                      "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
@@ -265,6 +268,38 @@ def fa_fwd_fp8(Q8, K8, V8, q_scales, k_scales, v_scales, O, L, scale, causal, st
                                      B, H, N, d, float(scale), int(bool(causal)), _dt(O), _stream(stream)))
 
 
+def _mask_args(block_mask, H):
+    """(pointer, mask_heads) of a uint8 block mask [nb, nb] (shared) or [H, nb, nb] (per head)."""
+    if block_mask is None:
+        return ctypes.c_void_p(0), 0
+    if block_mask.dtype != torch.uint8 or not block_mask.is_contiguous() or not block_mask.is_cuda:
+        raise ValueError("block_mask must be a contiguous uint8 CUDA tensor")
+    heads = 1 if block_mask.dim() == 2 else block_mask.shape[0]
+    return _p(block_mask), heads
+
+
+def fa_fwd_masked(Q, K, V, O, L, scale, causal, window=0, block_mask=None, stream=None):
+    """Forward with a sliding window and/or a block mask over 128 x 128 score blocks."""
+    B, H, N, d = _shape4(Q)
+    _, Hkv, _, _ = _shape4(K)
+    _same(Q, O)
+    mp, mh = _mask_args(block_mask, H)
+    _check(load_library().fa_fwd_masked(_p(Q), _p(K), _p(V), _p(O), _p(L), B, H, Hkv, N, d, float(scale),
+                                        int(bool(causal)), int(window), mp, mh, _dt(Q), _stream(stream)))
+
+
+def fa_bwd_masked(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, window=0, block_mask=None, stream=None):
+    """Backward of fa_fwd_masked (same mask)."""
+    B, H, N, d = _shape4(Q)
+    _, Hkv, _, _ = _shape4(K)
+    _same(Q, O, dO, dQ)
+    mp, mh = _mask_args(block_mask, H)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load_library().fa_bwd_masked(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV),
+                                        _p(workspace), nbytes, B, H, Hkv, N, d, float(scale), int(bool(causal)),
+                                        int(window), mp, mh, _dt(Q), _stream(stream)))
+
+
 def fa_check_device_error(stream=None):
     _check(load_library().fa_check_device_error(_stream(stream)))
 
@@ -293,28 +328,35 @@ def fa_last_error_message() -> str:
 # ---------------------------------------------------------------------------
 
 
-def attention_forward(q, k, v, causal=False, scale=None, stream=None):
-    """O, L = fa_fwd(q, k, v) (fa_fwd_gqa when k, v have fewer heads than q); outputs on q's device."""
+def attention_forward(q, k, v, causal=False, scale=None, stream=None, window=0, block_mask=None):
+    """O, L = fa_fwd(q, k, v) (fa_fwd_gqa when k, v have fewer heads than q; fa_fwd_masked with a
+    window or a block mask); outputs on q's device."""
     B, H, N, d = _shape4(q)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if k.shape[1] != H:
+    if window or block_mask is not None:
+        fa_fwd_masked(q, k, v, o, lse, scale, causal, window, block_mask, stream)
+    elif k.shape[1] != H:
         fa_fwd_gqa(q, k, v, o, lse, scale, causal, stream)
     else:
         fa_fwd(q, k, v, o, lse, scale, causal, stream)
     return o, lse
 
 
-def attention_backward(q, k, v, o, do, lse, causal=False, scale=None, workspace=None, stream=None):
-    """dQ, dK, dV = fa_bwd(...); outputs (and workspace, unless given) allocated with torch."""
+def attention_backward(q, k, v, o, do, lse, causal=False, scale=None, workspace=None, stream=None, window=0,
+                       block_mask=None):
+    """dQ, dK, dV = fa_bwd(...) (fa_bwd_masked with a window or a block mask); outputs (and
+    workspace, unless given) allocated with torch."""
     B, H, N, d = _shape4(q)
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         nbytes = fa_bwd_workspace_size(B, H, N, d)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
-    if k.shape[1] != H:
+    if window or block_mask is not None:
+        fa_bwd_masked(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, window, block_mask, stream)
+    elif k.shape[1] != H:
         fa_bwd_gqa(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)
     else:
         fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)

@@ -139,32 +139,66 @@ fa_status check_heads(int H, int Hkv) {
   return FA_OK;
 }
 
+// Masks beyond causal: a window (keys with |i - j| >= window hidden; 0 = none) and a block
+// mask of bytes [mask_heads][nb][nb] over 128 x 128 score blocks (NULL = none).
+struct MaskSpec {
+  int window = 0;
+  const uint8_t* block_mask = nullptr;
+  int mask_heads = 0;
+  bool any() const { return window > 0 || block_mask != nullptr; }
+};
+
+fa_status check_mask(const MaskSpec& m, int H, int Hkv, int N, int d, fa_dtype dtype, bool backward) {
+  if (m.window < 0) return fail(FA_ERR_INVALID_ARG, "window must be >= 0 (0: none), got %d", m.window);
+  if (m.block_mask) {
+    if (m.mask_heads != 1 && m.mask_heads != H)
+      return fail(FA_ERR_INVALID_ARG, "mask_heads must be 1 or H=%d, got %d", H, m.mask_heads);
+  } else if (m.mask_heads != 0) {
+    return fail(FA_ERR_INVALID_ARG, "mask_heads=%d without a block mask (must be 0)", m.mask_heads);
+  }
+  if (!m.any()) return FA_OK;
+  const bool tc = backward ? bwd_tc_supported((int)dtype, d) : fwd_tc_supported((int)dtype, d);
+  if (!tc)
+    return fail(FA_ERR_UNSUPPORTED, "block and window masks run on the tensor-core kernels (bf16/fp16, d in %s)",
+                backward ? "{64, 128}" : "{64, 128, 256}");
+  const bool fits = backward ? bwd_masked_fits(H / Hkv, N, d) : fwd_masked_fits(N, d);
+  if (!fits) return fail(FA_ERR_UNSUPPORTED, "masked problem too long for the kernels' tile lists (N=%d)", N);
+  return FA_OK;
+}
+
 fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv, int N,
-                   int d, float scale, int causal, fa_dtype dtype, void* stream, const char* name) {
+                   int d, float scale, int causal, fa_dtype dtype, void* stream, const char* name,
+                   const MaskSpec& mask = MaskSpec()) {
   bool empty;
   fa_status st = check_common(B, H, N, d, dtype, &empty);
   if (st != FA_OK || empty) return st;
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if ((st = check_ptrs({Q, K, V, O, L}, name)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
+  if ((st = check_mask(mask, H, Hkv, N, d, dtype, false)) != FA_OK) return st;
   DeviceSyms syms;
   if ((st = device_syms(&syms)) != FA_OK) return st;
   FwdArgs a{Q, K, V, O, L, B * H, N, d, scale, causal ? 1 : 0, (int)dtype, syms.err, syms.counter,
             static_cast<cudaStream_t>(stream)};
   a.group = H / Hkv;
+  a.window = mask.window;
+  a.block_mask = mask.block_mask;
+  a.mask_heads = mask.mask_heads;
+  a.heads = H;
   if (fwd_tc_supported(a.dtype, d)) return launched(launch_fwd_tc(a), "forward (tensor-core kernel)");
   return launched(launch_fwd_simt(a), "forward (CUDA-core kernel)");
 }
 
 fa_status bwd_main_impl(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
                         void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale,
-                        int causal, fa_dtype dtype, void* stream, const char* name) {
+                        int causal, fa_dtype dtype, void* stream, const char* name, const MaskSpec& mask = MaskSpec()) {
   bool empty;
   fa_status st = check_common(B, H, N, d, dtype, &empty);
   if (st != FA_OK || empty) return st;
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if ((st = check_ptrs({Q, K, V, dO, dK, dV, workspace}, name)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
+  if ((st = check_mask(mask, H, Hkv, N, d, dtype, true)) != FA_OK) return st;
   BwdArgs a{};
   if ((st = carve(&a, workspace, workspace_bytes, B, H, N, d)) != FA_OK) return st;
   DeviceSyms syms;
@@ -185,6 +219,10 @@ fa_status bwd_main_impl(const void* Q, const void* K, const void* V, const void*
   a.counter = syms.counter;
   a.stream = static_cast<cudaStream_t>(stream);
   a.group = H / Hkv;
+  a.window = mask.window;
+  a.block_mask = mask.block_mask;
+  a.mask_heads = mask.mask_heads;
+  a.heads = H;
   if (bwd_tc_supported(a.dtype, d)) return launched(launch_bwd_tc(a), "backward (tensor-core kernel)");
   return launched(launch_bwd_simt(a), "backward (CUDA-core kernels)");
 }
@@ -266,6 +304,38 @@ fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O,
   if ((st = fa_bwd_preprocess(O, dO, L, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK) return st;
   if ((st = bwd_main_impl(Q, K, V, dO, dK, dV, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, dtype,
                           stream, "fa_bwd")) != FA_OK)
+    return st;
+  return fa_bwd_dq_convert(workspace, workspace_bytes, dQ, B, H, N, d, scale, dtype, stream);
+}
+
+fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv, int N,
+                        int d, float scale, int causal, int window, const uint8_t* block_mask, int mask_heads,
+                        fa_dtype dtype, void* stream) {
+  MaskSpec m;
+  m.window = window;
+  m.block_mask = block_mask;
+  m.mask_heads = mask_heads;
+  return fwd_impl(Q, K, V, O, L, B, H, Hkv, N, d, scale, causal, dtype, stream, "fa_fwd_masked", m);
+}
+
+fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
+                        void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                        int N, int d, float scale, int causal, int window, const uint8_t* block_mask, int mask_heads,
+                        fa_dtype dtype, void* stream) {
+  MaskSpec m;
+  m.window = window;
+  m.block_mask = block_mask;
+  m.mask_heads = mask_heads;
+  bool empty;
+  fa_status st = check_common(B, H, N, d, dtype, &empty);
+  if (st != FA_OK || empty) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
+  if ((st = check_ptrs({Q, K, V, O, dO, L, dQ, dK, dV, workspace}, "fa_bwd_masked")) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if ((st = check_mask(m, H, Hkv, N, d, dtype, true)) != FA_OK) return st;
+  if ((st = fa_bwd_preprocess(O, dO, L, workspace, workspace_bytes, B, H, N, d, dtype, stream)) != FA_OK) return st;
+  if ((st = bwd_main_impl(Q, K, V, dO, dK, dV, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, dtype,
+                          stream, "fa_bwd_masked", m)) != FA_OK)
     return st;
   return fa_bwd_dq_convert(workspace, workspace_bytes, dQ, B, H, N, d, scale, dtype, stream);
 }

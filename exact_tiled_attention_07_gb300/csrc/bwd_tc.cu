@@ -66,6 +66,11 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_VEC + QSTAGES * 2 * BM * 4;
   static constexpr int NBAR = 16;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  // masked variant: the CTA's step list after the barriers (an int count, then uint16 entries
+  // (query head of the group << 12 | 128-row query block), rounded up to 8 entries)
+  static constexpr int OFF_LIST = SMEM;
+  static constexpr int list_bytes(int entries) { return 16 + 2 * ((entries + 7) & ~7); }
+  static constexpr int SUB = 128 / BM;  // steps per 128-row query block
   // TMEM columns: K_j as a 16-bit A operand (d/2 columns), S^T (P^T over its first BM/2),
   // dP^T (dS^T over its first BM/2), the dQ partial and the dV, dK accumulators
   static constexpr uint32_t COL_K = DQT ? 0 : 448;
@@ -106,13 +111,17 @@ __device__ __forceinline__ void store_row16(void* base, int64_t row, const uint3
   for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
 }
 
-template <int D, bool BF16>
+// Masked variant (block mask and/or window): one warp lists, before the roles start, the
+// (query head of the group, 128-row query block) pairs that can see this key tile (block-mask
+// byte set and some pair inside the causal and window bounds); every role walks that list.
+template <int D, bool BF16, bool MASKED>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
                   const float* __restrict__ delta, void* __restrict__ dk_out, void* __restrict__ dv_out, int n,
-                  int npad, int bh_count, int ktiles, float scale, int causal, int group, unsigned long long* err) {
+                  int npad, int bh_count, int ktiles, float scale, int causal, int group, unsigned long long* err,
+                  int window, const uint8_t* __restrict__ block_mask, int mask_heads, int heads) {
   using C = BwdCfg<D>;
   constexpr int BM = C::BM;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -137,7 +146,49 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const int i_start = causal ? kt * (BN / BM) : 0;  // first query tile reaching this key tile's diagonal
   // steps: (query head of this key/value head's group, query tile) pairs; dK, dV sum over all
   const int nsteps_head = qtiles - i_start;
-  const int nsteps = group * nsteps_head;
+  int nsteps = group * nsteps_head;
+  int* list_hdr = reinterpret_cast<int*>(smem + C::OFF_LIST);
+  uint16_t* slist = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST + 16);
+  if constexpr (MASKED) {
+    if (warp == C::PRODUCER_WARP) {
+      const int nblk = (n + 127) / 128;
+      const int kmax = min(n, k0 + BN) - 1;
+      int count = 0;
+      for (int g = 0; g < group; ++g) {
+        const int qh = kvh * group + g;
+        const uint8_t* mcol = block_mask ? block_mask + (int64_t)(mask_heads > 1 ? qh % heads : 0) * nblk * nblk + kt
+                                         : nullptr;
+        for (int base = 0; base < nblk; base += 32) {
+          const int qb = base + lane;
+          bool v = qb < nblk;
+          if (v) {
+            const int qmin = qb * 128, qmax = min(n, qmin + 128) - 1;
+            if (mcol) v = mcol[(int64_t)qb * nblk] != 0;
+            if (causal) v = v && k0 <= qmax;
+            if (window > 0) {
+              v = v && qmin - kmax < window;
+              if (!causal) v = v && k0 - qmax < window;
+            }
+          }
+          const unsigned any = __ballot_sync(0xffffffffu, v);
+          if (v) slist[count + __popc(any & ((1u << lane) - 1u))] = (uint16_t)((g << 12) | qb);
+          count += __popc(any);
+        }
+      }
+      if (lane == 0) list_hdr[0] = count;
+    }
+  }
+  // step i -> (query head within the group, first query row)
+  auto step_rows = [&](int i, int ii, int g, int* gm, int* q0) {
+    if constexpr (MASKED) {
+      const uint32_t e = slist[i / C::SUB];
+      *gm = (int)(e >> 12);
+      *q0 = (int)(e & 0xFFFu) * 128 + (i % C::SUB) * BM;
+    } else {
+      *gm = g;
+      *q0 = (i_start + ii) * BM;
+    }
+  };
   // each role walks the steps with a (query tile ii, query head g of the group) cursor, advanced
   // by step_next (no integer division on the per-step path)
   const float scale_log2 = scale * 1.4426950408889634f;
@@ -170,6 +221,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const bool start_ok = (*abort_flag == 0);
+  if constexpr (MASKED) nsteps = list_hdr[0] * C::SUB;
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
@@ -187,7 +239,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       for (int i = 0, ii = 0, g = 0; i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
         const int s = i % C::QSTAGES, use = i / C::QSTAGES;
         if (use > 0 && !mbar_wait(bar + B_QD_EMPTY + s, (use - 1) & 1, ctx, 110)) break;
-        const int q0 = (i_start + ii) * BM, qh = kvh * group + g;
+        int gm, q0;
+        step_rows(i, ii, g, &gm, &q0);
+        const int qh = kvh * group + gm;
         uint64_t* fb = bar + B_QD_FULL + s;
         mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + 2 * BM * 4);
         for (int kb = 0; kb < C::KB; ++kb) {
@@ -374,7 +428,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     for (int i = 0, ii = 0, g = 0; ok && i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
       const int s = i % C::QSTAGES;
-      const int q0 = (i_start + ii) * BM;
+      int gm, q0;
+      step_rows(i, ii, g, &gm, &q0);
       const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
       const float* dvec = l2v + BM;
       // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
@@ -382,8 +437,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, i & 1, ctx, 130));
       if (!ok) break;
       tc_fence_after();
-      // queries q0 + qc with qc < mask_below are in the past of this key (causal diagonal)
-      const int mask_below = causal ? key - q0 : 0;
+      // visible queries q0 + qc: qc in [mask_below, mask_above) (causal: not before this key;
+      // window: |query - key| < window, an upper bound on the query with or without causal)
+      int mask_below = causal ? key - q0 : INT32_MIN, mask_above = INT32_MAX;
+      if constexpr (MASKED) {
+        if (window > 0) {
+          mask_below = max(mask_below, key - window + 1 - q0);
+          mask_above = key + window - q0;
+        }
+      }
       // P^T row (this key against the BM queries), kept as packed 16-bit pairs: the same
       // rounded values feed dV += P^T dO and dS = P o (dP - D)
       uint32_t pk[BM / 2];
@@ -407,7 +469,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           for (int u = 0; u < 4; ++u) {
             const int qc = c * 32 + t + u;
             const float x = ex2(fmaf(__uint_as_float(r[t + u]), scale_log2, -lv[u]));
-            e[u] = (key_ok && qc >= mask_below) ? x : 0.f;
+            e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? x : 0.f;
           }
           pk[(c * 32 + t) / 2] = pack2<BF16>(e[0], e[1]);
           pk[(c * 32 + t) / 2 + 1] = pack2<BF16>(e[2], e[3]);
@@ -507,7 +569,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const bool leader = (warp == 4 && lane == 0);
     bool ok = start_ok;
     for (int i = 0, ii = 0, g = 0; ok && i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
-      const int q0 = (i_start + ii) * BM;
+      int gm, q0;
+      step_rows(i, ii, g, &gm, &q0);
       ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, i & 1, ctx, 140));
       if (!ok) break;
       tc_fence_after();
@@ -540,7 +603,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (leader) {
-        const int qh = kvh * group + g;
+        const int qh = kvh * group + gm;
         if constexpr (C::DQT) {
           tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
         } else {
@@ -561,7 +624,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASKED>
 cudaError_t launch_bwd_d(const BwdArgs& a) {
   using C = BwdCfg<D>;
   const int npad = (int)padded_rows(a.n);
@@ -572,24 +635,44 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
       !make_tmap_16bit_3d(&tdo, a.dout, BF16, D, a.n, a.bh, C::BM) ||
       !make_tmap_f32_3d(&tdq, a.dq_acc, D, npad, a.bh, C::DQT ? D : 32, C::BM, !C::DQT))
     return cudaErrorInvalidValue;
-  auto kern = bwd_tc_kernel<D, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  auto kern = bwd_tc_kernel<D, BF16, MASKED>;
+  const int nblk = (a.n + 127) / 128;
+  if (MASKED && !bwd_masked_fits(a.group, a.n, D)) return cudaErrorInvalidValue;
+  const int smem = C::SMEM + (MASKED ? C::list_bytes(a.group * nblk) : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int ktiles = (a.n + BN - 1) / BN;
-  kern<<<(unsigned)(bh_kv * ktiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, tdo, tdq, a.lse2, a.delta, a.dk, a.dv,
-                                                                      a.n, npad, bh_kv, ktiles, a.scale, a.causal, a.group, a.err);
+  kern<<<(unsigned)(bh_kv * ktiles), C::THREADS, smem, a.stream>>>(tq, tk, tv, tdo, tdq, a.lse2, a.delta, a.dk, a.dv,
+                                                                   a.n, npad, bh_kv, ktiles, a.scale, a.causal, a.group,
+                                                                   a.err, a.window, a.block_mask, a.mask_heads,
+                                                                   a.heads);
   return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_dm(const BwdArgs& a) {
+  return a.masked() ? launch_bwd_d<D, BF16, true>(a) : launch_bwd_d<D, BF16, false>(a);
 }
 
 }  // namespace
 
 bool bwd_tc_supported(int dtype, int d) { return (dtype == DT_BF16 || dtype == DT_FP16) && (d == 64 || d == 128); }
 
+bool bwd_masked_fits(int group, int n, int d) {
+  // step-list entries pack (query head of the group, 128-row block) into 16 bits, and the
+  // list must fit in shared memory beside the kernel's tiles
+  const int nblk = (n + 127) / 128;
+  if (group > 16 || nblk > 4096) return false;
+  const int smem = (d == 128 ? BwdCfg<128>::SMEM + BwdCfg<128>::list_bytes(group * nblk)
+                             : BwdCfg<64>::SMEM + BwdCfg<64>::list_bytes(group * nblk));
+  return smem <= 232448;
+}
+
 cudaError_t launch_bwd_tc(const BwdArgs& a) {
   const bool bf = a.dtype == DT_BF16;
   switch (a.d) {
-    case 64: return bf ? launch_bwd_d<64, true>(a) : launch_bwd_d<64, false>(a);
-    case 128: return bf ? launch_bwd_d<128, true>(a) : launch_bwd_d<128, false>(a);
+    case 64: return bf ? launch_bwd_dm<64, true>(a) : launch_bwd_dm<64, false>(a);
+    case 128: return bf ? launch_bwd_dm<128, true>(a) : launch_bwd_dm<128, false>(a);
     default: return cudaErrorNotSupported;
   }
 }

@@ -63,6 +63,10 @@ struct FwdCfg {
   static constexpr int OFF_BAR = OFF_RING + STAGES * TILE_BYTES;
   static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  // masked variant: the CTA's key-tile list after the barriers (4 ints, then uint16 tile
+  // indices and uint8 visibility flags, nb rounded up to 16 entries each)
+  static constexpr int OFF_LIST = SMEM;
+  static constexpr int list_bytes(int nb) { return 16 + 3 * ((nb + 15) & ~15); }
 };
 
 struct FwdSmemBars {
@@ -76,12 +80,19 @@ struct FwdSmemBars {
   uint64_t* drain;    // [1]
 };
 
-template <int D, bool BF16>
+// Masked variant (block mask and/or window, "Lecture 8" §5.7 block-sparse attention): one warp
+// lists, before the roles start, the key tiles that either query tile of the CTA can see (a
+// tile is skipped when its block-mask byte is 0 or the causal/window bounds leave no visible
+// score in it) with a flag per query tile; the producer, the MMA warp and the softmax walk
+// that list.  A query tile processes every listed tile up to its own last visible one, the
+// ones it cannot see fully masked, so both tiles keep the same ping-pong schedule.
+template <int D, bool BF16, bool MASKED>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, float* __restrict__ lse, int n,
                   int bh_count, int tiles_per_head, float scale_log2, int causal, int group, unsigned long long* err,
-                  unsigned long long* counter) {
+                  unsigned long long* counter, int window, const uint8_t* __restrict__ block_mask, int mask_heads,
+                  int heads) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -127,7 +138,60 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       nq[q] = nblocks;
     }
   }
-  const int nmax = max(nq[0], nq[1]);
+  int* list_hdr = reinterpret_cast<int*>(smem + C::OFF_LIST);  // nq[0], nq[1], visible tiles of q 0, 1
+  uint16_t* jlist = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST + 16);
+  uint8_t* jflag = reinterpret_cast<uint8_t*>(jlist + ((nblocks + 15) & ~15));
+  if constexpr (MASKED) {
+    if (warp == C::PRODUCER_WARP) {
+      // visible key tiles of query tile q: block-mask byte set, and some (row, key) pair of the
+      // two tiles inside the causal and window bounds
+      int qr0[2], qr1[2];
+      const uint8_t* mrow[2] = {nullptr, nullptr};
+      const int mh = mask_heads > 1 ? head % heads : 0;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        qr0[q] = qrow0 + q * BM;
+        qr1[q] = min(n, qr0[q] + BM) - 1;
+        if (block_mask && q < C::NQ && qr0[q] < n)
+          mrow[q] = block_mask + ((int64_t)mh * nblocks + qr0[q] / BM) * nblocks;
+      }
+      auto visible = [&](int q, int j) {
+        if (q >= C::NQ || qr0[q] >= n) return false;
+        const int kmin = j * BN, kmax = min(n, kmin + BN) - 1;
+        bool v = !block_mask || mrow[q][j] != 0;
+        if (causal) v = v && kmin <= qr1[q];
+        if (window > 0) {
+          v = v && qr0[q] - kmax < window;
+          if (!causal) v = v && kmin - qr1[q] < window;
+        }
+        return v;
+      };
+      int count = 0, last0 = -1, last1 = -1, nv0 = 0, nv1 = 0;
+      for (int base = 0; base < nblocks; base += 32) {
+        const int j = base + lane;
+        const bool v0 = j < nblocks && visible(0, j);
+        const bool v1 = j < nblocks && visible(1, j);
+        const unsigned any = __ballot_sync(0xffffffffu, v0 || v1);
+        const unsigned b0 = __ballot_sync(0xffffffffu, v0), b1 = __ballot_sync(0xffffffffu, v1);
+        if (v0 || v1) {
+          const int pos = count + __popc(any & ((1u << lane) - 1u));
+          jlist[pos] = (uint16_t)j;
+          jflag[pos] = (uint8_t)((v0 ? 1 : 0) | (v1 ? 2 : 0));
+        }
+        if (b0) last0 = count + __popc(any & ((1u << (31 - __clz(b0))) - 1u));
+        if (b1) last1 = count + __popc(any & ((1u << (31 - __clz(b1))) - 1u));
+        nv0 += __popc(b0);
+        nv1 += __popc(b1);
+        count += __popc(any);
+      }
+      if (lane == 0) {
+        list_hdr[0] = last0 + 1;
+        list_hdr[1] = last1 + 1;
+        list_hdr[2] = nv0;
+        list_hdr[3] = nv1;
+      }
+    }
+  }
 
   if (threadIdx.x == 0) {
     if ((smem_u32(smem) & 1023u) != 0) report_error(err, DERR_BAD_SMEM_ALIGN, 0);
@@ -155,6 +219,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const bool start_ok = (*abort_flag == 0);
+  if constexpr (MASKED) {
+    nq[0] = list_hdr[0];
+    nq[1] = list_hdr[1];
+  }
+  const int nmax = max(nq[0], nq[1]);
+  // key tile at position t of the CTA's sequence
+  auto tile_at = [&](int t) { return MASKED ? (int)jlist[t] : t; };
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
@@ -175,7 +246,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
         const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, kb * 64, (idx >> 1) * BN, kvhead);
+          tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, kb * 64, tile_at(idx >> 1) * BN, kvhead);
         issued = idx + 1;
       }
       // drain: every copy this thread started must land before the CTA may exit
@@ -352,13 +423,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
-      // mask: keys past N, and (causal) keys after this row
-      int limit = n - j * BN;
-      if (causal) limit = min(limit, row - j * BN + 1);
-      if (limit < BN) {
+      // visible columns [lo, hi) of this row: keys before N, (causal) not after the row,
+      // (window) within the window; none when the tile is listed only for the other query tile
+      const int jt = tile_at(j);
+      int lo = 0, hi = n - jt * BN;
+      if (causal) hi = min(hi, row - jt * BN + 1);
+      if constexpr (MASKED) {
+        if (window > 0) {
+          lo = row - window + 1 - jt * BN;
+          if (!causal) hi = min(hi, row + window - jt * BN);
+        }
+        if (!((jflag[j] >> q) & 1)) hi = lo = 0;
+      }
+      if (lo > 0 || hi < BN) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          if (c >= limit) s[c] = -INFINITY;
+          if (c < lo || c >= hi) s[c] = -INFINITY;
       }
       const float mx = row_max(s);
       const float m_blk = mx * scale_log2;
@@ -440,8 +520,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
         }
         if (row < n) lse[(int64_t)head * n + row] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-        if (counter && rit == 0) atomicAdd(counter, (unsigned long long)nb);
+        if (counter && rit == 0) atomicAdd(counter, (unsigned long long)(MASKED ? list_hdr[2 + q] : nb));
       }
+    } else if (MASKED && ok && nb == 0 && row < n) {
+      // no listed key tile for this query tile: its rows see no key (O = 0, L = -inf)
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2);
+#pragma unroll 1
+      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+      lse[(int64_t)head * n + row] = -INFINITY;
     }
   }
 
@@ -453,7 +539,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool MASKED>
 cudaError_t launch_fwd_d(const FwdArgs& a) {
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
@@ -461,17 +547,33 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
   if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) ||
       !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN))
     return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<D, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  auto kern = fwd_tc_kernel<D, BF16, MASKED>;
+  const int nblocks = (a.n + BN - 1) / BN;
+  const int smem = C::SMEM + (MASKED ? C::list_bytes(nblocks) : 0);
+  if (smem > 232448) return cudaErrorInvalidValue;  // key-tile list too long for shared memory
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  kern<<<(unsigned)(a.bh * tiles), C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles,
-                                                                     scale_log2, a.causal, a.group, a.err, a.counter);
+  kern<<<(unsigned)(a.bh * tiles), C::THREADS, smem, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
+                                                                 a.causal, a.group, a.err, a.counter, a.window,
+                                                                 a.block_mask, a.mask_heads, a.heads);
   return cudaGetLastError();
 }
 
+template <int D, bool BF16>
+cudaError_t launch_fwd_dm(const FwdArgs& a) {
+  return a.masked() ? launch_fwd_d<D, BF16, true>(a) : launch_fwd_d<D, BF16, false>(a);
+}
+
 }  // namespace
+
+bool fwd_masked_fits(int n, int d) {
+  const int nb = (n + BN - 1) / BN;
+  if (nb > 65535) return false;
+  const int base = d == 64 ? FwdCfg<64>::SMEM : (d == 128 ? FwdCfg<128>::SMEM : FwdCfg<256>::SMEM);
+  return base + FwdCfg<64>::list_bytes(nb) <= 232448;
+}
 
 bool fwd_tc_supported(int dtype, int d) {
   return (dtype == DT_BF16 || dtype == DT_FP16) && (d == 64 || d == 128 || d == 256);
@@ -480,9 +582,9 @@ bool fwd_tc_supported(int dtype, int d) {
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
   const bool bf = a.dtype == DT_BF16;
   switch (a.d) {
-    case 64: return bf ? launch_fwd_d<64, true>(a) : launch_fwd_d<64, false>(a);
-    case 128: return bf ? launch_fwd_d<128, true>(a) : launch_fwd_d<128, false>(a);
-    case 256: return bf ? launch_fwd_d<256, true>(a) : launch_fwd_d<256, false>(a);
+    case 64: return bf ? launch_fwd_dm<64, true>(a) : launch_fwd_dm<64, false>(a);
+    case 128: return bf ? launch_fwd_dm<128, true>(a) : launch_fwd_dm<128, false>(a);
+    case 256: return bf ? launch_fwd_dm<256, true>(a) : launch_fwd_dm<256, false>(a);
     default: return cudaErrorNotSupported;
   }
 }

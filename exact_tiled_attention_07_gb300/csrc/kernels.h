@@ -26,6 +26,14 @@ struct FwdArgs {
   unsigned long long* counter;  // device count of processed (query tile, key tile) pairs
   cudaStream_t stream;
   int group = 1;  // query heads per key/value head: K, V hold bh / group heads
+  // masks beyond causal (0 / null: none): keys with |i - j| >= window are hidden, and the
+  // 128 x 128 score blocks whose byte in block_mask [mask_heads][nb][nb] is 0 (mask_heads is 1
+  // or the number of query heads `heads`; nb = ceil(n / 128))
+  int window = 0;
+  const uint8_t* block_mask = nullptr;
+  int mask_heads = 0;
+  int heads = 1;
+  bool masked() const { return window > 0 || block_mask != nullptr; }
 };
 
 // Backward workspace, carved from one caller buffer of fa_bwd_workspace_size bytes:
@@ -55,6 +63,11 @@ struct BwdArgs {
   unsigned long long* counter;
   cudaStream_t stream;
   int group = 1;  // query heads per key/value head: K, V, dK, dV hold bh / group heads
+  int window = 0;  // masks beyond causal, as in FwdArgs
+  const uint8_t* block_mask = nullptr;
+  int mask_heads = 0;
+  int heads = 1;
+  bool masked() const { return window > 0 || block_mask != nullptr; }
 };
 
 // Decode over a key/value cache: Q, O [b][h][nq][d], K, V [b][hkv][nk][d], L [b][h][nq].
@@ -123,6 +136,8 @@ int set_last_error(int status, const char* fmt, ...);
 
 bool fwd_tc_supported(int dtype, int d);
 bool bwd_tc_supported(int dtype, int d);
+bool bwd_masked_fits(int group, int n, int d);  // masked backward's step list fits (tensor-core path)
+bool fwd_masked_fits(int n, int d);             // masked forward's key-tile list fits
 
 cudaError_t launch_fwd_tc(const FwdArgs& a);
 cudaError_t launch_fwd_simt(const FwdArgs& a);

@@ -320,7 +320,9 @@ __global__ void __launch_bounds__(256) bwd_pre(const T* __restrict__ O, const T*
   }
   if (lane == 0) {
     delta[gw] = row < n ? acc : 0.f;
-    lse2[gw] = row < n ? lse[bh * n + row] * 1.4426950408889634f : INFINITY;
+    // +inf (P = 0) on padding rows and on rows that saw no key (L = -inf)
+    const float lv = row < n ? lse[bh * n + row] : -INFINITY;
+    lse2[gw] = lv > -INFINITY ? lv * 1.4426950408889634f : INFINITY;
   }
   float* q = dq_acc + gw * d;
   for (int c = lane; c < d; c += 32) q[c] = 0.f;
@@ -366,7 +368,8 @@ __global__ void __launch_bounds__(256) bwd_pre_vec(const T* __restrict__ O, cons
   if (!active) return;
   if (sub == 0) {
     delta[grow] = row < n ? acc : 0.f;
-    lse2[grow] = row < n ? lse[bh * n + row] * 1.4426950408889634f : INFINITY;
+    const float lv = row < n ? lse[bh * n + row] : -INFINITY;
+    lse2[grow] = lv > -INFINITY ? lv * 1.4426950408889634f : INFINITY;
   }
   float4* q = reinterpret_cast<float4*>(dq_acc + grow * d + sub * 8);
   q[0] = make_float4(0.f, 0.f, 0.f, 0.f);

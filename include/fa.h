@@ -39,6 +39,7 @@
 #define FA_H_
 
 #include <stddef.h>
+#include <stdint.h>
 
 #if defined(__GNUC__)
 #define FA_API __attribute__((visibility("default")))
@@ -181,6 +182,33 @@ FA_API size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, in
 FA_API fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv,
                            int Nq, int Nk, int d, float scale, int splits, fa_dtype dtype, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/*
+ * Attention with a block-sparse mask and/or a sliding window ("Lecture 8" §5.7: block-sparse
+ * FlashAttention computes only the non-zero B_r x B_c blocks of S, and reads, writes and FLOPs
+ * fall in proportion, Proposition 4; the sliding window is the local approximation).
+ * Key j is visible to query i when all of these hold:
+ *   block_mask  NULL, or byte [i / 128][j / 128] of the head's [nb][nb] mask is non-zero
+ *               (nb = ceil(N / 128); device memory, mask_heads masks of nb * nb bytes:
+ *               mask_heads = 1 shares one mask, mask_heads = H gives one per query head;
+ *               mask_heads must be 0 when block_mask is NULL)
+ *   causal      j <= i (when causal != 0)
+ *   window      |i - j| < window (when window > 0; with causal: the last `window` positions)
+ * A row that sees no key gets O = 0 and L = -inf and contributes nothing to the gradients.
+ * Blocks with no visible score are never loaded or multiplied. Other arguments, layouts and
+ * errors as fa_fwd_gqa / fa_bwd_gqa. Runs on the tensor-core kernels only: bf16/fp16 with
+ * d in {64, 128, 256} (forward) or {64, 128} (backward); other dtypes or head dims return
+ * FA_ERR_UNSUPPORTED, as does a sequence whose tile list does not fit in shared memory
+ * (forward: N up to about 1.5M; backward: H/Hkv <= 16 and N <= 524,288, less when the
+ * query heads per key/value head times N/128 passes about 4,000 for d = 128).
+ */
+FA_API fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv,
+                               int N, int d, float scale, int causal, int window, const uint8_t* block_mask,
+                               int mask_heads, fa_dtype dtype, void* stream);
+FA_API fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                               const float* L, void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                               int B, int H, int Hkv, int N, int d, float scale, int causal, int window,
+                               const uint8_t* block_mask, int mask_heads, fa_dtype dtype, void* stream);
 
 /*
  * FP8 (E4M3) block quantisation ("Lecture 8" §8.1, "FlashAttention and GPU memory" §11: the

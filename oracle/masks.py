@@ -24,8 +24,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["visible_mask", "attn_fwd64_masked", "attn_bwd64_masked", "tiled_fwd_block_sparse", "blocks_visited",
-           "BLOCK"]
+__all__ = ["visible_mask", "visible_row", "attn_fwd64_masked", "attn_bwd64_masked", "attn_fwd64_masked_rows",
+           "tiled_fwd_block_sparse", "blocks_visited", "BLOCK"]
 
 BLOCK = 128
 
@@ -142,3 +142,33 @@ def tiled_fwd_block_sparse(q, k, v, scale, visible, block=BLOCK):
         with np.errstate(divide="ignore"):
             lse[rows] = np.where(seen, m + np.log(np.where(seen, ell, 1.0)), -np.inf)
     return o, lse, visited
+
+
+def visible_row(n, i, causal=False, window=0, block_mask=None, block=BLOCK):
+    """Row i of ``visible_mask`` (block_mask: the head's [nb, nb] mask or None), without the N x N array."""
+    j = np.arange(n)
+    vis = np.ones(n, dtype=bool)
+    if causal:
+        vis &= j <= i
+    if window and window > 0:
+        vis &= np.abs(i - j) < window
+    if block_mask is not None:
+        vis &= np.asarray(block_mask)[i // block, j // block] != 0
+    return vis
+
+
+def attn_fwd64_masked_rows(q, k, v, scale, samples, causal=False, window=0, block_mask=None, block=BLOCK):
+    """O rows [S, dv] and L [S] for sampled (b, h, i) of masked attention (block_mask [nb, nb] or [H, nb, nb])."""
+    out_o = np.zeros((len(samples), np.asarray(v).shape[-1]))
+    out_l = np.zeros(len(samples))
+    n = np.asarray(k).shape[2]
+    for t, (b, h, i) in enumerate(samples):
+        bm = None
+        if block_mask is not None:
+            bm = np.asarray(block_mask)
+            bm = bm if bm.ndim == 2 else bm[h if bm.shape[0] > 1 else 0]
+        vis = visible_row(n, i, causal, window, bm, block)
+        p, lse = _rows_probabilities(np.asarray(q[b, h, i], np.float64)[None], k[b, h], scale, vis[None])
+        out_o[t] = p[0] @ np.asarray(v[b, h], np.float64)
+        out_l[t] = lse[0]
+    return out_o, out_l

@@ -131,3 +131,18 @@ def test_decode_workspace_size_host_rules(lib):
     assert f(1, 8, 3, 1, 100, 128, 4) == 0  # heads do not divide: invalid
     assert f(1, 8, 2, 1, 100, 96, 4) == 0  # unsupported head dim
     assert f(1, 8, 2, 1, 1 << 20, 128, 0) > 0  # long cache: split automatically
+
+
+def test_mask_arguments_are_validated(lib):
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.fa_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, i, vp, i, i, vp]
+    lib.fa_last_error_message.restype = ctypes.c_char_p
+    g = vp(0x10000)
+    # negative window; mask_heads without a mask; mask_heads neither 1 nor H
+    assert lib.fa_fwd_masked(g, g, g, g, g, 1, 4, 4, 128, 64, 0.125, 1, -1, None, 0, 0, None) == 1
+    assert lib.fa_fwd_masked(g, g, g, g, g, 1, 4, 4, 128, 64, 0.125, 1, 8, None, 1, 0, None) == 1
+    assert lib.fa_fwd_masked(g, g, g, g, g, 1, 4, 4, 128, 64, 0.125, 0, 0, g, 3, 0, None) == 1
+    assert b"mask_heads" in lib.fa_last_error_message()
+    # masks run on the tensor-core kernels only: fp32 and odd head dims are unsupported
+    assert lib.fa_fwd_masked(g, g, g, g, g, 1, 4, 4, 128, 64, 0.125, 1, 8, None, 0, 2, None) == 2
+    assert lib.fa_fwd_masked(g, g, g, g, g, 1, 4, 4, 128, 96, 0.125, 1, 8, None, 0, 0, None) == 2

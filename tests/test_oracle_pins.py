@@ -695,3 +695,17 @@ def test_planted_window_off_by_one_fails():
     wrong &= np.arange(n)[None, :] <= np.arange(n)[:, None]
     o, _ = MK.attn_fwd64_masked(q, k, v, 0.7, wrong)
     assert np.abs(o - v).max() > 1e-3  # the window-of-one closed form O = V catches it
+
+
+def test_masked_sampled_rows_equal_the_full_definition():
+    q, k, v = _qkv(89, b=2, h=3, n=50)
+    rng = np.random.default_rng(90)
+    bm = (rng.random((3, 4, 4)) < 0.6).astype(np.uint8)
+    for causal, window in [(True, 7), (False, 12), (True, 0)]:
+        vis = MK.visible_mask(50, causal, window, bm, 16)
+        o, lse = MK.attn_fwd64_masked(q, k, v, 0.5, vis)
+        samples = [(0, 0, 0), (1, 2, 49), (0, 1, 17), (1, 0, 33)]
+        o_r, l_r = MK.attn_fwd64_masked_rows(q, k, v, 0.5, samples, causal, window, bm, 16)
+        for t, (b, h, i) in enumerate(samples):
+            np.testing.assert_allclose(o_r[t], o[b, h, i], atol=1e-15)
+            np.testing.assert_allclose(l_r[t], lse[b, h, i], atol=1e-15)
