@@ -20,7 +20,8 @@ __all__ = [
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
-    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked", "attention_forward", "attention_backward", "attention_decode",
+    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait",
+    "attention_forward", "attention_backward", "attention_decode",
     "attention_forward_fp8", "quantize_fp8", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -34,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
-    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked",
+    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait",
 )
 
 _lib = None
@@ -81,6 +82,7 @@ def load_library():
         lib.fa_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, i, i, vp]
         lib.fa_bwd_masked.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, vp, i, i, vp]
         lib.fa_fwd_fp8.argtypes = [vp] * 8 + [i, i, i, i, f, i, i, vp]
+        lib.fa_selftest_bounded_wait.argtypes = [i, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
         lib.fa_uses_tensor_cores.argtypes = [i, i, i]
@@ -89,7 +91,7 @@ def load_library():
         lib.fa_last_error_message.argtypes = []
         lib.fa_last_error_message.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_quantize_fp8", "fa_fwd_fp8",
-                     "fa_fwd_masked", "fa_bwd_masked",
+                     "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait",
                      "fa_bwd_noalloc", "fa_bwd_preprocess",
                      "fa_bwd_main", "fa_bwd_dq_convert",
                      "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
@@ -298,6 +300,11 @@ def fa_bwd_masked(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, windo
     _check(load_library().fa_bwd_masked(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV),
                                         _p(workspace), nbytes, B, H, Hkv, N, d, float(scale), int(bool(causal)),
                                         int(window), mp, mh, _dt(Q), _stream(stream)))
+
+
+def fa_selftest_bounded_wait(timeout_ms=20, arrive=False, stream=None):
+    """Launch the bounded-wait self-test (see include/fa.h); read the outcome with fa_check_device_error."""
+    _check(load_library().fa_selftest_bounded_wait(int(timeout_ms), int(bool(arrive)), _stream(stream)))
 
 
 def fa_check_device_error(stream=None):

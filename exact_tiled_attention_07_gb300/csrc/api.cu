@@ -491,6 +491,16 @@ fa_status fa_check_device_error(void* stream) {
   return fail(FA_ERR_DEVICE, "device check %u failed (site %u, block %llu)", code, site, block);
 }
 
+fa_status fa_selftest_bounded_wait(int timeout_ms, int arrive, void* stream) {
+  if (timeout_ms < 1 || timeout_ms > 1000)
+    return fail(FA_ERR_INVALID_ARG, "fa_selftest_bounded_wait: timeout_ms must be in [1, 1000], got %d", timeout_ms);
+  DeviceSyms syms;
+  fa_status st = device_syms(&syms);
+  if (st != FA_OK) return st;
+  return launched(launch_bounded_wait_selftest(syms.err, timeout_ms, arrive ? 1 : 0, static_cast<cudaStream_t>(stream)),
+                  "fa_selftest_bounded_wait");
+}
+
 fa_status fa_tile_counter(void* stream, unsigned long long* value, int reset) {
   if (!value) return fail(FA_ERR_INVALID_ARG, "fa_tile_counter: null output");
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -130,6 +130,10 @@ struct Fp8FwdArgs {
 bool fwd_fp8_supported(int d);
 cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a);
 
+// One CTA waits (bounded by timeout_ms) on an mbarrier phase nothing completes, or that it
+// completes itself when arrive != 0.
+cudaError_t launch_bounded_wait_selftest(unsigned long long* err, int timeout_ms, int arrive, cudaStream_t stream);
+
 // Records the calling thread's last error message (read by fa_last_error_message) and
 // returns `status`.
 int set_last_error(int status, const char* fmt, ...);

@@ -112,9 +112,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase of parity `parity` to complete.  Once any role of
-// the CTA has given up (ctx.abort), the others stop waiting too.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const ErrCtx& ctx, uint32_t site) {
+// Bounded wait for the phase of parity `parity` to complete, giving up after limit_ns of
+// global-timer time (recorded as a timeout at `site`).  Once any role of the CTA has given up
+// (ctx.abort), the others stop waiting too.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, const ErrCtx& ctx, uint32_t site,
+                                              uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -122,13 +124,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0) {
       if (*ctx.abort) return false;
-      if (globaltimer() - t0 > FA_WAIT_LIMIT_NS) {
+      if (globaltimer() - t0 > limit_ns) {
         report_error(ctx.err, DERR_TIMEOUT, site);
         *ctx.abort = 1;
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const ErrCtx& ctx, uint32_t site) {
+  return mbar_wait_for(bar, parity, ctx, site, FA_WAIT_LIMIT_NS);
 }
 
 // ---------------------------------------------------------------------------

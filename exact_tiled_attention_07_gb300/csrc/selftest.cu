@@ -1,0 +1,38 @@
+// Self-test of the bounded waits: a CTA waits on an mbarrier phase that nothing completes (or,
+// as the control case, that its own thread completes), with a short limit.  The wait gives
+// up, records a timeout in the device error word and the kernel returns, so the context stays
+// usable; fa_check_device_error then reports FA_ERR_TIMEOUT.  Every kernel of the library
+// waits through the same mbar_wait_for.
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr uint32_t kSelftestSite = 900;
+
+__global__ void bounded_wait_selftest_kernel(unsigned long long* err, uint64_t limit_ns, int arrive) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (arrive && threadIdx.x == 0) mbar_arrive(&bar);
+  const ErrCtx ctx{err, &abort_flag};
+  mbar_wait_for(&bar, 0, ctx, kSelftestSite, limit_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_bounded_wait_selftest(unsigned long long* err, int timeout_ms, int arrive, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(err, (uint64_t)timeout_ms * 1000000ull, arrive);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

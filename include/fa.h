@@ -251,6 +251,16 @@ FA_API fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, cons
 FA_API fa_status fa_check_device_error(void* stream);
 
 /*
+ * Self-test of failure detection without a GPU fault: launches one thread block that waits on
+ * an mbarrier phase, through the same bounded wait every kernel uses, with a limit of
+ * timeout_ms (1..1000). With arrive == 0 nothing completes the phase: the wait gives up after
+ * timeout_ms, records a timeout in the device error word and the kernel returns, so the next
+ * fa_check_device_error returns FA_ERR_TIMEOUT and the context stays usable. With arrive != 0
+ * the block completes the phase itself and nothing is recorded.
+ */
+FA_API fa_status fa_selftest_bounded_wait(int timeout_ms, int arrive, void* stream);
+
+/*
  * Diagnostic: number of (query tile, key tile) pairs the forward kernels processed on the
  * current device since the last reset (128 x 128 tiles on the tensor-core path, 32 x 32 on
  * the CUDA-core path); skipped causal tiles are not counted. Synchronises `stream`;

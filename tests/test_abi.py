@@ -146,3 +146,9 @@ def test_mask_arguments_are_validated(lib):
     # masks run on the tensor-core kernels only: fp32 and odd head dims are unsupported
     assert lib.fa_fwd_masked(g, g, g, g, g, 1, 4, 4, 128, 64, 0.125, 1, 8, None, 0, 2, None) == 2
     assert lib.fa_fwd_masked(g, g, g, g, g, 1, 4, 4, 128, 96, 0.125, 1, 8, None, 0, 0, None) == 2
+
+
+def test_selftest_timeout_range(lib):
+    lib.fa_selftest_bounded_wait.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    assert lib.fa_selftest_bounded_wait(0, 0, None) == 1
+    assert lib.fa_selftest_bounded_wait(5000, 0, None) == 1
