@@ -485,6 +485,48 @@ def run_gpu(args, w: Workload):
             del q8, k8, v8, o8
         binding.fa_check_device_error()
 
+    # the other full-size workloads of the pages (same step, same timing): GPT-2-medium shape
+    # (fp16, d = 64) and the long causal sequence (bf16, d = 64)
+    others = None
+    if not args.no_targets and rank == 0:
+        others = {}
+        for wname in ("gpt2m_fp16", "long_causal_bf16"):
+            ow = WORKLOADS[wname]
+            ox = make_inputs(ow)
+            od = {k_: _dev_tensor(v_, ow.dtype, device)[0] for k_, v_ in ox.items()}
+            del ox
+            oo = torch.empty_like(od["q"])
+            ol = torch.empty((ow.B, ow.H, ow.N), dtype=torch.float32, device=device)
+            odq, odk, odv = torch.empty_like(od["q"]), torch.empty_like(od["k"]), torch.empty_like(od["v"])
+            ows = torch.empty(binding.fa_bwd_workspace_size(ow.B, ow.H, ow.N, ow.d), dtype=torch.uint8,
+                              device=device)
+
+            def ofwd():
+                binding.fa_fwd(od["q"], od["k"], od["v"], oo, ol, ow.scale, ow.causal)
+
+            def obwd():
+                binding.fa_bwd(od["q"], od["k"], od["v"], oo, od["do"], ol, odq, odk, odv, ows, ow.scale, ow.causal)
+
+            entry = {"config": workload_config(ow)}
+            reps = max(3, min(args.steps, 10))
+            for pname, fns in (("fwd", (ofwd,)), ("bwd", (obwd,)), ("fwd+bwd", (ofwd, obwd))):
+                for _ in range(2):
+                    for fn in fns:
+                        fn()
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                for _ in range(reps):
+                    for fn in fns:
+                        fn()
+                b_.record(stream)
+                torch.cuda.synchronize()
+                ms = a_.elapsed_time(b_) / reps
+                tf = attention_flops(ow.B, ow.H, ow.N, ow.d, ow.causal, pname) / (ms * 1e-3) / 1e12
+                entry[pname] = {"ms": ms, "tflops": tf, "pct_of_sustained_peak": 100 * tf / peak_sus}
+            others[wname] = entry
+            del od, oo, ol, odq, odk, odv, ows
+        binding.fa_check_device_error()
+
     decode = None
     if not args.no_decode:
         decode = measure_decode(binding, device, peaks, peak_src)
@@ -501,7 +543,7 @@ def run_gpu(args, w: Workload):
                                 "source": peak_src},
                 "kernels_ms": per_kernel, "gpu_launches": len(names) * args.steps, "roofline": roofline,
                 "e2e": e2e, "clocks": clocks.summary(wall0, wall1), "cpu_baseline": cpu, "targets": targets,
-                "decode": decode}
+                "other_workloads": others, "decode": decode}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -17,10 +17,13 @@
 // the shared-memory read of A that an all-smem MMA pays; dS^T also goes to shared memory
 // as an operand of the dQ GEMM.
 //
-// dQ partials are summed over key tiles in an fp32 accumulator in global memory.  A second
-// warpgroup drains each partial from TMEM into a shared-memory staging tile and one thread
-// adds the tile to global memory with a TMA bulk reduction (whole 128-byte lines, no
-// per-element atomics).  Two shapes of the dQ GEMM keep every TMEM region separate, so no
+// Two warpgroups share the elementwise work: both own the tile's 128 key rows (a warp reads
+// the TMEM lanes of its quarter, so warps w and w + 4 see the same rows) and each takes half of
+// every step's queries for P^T and dS^T.  dQ partials are summed over key tiles in an fp32
+// accumulator in global memory: after its dS^T half, each warpgroup drains its half of the
+// previous step's dQ partial from TMEM into a shared-memory staging tile, and one thread adds
+// the tile to global memory with a TMA bulk reduction (whole 128-byte lines, no per-element
+// atomics).  Two shapes of the dQ GEMM keep every TMEM region separate, so no
 // GEMM waits for another region to be drained:
 //   d = 64:  128 queries per step, dQ = dS K   (M = 128 queries, N = 64)
 //   d = 128:  64 queries per step, dQ^T = K^T dS^T (M = 128 = d, N = 64 queries)
@@ -52,7 +55,7 @@ struct BwdCfg {
   static constexpr int QT_BYTES = BM * D * 2;
   static constexpr int DS_BYTES = BN * BM * 2;
   static constexpr int STG_BYTES = BM * D * 4;
-  static constexpr int THREADS = 320;            // WG0 P/dS, WG1 dQ drain, TMA warp, MMA warp
+  static constexpr int THREADS = 320;            // WG0, WG1 (P/dS, dQ drain), TMA warp, MMA warp
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
   static constexpr int OFF_K = 0;
@@ -64,15 +67,23 @@ struct BwdCfg {
   static constexpr int OFF_STG = OFF_DS + DS_BYTES;              // dQ staging tile
   static constexpr int OFF_VEC = OFF_STG + STG_BYTES;            // [QSTAGES] x (L2[BM], D[BM]) fp32
   static constexpr int OFF_BAR = OFF_VEC + QSTAGES * 2 * BM * 4;
-  static constexpr int NBAR = 16;
+  static constexpr int NBAR = 18;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   // masked variant: the CTA's step list after the barriers (an int count, then uint16 entries
   // (query head of the group << 12 | 128-row query block), rounded up to 8 entries)
   static constexpr int OFF_LIST = SMEM;
   static constexpr int list_bytes(int entries) { return 16 + 2 * ((entries + 7) & ~7); }
   static constexpr int SUB = 128 / BM;  // steps per 128-row query block
-  // TMEM columns: K_j as a 16-bit A operand (d/2 columns), S^T (P^T over its first BM/2),
-  // dP^T (dS^T over its first BM/2), the dQ partial and the dV, dK accumulators
+  // d = 64 (128 queries per step): both warpgroups compute P^T, dS^T (half the queries each)
+  // and drain half of each dQ partial; d = 128 (tensor-bound): warpgroup 0 computes P^T, dS^T
+  // and warpgroup 1 drains whole dQ partials as soon as they complete
+  static constexpr bool SPLIT = !DQT;
+  static constexpr int COMPUTE_THREADS = SPLIT ? 256 : 128;
+  static constexpr int DRAIN_THREADS = SPLIT ? 256 : 128;
+  static constexpr int CH_COLS = SPLIT ? 32 : 16;  // TMEM columns between packed 32-query chunks
+  // TMEM columns: K_j as a 16-bit A operand (d/2 columns), S^T (P^T packed into the first 16
+  // of each 32-query chunk's columns), dP^T (dS^T likewise), the dQ partial and the dV, dK
+  // accumulators
   static constexpr uint32_t COL_K = DQT ? 0 : 448;
   static constexpr uint32_t COL_S = DQT ? 64 : 0;
   static constexpr uint32_t COL_DP = COL_S + BM;
@@ -94,7 +105,17 @@ enum BwdBar {
   B_ACC_FULL = 13,
   B_DRAIN = 14,
   B_KT_READY = 15,  // K_j copied into TMEM
+  B_STG_FREE = 16,  // dQ staging tile free (the previous reduction has read it)
+  B_STG_FULL = 17,  // both warpgroups wrote their half of the staging tile
 };
+
+// TMEM column of the packed 16-bit A operand (P^T or dS^T) for MMA k-step kk (16 queries),
+// chunk c of 32 queries starting at c * ch_cols: contiguous (16) when one warpgroup reads every
+// score before writing any, or at the start of the chunk's own 32 fp32 columns (32) when two
+// warpgroups share the queries, so neither writes over scores the other has yet to read
+__host__ __device__ constexpr uint32_t packed_col(int kk, int ch_cols) {
+  return (uint32_t)((kk >> 1) * ch_cols + (kk & 1) * 8);
+}
 
 // advance a (query tile, query head) step cursor
 __device__ __forceinline__ void step_next(int& ii, int& g, int tiles_per_head) {
@@ -203,10 +224,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     mbar_init(bar + B_S_FULL, 1);
     mbar_init(bar + B_DP_FULL, 1);
-    mbar_init(bar + B_P_READY, 128);
-    mbar_init(bar + B_DS_READY, 128);
+    mbar_init(bar + B_P_READY, C::COMPUTE_THREADS);
+    mbar_init(bar + B_DS_READY, C::COMPUTE_THREADS);
     mbar_init(bar + B_DQ_FULL, 1);
-    mbar_init(bar + B_DQ_FREE, 128);
+    mbar_init(bar + B_DQ_FREE, C::DRAIN_THREADS);
+    mbar_init(bar + B_STG_FREE, 1);
+    mbar_init(bar + B_STG_FULL, C::DRAIN_THREADS);
     mbar_init(bar + B_ACC_FULL, 1);
     mbar_init(bar + B_DRAIN, 1);
     mbar_init(bar + B_KT_READY, 128);
@@ -336,7 +359,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
-              umma_ts(tbase + C::COL_DV, tbase + C::COL_S + kk * 8, bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
+              umma_ts(tbase + C::COL_DV, tbase + C::COL_S + packed_col(kk, C::CH_COLS), bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
           }
           __syncwarp();
         }
@@ -357,7 +380,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
-              umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + kk * 8, bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
+              umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + packed_col(kk, C::CH_COLS), bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
           }
           __syncwarp();
         }
@@ -396,8 +419,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_wait(bar + B_DRAIN, 0, nctx, 125);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------ WG0: P^T, dS^T, epilogue
+  } else if (!C::SPLIT && warp < 4) {
+    // ---------------------------------------------------------------- WG0: P^T, dS^T, epilogue
     const uint32_t lane_base = warp * 32;
     const int rit = warp * 32 + lane;  // key row within the tile
     const int key = k0 + rit;
@@ -560,19 +583,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         store_row16<D>(dv_out, (int64_t)kvh * n + key, pk, c);
       }
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------------ WG1: drain dQ partials
+
+  } else if (!C::SPLIT && warp < 8) {
     // TMEM lane = d index (DQT) or query row; the partial goes to a staging tile in the layout
     // of the dQ accumulator's tensor map and one thread adds it to global memory (TMA reduce).
     const uint32_t lane_base = (warp & 3) * 32;
     const int rr = (warp & 3) * 32 + lane;
     const bool leader = (warp == 4 && lane == 0);
     bool ok = start_ok;
-    for (int i = 0, ii = 0, g = 0; ok && i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
+    // Every warp runs every step and passes both named barriers in each; once a bounded wait
+    // has run out (the abort flag then ends every later wait at once) the warp still passes
+    // them, staging stale TMEM columns that are never reduced, so none is left waiting.
+    for (int i = 0, ii = 0, g = 0; i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
       int gm, q0;
       step_rows(i, ii, g, &gm, &q0);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, i & 1, ctx, 140));
-      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, i & 1, ctx, 140)) && ok;
       tc_fence_after();
       uint32_t vr[2][32];
 #pragma unroll
@@ -602,7 +627,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
-      if (leader) {
+      if (leader && ok) {
         const int qh = kvh * group + gm;
         if constexpr (C::DQT) {
           tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
@@ -614,8 +639,250 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
     }
     if (leader) bulk_wait_group<0>();  // every reduction issued here has completed
-  }
 
+  } else if (warp < 8) {
+    if constexpr (C::SPLIT) {
+      // ---------------------------------------------------------------- WG0, WG1: P^T, dS^T, dQ drain
+      // (d = 64, 128 queries per step) Both warpgroups own the same 128 key rows (TMEM lane
+      // quarter warp % 4) and each takes half of every step's 32-query chunks for P^T and dS^T;
+      // after its dS^T half of step i each drains its half of the dQ partial of step i - 1 (that
+      // MMA completed before dP^T_i, which the dS^T half has just read).  WG0 also copies K_j
+      // into TMEM at the start and writes dK, dV at the end.
+      constexpr bool SPLIT = C::SPLIT;
+      const int wg = warp >> 2;
+      const uint32_t lane_base = (warp & 3) * 32;
+      const int rit = (warp & 3) * 32 + lane;  // key row within the tile (and TMEM lane)
+      const int key = k0 + rit;
+      const bool key_ok = key < n;
+      uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
+      const uint32_t sw = (uint32_t)(rit & 7);
+      constexpr int NCH = SPLIT ? BM / 64 : BM / 32;  // 32-query chunks a computing warpgroup takes
+      const int c0 = SPLIT ? wg * NCH : 0;
+      constexpr int DCOLS = SPLIT ? 32 : 64;  // TMEM columns of a dQ partial one thread drains
+      const int dcol0 = SPLIT ? wg * 32 : 0;
+      const bool leader = (warp == (SPLIT ? 0 : 4) && lane == 0);  // issues the dQ reductions
+      uint8_t* stg = smem + C::OFF_STG;
+      bool ok = start_ok;
+      if (wg == 0) {
+        // K_j row -> TMEM (A operand of S^T = K Q^T): 16-byte chunks of the swizzled smem tile
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_KV, 0, ctx, 134));
+        if (ok) {
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb) {
+            const uint8_t* krow = smem + C::OFF_K + kb * (BN * 128) + rit * 128;
+            uint32_t w[32];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 x = *reinterpret_cast<const uint4*>(krow + (((uint32_t)ch ^ sw) << 4));
+              w[4 * ch] = x.x;
+              w[4 * ch + 1] = x.y;
+              w[4 * ch + 2] = x.z;
+              w[4 * ch + 3] = x.w;
+            }
+            tmem_st32(tmem_addr(tbase, lane_base, C::COL_K + kb * 32), w);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar + B_KT_READY);
+        }
+      }
+      // dQ partial k -> staging tile (this warpgroup's half) -> one TMA reduce-add into the fp32
+      // accumulator.  The staging handshake uses mbarriers (bounded waits), not named barriers,
+      // so a warp that gave up cannot leave the others waiting.
+      auto drain = [&](int k, int q0, int qh) {
+        bool good = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, k & 1, ctx, 140));
+        if (!good) return false;
+        tc_fence_after();
+        uint32_t vr[DCOLS / 32][32];  // this thread's TMEM columns of the partial
+#pragma unroll
+        for (int c = 0; c < DCOLS / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + dcol0 + c * 32), vr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < DCOLS / 32; ++c) reg_fence(vr[c]);
+        const uint32_t* v = &vr[0][0];
+        tc_fence_before();
+        mbar_arrive(bar + B_DQ_FREE);
+        if (leader) {
+          bulk_wait_group_read<0>();  // the previous reduction has finished reading the tile
+          mbar_arrive(bar + B_STG_FREE);
+        }
+        good = __all_sync(0xffffffffu, mbar_wait(bar + B_STG_FREE, k & 1, ctx, 141));
+        if (!good) return false;
+        if constexpr (C::DQT) {
+          // [BM queries][D] fp32 row-major; TMEM lane = d (rit), columns = this thread's queries
+          float* st = reinterpret_cast<float*>(stg) + rit;
+#pragma unroll
+          for (int qq = 0; qq < DCOLS; ++qq) st[(dcol0 + qq) * D] = __uint_as_float(v[qq]);
+        } else {
+          // [128 queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns; TMEM lane =
+          // query row (rit), columns = this thread's d (one box per 32)
+#pragma unroll
+          for (int j = 0; j < DCOLS / 4; ++j) {
+            uint8_t* bx = stg + (dcol0 / 32 + j / 8) * (BM * 128) + rit * 128;
+            *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ sw) << 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar + B_STG_FULL);
+        if (leader) {
+          if (!mbar_wait(bar + B_STG_FULL, k & 1, ctx, 142)) return false;
+          if constexpr (C::DQT) {
+            tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
+          } else {
+            tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
+            tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, qh);
+          }
+          bulk_commit_group();
+        }
+        return true;
+      };
+      int prev_q0 = 0, prev_qh = 0;
+      for (int i = 0, ii = 0, g = 0; ok && i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
+        const int s = i % C::QSTAGES;
+        int gm, q0;
+        step_rows(i, ii, g, &gm, &q0);
+
+        const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
+        const float* dvec = l2v + BM;
+        // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
+        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (i / C::QSTAGES) & 1, ctx, 133));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, i & 1, ctx, 130));
+        if (!ok) break;
+        tc_fence_after();
+        // visible queries q0 + qc: qc in [mask_below, mask_above) (causal: not before this key;
+        // window: |query - key| < window, an upper bound on the query with or without causal)
+        int mask_below = causal ? key - q0 : INT32_MIN, mask_above = INT32_MAX;
+        if constexpr (MASKED) {
+          if (window > 0) {
+            mask_below = max(mask_below, key - window + 1 - q0);
+            mask_above = key + window - q0;
+          }
+        }
+        // P^T of this key against this half's queries, kept as packed 16-bit pairs: the same
+        // rounded values feed dV += P^T dO and dS = P o (dP - D)
+        uint32_t pk[NCH * 16];
+        {
+          uint32_t sr[NCH][32];
+#pragma unroll
+          for (int cl = 0; cl < NCH; ++cl) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + (c0 + cl) * 32), sr[cl]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int cl = 0; cl < NCH; ++cl) {
+            const int c = c0 + cl;
+            uint32_t(&r)[32] = sr[cl];
+            reg_fence(r);
+#pragma unroll
+            for (int t = 0; t < 32; t += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(l2v + c * 32 + t);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              float e[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int qc = c * 32 + t + u;
+                const float x = ex2(fmaf(__uint_as_float(r[t + u]), scale_log2, -lv[u]));
+                e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? x : 0.f;
+              }
+              pk[cl * 16 + t / 2] = pack2<BF16>(e[0], e[1]);
+              pk[cl * 16 + t / 2 + 1] = pack2<BF16>(e[2], e[3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int cl = 0; cl < NCH; ++cl) {
+          uint32_t w[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) w[t] = pk[cl * 16 + t];
+          tmem_st16(tmem_addr(tbase, lane_base, C::COL_S + (c0 + cl) * C::CH_COLS), w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar + B_P_READY);
+        // dS^T = P^T o (dP^T - D); dp_full(i) also means the MMAs of step i-1 that read dS^T are done
+        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DP_FULL, i & 1, ctx, 131));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint32_t dr[NCH][32];
+#pragma unroll
+          for (int cl = 0; cl < NCH; ++cl) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + (c0 + cl) * 32), dr[cl]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int cl = 0; cl < NCH; ++cl) {
+            const int c = c0 + cl;
+            uint32_t(&r)[32] = dr[cl];
+            reg_fence(r);
+            uint32_t dsk[16];
+#pragma unroll
+            for (int t = 0; t < 16; t += 2) {
+              const float4 d4 = *reinterpret_cast<const float4*>(dvec + c * 32 + 2 * t);
+              const float2 p01 = unpack2<BF16>(pk[cl * 16 + t]);
+              const float2 p23 = unpack2<BF16>(pk[cl * 16 + t + 1]);
+              dsk[t] = pack2<BF16>(p01.x * (__uint_as_float(r[2 * t]) - d4.x),
+                                   p01.y * (__uint_as_float(r[2 * t + 1]) - d4.y));
+              dsk[t + 1] = pack2<BF16>(p23.x * (__uint_as_float(r[2 * t + 2]) - d4.z),
+                                       p23.y * (__uint_as_float(r[2 * t + 3]) - d4.w));
+            }
+            // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
+            uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
+              *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
+                  make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
+            }
+            // and packed into TMEM over this chunk's dP^T columns, already read (A operand of
+            // dK += dS^T Q)
+            tmem_st16(tmem_addr(tbase, lane_base, C::COL_DP + c * C::CH_COLS), dsk);
+          }
+        }
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar + B_DS_READY);
+        if constexpr (SPLIT) {
+          if (i > 0 && !(ok = drain(i - 1, prev_q0, prev_qh))) break;
+        }
+        prev_q0 = q0;
+        prev_qh = kvh * group + gm;
+      }
+      if (SPLIT && ok && nsteps > 0) ok = drain(nsteps - 1, prev_q0, prev_qh);
+      if (leader) bulk_wait_group<0>();  // every reduction issued here has completed
+      // epilogue (WG0): dV, dK (x tau) from TMEM to global
+      if (wg == 0 && ok && nsteps > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, 0, ctx, 132));
+        if (ok) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t col = which ? C::COL_DK : C::COL_DV;
+            const float f = which ? scale : 1.f;
+            void* dst = which ? dk_out : dv_out;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tmem_addr(tbase, lane_base, col + c * 32), r);
+              tmem_wait_ld();
+              reg_fence(r);
+              uint32_t pk[16];
+#pragma unroll
+              for (int t = 0; t < 16; ++t)
+                pk[t] = pack2<BF16>(__uint_as_float(r[2 * t]) * f, __uint_as_float(r[2 * t + 1]) * f);
+              if (key_ok) store_row16<D>(dst, (int64_t)kvh * n + key, pk, c);
+            }
+          }
+        }
+      } else if (wg == 0 && ok && nsteps == 0 && key_ok) {
+        // no query meets this key tile: zero gradients (not reachable for square causal masks)
+        uint32_t pk[16] = {};
+        for (int c = 0; c < D / 32; ++c) {
+          store_row16<D>(dk_out, (int64_t)kvh * n + key, pk, c);
+          store_row16<D>(dv_out, (int64_t)kvh * n + key, pk, c);
+        }
+      }
+
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == C::MMA_WARP) {
