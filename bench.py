@@ -210,7 +210,18 @@ def run_reference(args, w: Workload):
 def workload_config(w: Workload):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype, "causal": w.causal,
             "passes": "fwd" if w.fwd_only else "fwd+bwd",
-            "l2": "inputs larger than L2 (no flush)" if w.B * w.H * w.N * w.d * 2 > 129e6 else "L2 flushed"}
+            "l2": l2_note(w)}
+
+
+def l2_note(w: Workload) -> str:
+    """What keeps L2 from serving a step's inputs from the previous step (no flush is done)."""
+    e = 4 if w.dtype == "fp32" else 2
+    ins = (w.B * w.H * w.N * w.d + 2 * w.B * w.kv_heads * w.N * w.d) * e  # Q, K, V
+    if not w.fwd_only:
+        ins += w.B * w.H * w.N * w.d * e  # dO
+    if ins > 129e6:
+        return f"inputs of {ins / 1e6:.0f} MB per step, larger than the 129 MB L2 (no flush)"
+    return f"inputs of {ins / 1e6:.1f} MB per step fit in L2 (no flush)"
 
 
 # ---------------------------------------------------------------------------
