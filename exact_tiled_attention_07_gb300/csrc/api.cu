@@ -118,6 +118,17 @@ fa_status carve(BwdArgs* a, void* ws, size_t ws_bytes, int B, int H, int N, int 
 
 }  // namespace
 
+int device_sm_count() {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kSmCount;
+  if (cached[dev] == 0) {
+    int v = 0;
+    cached[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : kSmCount;
+  }
+  return cached[dev];
+}
+
 int set_last_error(int status, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);

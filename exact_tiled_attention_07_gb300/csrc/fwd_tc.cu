@@ -26,10 +26,19 @@
 //
 // Causal: key tiles wholly in the future of a query tile are never loaded or multiplied
 // (§5.3 closing paragraph); only diagonal tiles are masked element-wise.
+//
+// Persistent: a CTA (one per SM) walks work items (head, NQ query tiles), round by round
+// across the grid: in grid order, or for causal launches whose items a host-side estimate
+// balances better that way, backwards in odd rounds (heavy and light items pair up).  The K/V ring, S/P and O barriers keep their phases across items; q_empty (all of
+// an item's S = Q K^T issued and done) lets the next item's Q load while the item finishes,
+// and o_empty (the softmax has read O) lets the next item's first P V overwrite O, so one
+// item's epilogue overlaps the next item's loads and first S tiles.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <vector>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -61,7 +70,7 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = NQ * Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + STAGES * TILE_BYTES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2;
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 3;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   // masked variant: the CTA's key-tile list after the barriers (4 ints, then uint16 tile
   // indices and uint8 visibility flags, nb rounded up to 16 entries each)
@@ -78,6 +87,8 @@ struct FwdSmemBars {
   uint64_t* o_full;   // [2]
   uint64_t* pv_done;  // [1] (NQ = 1)
   uint64_t* drain;    // [1]
+  uint64_t* o_empty;  // [2] the softmax has read O_q of its last item
+  uint64_t* q_empty;  // [1] every S = Q K^T of the last item is done (Q may be overwritten)
 };
 
 // Masked variant (block mask and/or window, "Lecture 8" §5.7 block-sparse attention): one warp
@@ -92,7 +103,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, float* __restrict__ lse, int n,
                   int bh_count, int tiles_per_head, float scale_log2, int causal, int group, unsigned long long* err,
                   unsigned long long* counter, int window, const uint8_t* __restrict__ block_mask, int mask_heads,
-                  int heads) {
+                  int heads, int snake) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -108,41 +119,53 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   B.o_full = B.p_full + 2;
   B.pv_done = B.o_full + 2;
   B.drain = B.pv_done + 1;
+  B.o_empty = B.drain + 1;
+  B.q_empty = B.o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const ErrCtx ctx{err, abort_flag};
 
-  // work item: head-major (CTAs running together share K/V in L2); causal: heaviest (last)
+  // work items: head-major (CTAs running together share K/V in L2); causal: heaviest (last)
   // query tiles first within groups of heads
-  int head, tile;
-  if (causal) {
-    int rank;
-    grouped_work_item(blockIdx.x, bh_count, tiles_per_head, &head, &rank);
-    tile = tiles_per_head - 1 - rank;
-  } else {
-    head = blockIdx.x / tiles_per_head;
-    tile = blockIdx.x - head * tiles_per_head;
-  }
-  const int kvhead = head / group;  // grouped-query attention: key/value head shared by `group` query heads
-  const int qrow0 = tile * (C::NQ * BM);
+  const int total_items = bh_count * tiles_per_head;
   const int nblocks = (n + BN - 1) / BN;
-  int nq[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int first = qrow0 + q * BM;
-    if (q >= C::NQ || first >= n) {
-      nq[q] = 0;
-    } else if (causal) {
-      nq[q] = min(nblocks, (min(first + BM, n) - 1) / BN + 1);
+  struct Item {
+    int head, kvhead, qrow0;
+    int nq[2];  // key tiles of each query tile
+  };
+  auto item_of = [&](int item) {
+    Item w;
+    int tile;
+    if (causal) {
+      int rank;
+      grouped_work_item(item, bh_count, tiles_per_head, &w.head, &rank);
+      tile = tiles_per_head - 1 - rank;
     } else {
-      nq[q] = nblocks;
+      w.head = item / tiles_per_head;
+      tile = item - w.head * tiles_per_head;
     }
-  }
+    w.kvhead = w.head / group;  // grouped-query attention: key/value head shared by `group` query heads
+    w.qrow0 = tile * (C::NQ * BM);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int first = w.qrow0 + q * BM;
+      if (q >= C::NQ || first >= n) {
+        w.nq[q] = 0;
+      } else if (causal) {
+        w.nq[q] = min(nblocks, (min(first + BM, n) - 1) / BN + 1);
+      } else {
+        w.nq[q] = nblocks;
+      }
+    }
+    return w;
+  };
   int* list_hdr = reinterpret_cast<int*>(smem + C::OFF_LIST);  // nq[0], nq[1], visible tiles of q 0, 1
   uint16_t* jlist = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST + 16);
   uint8_t* jflag = reinterpret_cast<uint8_t*>(jlist + ((nblocks + 15) & ~15));
   if constexpr (MASKED) {
     if (warp == C::PRODUCER_WARP) {
+      // (masked launches give every CTA one item, blockIdx.x)
+      const int head = item_of(blockIdx.x).head, qrow0 = item_of(blockIdx.x).qrow0;
       // visible key tiles of query tile q: block-mask byte set, and some (row, key) pair of the
       // two tiles inside the causal and window bounds
       int qr0[2], qr1[2];
@@ -208,6 +231,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
     mbar_init(B.pv_done, 1);
     mbar_init(B.drain, 1);
+    mbar_init(B.o_empty + 0, 128);
+    mbar_init(B.o_empty + 1, 128);
+    mbar_init(B.q_empty, 1);
     fence_barrier_init();
   }
   if (warp == C::MMA_WARP) {
@@ -219,12 +245,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const bool start_ok = (*abort_flag == 0);
-  if constexpr (MASKED) {
-    nq[0] = list_hdr[0];
-    nq[1] = list_hdr[1];
-  }
-  const int nmax = max(nq[0], nq[1]);
-  // key tile at position t of the CTA's sequence
+  // this CTA's r-th item: rounds of gridDim.x items, in grid order, or (snake) backwards in odd
+  // rounds so that a CTA's heavy and light causal items pair up; -1 when done.  The grid size and
+  // CTA index are read afresh each time (volatile reads cannot be hoisted): kept live across the
+  // softmax loop they cost the d = 128 kernel spills.
+  auto nth_item = [&](int r) {
+    const int g = (int)grid_dim_x(), c = (int)cta_id_x();
+    const int64_t item = (int64_t)r * g + ((snake && (r & 1)) ? (g - 1 - c) : c);
+    return item < total_items ? (int)item : -1;
+  };
+  // the item with, for masked launches, the key-tile counts of its list
+  auto item_at = [&](int item) {
+    Item w = item_of(item);
+    if constexpr (MASKED) {
+      w.nq[0] = list_hdr[0];
+      w.nq[1] = list_hdr[1];
+    }
+    return w;
+  };
+  // key tile at position t of an item's sequence
   auto tile_at = [&](int t) { return MASKED ? (int)jlist[t] : t; };
 
   if (warp == C::PRODUCER_WARP) {
@@ -233,29 +272,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(B.q_full, C::NQ * C::Q_BYTES);
-      for (int q = 0; q < C::NQ; ++q)
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(smem + C::OFF_Q + q * C::Q_BYTES + kb * (BM * 128), &tm_q, B.q_full, kb * 64,
-                      qrow0 + q * BM, head);
-      int issued = 0;
-      for (int idx = 0; idx < 2 * nmax; ++idx) {
-        const int slot = idx % C::STAGES, use = idx / C::STAGES;
-        if (use > 0 && !mbar_wait(B.kv_empty + slot, (use - 1) & 1, ctx, 10)) break;
-        mbar_arrive_expect_tx(B.kv_full + slot, C::TILE_BYTES);
-        uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
-        const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, kb * 64, tile_at(idx >> 1) * BN, kvhead);
-        issued = idx + 1;
+      uint32_t ring_pos = 0;  // ring loads issued so far (all items)
+      int q_loads = 0;
+      bool ok = true;
+      for (int r = 0, item = nth_item(0); ok && item >= 0; item = nth_item(++r)) {
+        const Item w = item_at(item);
+        const int nmax = max(w.nq[0], w.nq[1]);
+        // Q of this item once the previous item's S = Q K^T are done
+        if (q_loads > 0 && !(ok = mbar_wait(B.q_empty, (q_loads - 1) & 1, ctx, 13))) break;
+        mbar_arrive_expect_tx(B.q_full, C::NQ * C::Q_BYTES);
+        for (int q = 0; q < C::NQ; ++q)
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(smem + C::OFF_Q + q * C::Q_BYTES + kb * (BM * 128), &tm_q, B.q_full, kb * 64,
+                        w.qrow0 + q * BM, w.head);
+        ++q_loads;
+        for (int idx = 0; idx < 2 * nmax; ++idx) {
+          const uint32_t g = ring_pos;
+          const int slot = g % C::STAGES, use = g / C::STAGES;
+          if (use > 0 && !(ok = mbar_wait(B.kv_empty + slot, (use - 1) & 1, ctx, 10))) break;
+          mbar_arrive_expect_tx(B.kv_full + slot, C::TILE_BYTES);
+          uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
+          const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, kb * 64, tile_at(idx >> 1) * BN, w.kvhead);
+          ++ring_pos;
+        }
       }
       // drain: every copy this thread started must land before the CTA may exit
       ErrCtx nctx = ctx;
       int no_abort = 0;
       nctx.abort = &no_abort;
-      mbar_wait(B.q_full, 0, nctx, 11);
-      for (int idx = issued - 1; idx >= 0 && idx >= issued - C::STAGES; --idx)
-        mbar_wait(B.kv_full + idx % C::STAGES, (idx / C::STAGES) & 1, nctx, 12);
+      if (q_loads > 0) mbar_wait(B.q_full, (q_loads - 1) & 1, nctx, 11);
+      for (int g = (int)ring_pos - 1; g >= 0 && g >= (int)ring_pos - C::STAGES; --g)
+        mbar_wait(B.kv_full + g % C::STAGES, (g / C::STAGES) & 1, nctx, 12);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
@@ -268,11 +317,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const uint32_t idesc_pv = make_idesc_f16(BM, D, BF16, false, true);
       const uint32_t q_base = smem_u32(smem + C::OFF_Q);
       const uint32_t ring = smem_u32(smem + C::OFF_RING);
-      auto slot_of = [&](int idx) { return idx % C::STAGES; };
+      uint32_t ring_pos = 0;    // ring entry of the item's first K tile (all items so far)
+      int tq[2] = {0, 0};       // key tiles processed by each query tile (all items): P phases
+      int oq[2] = {0, 0};       // items with a result for each query tile: O phases
+      int items = 0;
+      auto slot_of = [&](int idx) { return (int)((ring_pos + idx) % C::STAGES); };
       auto wait = [&](uint64_t* b, uint32_t parity, uint32_t site) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, ctx, site));
       };
-      auto wait_full = [&](int idx) { return wait(B.kv_full + slot_of(idx), (idx / C::STAGES) & 1, 20); };
+      auto wait_full = [&](int idx) {
+        return wait(B.kv_full + slot_of(idx), ((ring_pos + idx) / C::STAGES) & 1, 20);
+      };
       auto commit = [&](uint64_t* b) {
         if (leader) umma_commit(b);
         __syncwarp();
@@ -307,73 +362,91 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
         __syncwarp();
       };
-      bool ok = wait(B.q_full, 0, 21);
-      if (ok) tc_fence_after();
-      if constexpr (C::NQ == 2) {
-        if (ok && nmax > 0) {
-          ok = wait_full(0);
-          if (ok) {
+      // the first P V of query tile q in an item overwrites O_q: the softmax must have read it
+      auto o_free = [&](int q) { return oq[q] == 0 || wait(B.o_empty + q, (oq[q] - 1) & 1, 26 + q); };
+      bool ok = true;
+      for (int r = 0, item = nth_item(0); ok && item >= 0; item = nth_item(++r)) {
+        const Item w = item_at(item);
+        const int* nq = w.nq;
+        const int nmax = max(nq[0], nq[1]);
+        if (!(ok = wait(B.q_full, items & 1, 21))) break;
+        tc_fence_after();
+        if constexpr (C::NQ == 2) {
+          if (nmax > 0) {
+            if (!(ok = wait_full(0))) break;
             tc_fence_after();
             if (nq[0] > 0) { issue_qk(0, 0, C::S_COL0); commit(B.s_full + 0); }
             if (nq[1] > 0) { issue_qk(1, 0, C::S_COL1); commit(B.s_full + 1); }
             commit(B.kv_empty + slot_of(0));
           }
-        }
-        for (int j = 0; ok && j < nmax; ++j) {
-          const int vidx = 2 * j + 1, kidx = 2 * j + 2;
-          if (!(ok = wait_full(vidx))) break;
-          if (j < nq[0]) {
-            if (!(ok = wait(B.p_full + 0, j & 1, 22))) break;
-            tc_fence_after();
-            issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
+          if (nmax <= 1) commit(B.q_empty);  // every S of the item is issued
+          for (int j = 0; ok && j < nmax; ++j) {
+            const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+            if (!(ok = wait_full(vidx))) break;
+            if (j < nq[0]) {
+              if (!(ok = wait(B.p_full + 0, (tq[0] + j) & 1, 22))) break;
+              if (j == 0 && !(ok = o_free(0))) break;
+              tc_fence_after();
+              issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
+            }
+            if (j + 1 < nmax) {
+              if (!(ok = wait_full(kidx))) break;
+              tc_fence_after();
+            }
+            if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); commit(B.s_full + 0); }
+            if (j < nq[1]) {
+              if (!(ok = wait(B.p_full + 1, (tq[1] + j) & 1, 23))) break;
+              if (j == 0 && !(ok = o_free(1))) break;
+              tc_fence_after();
+              issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
+            }
+            commit(B.kv_empty + slot_of(vidx));
+            if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); commit(B.s_full + 1); }
+            if (j + 1 < nmax) commit(B.kv_empty + slot_of(kidx));
+            if (j == nmax - 2) commit(B.q_empty);  // the item's last S are issued
+            if (j == nq[0] - 1) commit(B.o_full + 0);
+            if (j == nq[1] - 1) commit(B.o_full + 1);
           }
-          if (j + 1 < nmax) {
-            if (!(ok = wait_full(kidx))) break;
-            tc_fence_after();
-          }
-          if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); commit(B.s_full + 0); }
-          if (j < nq[1]) {
-            if (!(ok = wait(B.p_full + 1, j & 1, 23))) break;
-            tc_fence_after();
-            issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
-          }
-          commit(B.kv_empty + slot_of(vidx));
-          if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); commit(B.s_full + 1); }
-          if (j + 1 < nmax) commit(B.kv_empty + slot_of(kidx));
-          if (j == nq[0] - 1) commit(B.o_full + 0);
-          if (j == nq[1] - 1) commit(B.o_full + 1);
-        }
-      } else {
-        // NQ == 1: S double-buffered in columns 0 / 128, O at 256
-        const int nb = nq[0];
-        if (ok && nb > 0) {
+        } else {
+          // NQ == 1: S double-buffered in columns 0 / 128 (by the global tile count), O at 256
+          const int nb = nq[0];
+          auto buf = [&](int j) { return ((tq[0] + j) & 1) ? C::S_COL1 : C::S_COL0; };
           for (int j = 0; ok && j < 2 && j < nb; ++j) {
             if (!(ok = wait_full(2 * j))) break;
             tc_fence_after();
-            issue_qk(0, 2 * j, j ? C::S_COL1 : C::S_COL0);
-            commit(B.s_full + j);
+            issue_qk(0, 2 * j, buf(j));
+            commit(B.s_full + ((tq[0] + j) & 1));
             commit(B.kv_empty + slot_of(2 * j));
           }
-        }
-        for (int j = 0; ok && j < nb; ++j) {
-          const int vidx = 2 * j + 1;
-          const uint32_t buf = (j & 1) ? C::S_COL1 : C::S_COL0;
-          if (!(ok = wait_full(vidx))) break;
-          if (!(ok = wait(B.p_full + (j & 1), (j >> 1) & 1, 24))) break;
-          tc_fence_after();
-          issue_pv(C::O_COL0, buf, vidx, j > 0);
-          commit(B.pv_done);
-          commit(B.kv_empty + slot_of(vidx));
-          if (j + 2 < nb) {
-            const int kidx = 2 * (j + 2);
-            if (!(ok = wait_full(kidx))) break;
+          if (ok && nb <= 2) commit(B.q_empty);
+          for (int j = 0; ok && j < nb; ++j) {
+            const int vidx = 2 * j + 1;
+            const int t = tq[0] + j;
+            if (!(ok = wait_full(vidx))) break;
+            if (!(ok = wait(B.p_full + (t & 1), (t >> 1) & 1, 24))) break;
+            if (j == 0 && !(ok = o_free(0))) break;
             tc_fence_after();
-            issue_qk(0, kidx, buf);
-            commit(B.s_full + (j & 1));
-            commit(B.kv_empty + slot_of(kidx));
+            issue_pv(C::O_COL0, buf(j), vidx, j > 0);
+            commit(B.pv_done);
+            commit(B.kv_empty + slot_of(vidx));
+            if (j + 2 < nb) {
+              const int kidx = 2 * (j + 2);
+              if (!(ok = wait_full(kidx))) break;
+              tc_fence_after();
+              issue_qk(0, kidx, buf(j));  // in order after P_j V_j, which reads this buffer
+              commit(B.s_full + (t & 1));
+              commit(B.kv_empty + slot_of(kidx));
+              if (j + 2 == nb - 1) commit(B.q_empty);
+            }
+            if (j == nb - 1) commit(B.o_full + 0);
           }
-          if (j == nb - 1) commit(B.o_full + 0);
         }
+        ring_pos += 2 * nmax;
+        for (int q = 0; q < 2; ++q) {
+          tq[q] += nq[q];
+          oq[q] += nq[q] > 0 ? 1 : 0;
+        }
+        ++items;
       }
       // drain: all MMAs complete before TMEM is released
       ErrCtx nctx = ctx;
@@ -389,145 +462,157 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_base = quarter * 32;
     const int rit = quarter * 32 + lane;
-    const int row = qrow0 + q * BM + rit;
-    const int nb = nq[q];
     const uint32_t o_col = q ? C::O_COL1 : C::O_COL0;
-    float m = -INFINITY;  // reference maximum, log2 units (scores * tau * log2 e)
-    float l = 0.f;
+    int tq = 0;  // key tiles this query tile processed (all items): S / P phases
+    int oq = 0;  // items with a result: O phases
     bool ok = start_ok;
-    for (int j = 0; ok && j < nb; ++j) {
-      uint32_t s_col;
-      uint64_t* sbar;
-      uint32_t sparity;
-      if constexpr (C::NQ == 2) {
-        s_col = q ? C::S_COL1 : C::S_COL0;
-        sbar = B.s_full + q;
-        sparity = j & 1;
-      } else {
-        s_col = (j & 1) ? C::S_COL1 : C::S_COL0;
-        sbar = B.s_full + (j & 1);
-        sparity = (j >> 1) & 1;
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(sbar, sparity, ctx, 30 + q));
-      if (!ok) break;
-      tc_fence_after();
-      // whole S row: all TMEM loads in flight before one wait
-      uint32_t sr[BN / 32][32];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, s_col + c * 32), sr[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
-      float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
-      // visible columns [lo, hi) of this row: keys before N, (causal) not after the row,
-      // (window) within the window; none when the tile is listed only for the other query tile
-      const int jt = tile_at(j);
-      int lo = 0, hi = n - jt * BN;
-      if (causal) hi = min(hi, row - jt * BN + 1);
-      if constexpr (MASKED) {
-        if (window > 0) {
-          lo = row - window + 1 - jt * BN;
-          if (!causal) hi = min(hi, row + window - jt * BN);
+    for (int r = 0, item = nth_item(0); ok && item >= 0; item = nth_item(++r)) {
+      const Item w = item_at(item);
+      const int head = w.head;
+      const int row = w.qrow0 + q * BM + rit;
+      const int nb = w.nq[q];
+      float m = -INFINITY;  // reference maximum, log2 units (scores * tau * log2 e)
+      float l = 0.f;
+      for (int j = 0; ok && j < nb; ++j) {
+        const int t = tq + j;
+        uint32_t s_col;
+        uint64_t* sbar;
+        uint32_t sparity;
+        if constexpr (C::NQ == 2) {
+          s_col = q ? C::S_COL1 : C::S_COL0;
+          sbar = B.s_full + q;
+          sparity = t & 1;
+        } else {
+          s_col = (t & 1) ? C::S_COL1 : C::S_COL0;
+          sbar = B.s_full + (t & 1);
+          sparity = (t >> 1) & 1;
         }
-        if (!((jflag[j] >> q) & 1)) hi = lo = 0;
-      }
-      if (lo > 0 || hi < BN) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c < lo || c >= hi) s[c] = -INFINITY;
-      }
-      const float mx = row_max(s);
-      const float m_blk = mx * scale_log2;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (m == -INFINITY) {
-        m = m_blk;  // first visible block of this row: O is written fresh (or is still zero)
-        alpha = 0.f;
-      } else if (m_blk > m + kRescaleThreshold) {
-        alpha = ex2(m - m_blk);
-        m = m_blk;
-        rescale = true;
-      }
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
-#pragma unroll
-      for (int h = 0; h < BN / 64; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(s[h * 64 + 2 * i], scale_log2, neg_m));
-          const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], scale_log2, neg_m));
-          part[i & 3] += p0 + p1;
-          pk[i] = pack2<BF16>(p0, p1);
-        }
-        tmem_st32(tmem_addr(tbase, lane_base, s_col + h * 32), pk);
-      }
-      const float sum = (part[0] + part[1]) + (part[2] + part[3]);
-      l = l * alpha + sum;
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O row *= alpha; O is stable: the PV of block j-1 completed before S_j
-        // (NQ = 2: same issuing thread, in order) or pv_done says so (NQ = 1).
-        if constexpr (C::NQ == 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done, (j - 1) & 1, ctx, 34));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const float a = rescale ? alpha : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          const uint32_t ta = tmem_addr(tbase, lane_base, o_col + c * 32);
-          tmem_ld32(ta, r);
-          tmem_wait_ld();
-          reg_fence(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-          tmem_st32(ta, r);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      // NQ = 1: one barrier per S buffer; with a single one the softmax could finish blocks j
-      // and j + 1 while the MMA warp still waits for V_j, and its parity wait on phase j would
-      // then see phase j + 1
-      mbar_arrive(B.p_full + (C::NQ == 2 ? q : (j & 1)));
-    }
-    // epilogue: O / l -> global (16-bit), L = (m + log2 l) ln 2
-    if (ok && nb > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(B.o_full + q, 0, ctx, 40 + q));
-      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(sbar, sparity, ctx, 30 + q));
+        if (!ok) break;
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint8_t* orow = reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2;
+        // whole S row: all TMEM loads in flight before one wait
+        uint32_t sr[BN / 32][32];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, s_col + c * 32), sr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
+        float s[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+        // visible columns [lo, hi) of this row: keys before N, (causal) not after the row,
+        // (window) within the window; none when the tile is listed only for the other query tile
+        const int jt = tile_at(j);
+        int lo = 0, hi = n - jt * BN;
+        if (causal) hi = min(hi, row - jt * BN + 1);
+        if constexpr (MASKED) {
+          if (window > 0) {
+            lo = row - window + 1 - jt * BN;
+            if (!causal) hi = min(hi, row + window - jt * BN);
+          }
+          if (!((jflag[j] >> q) & 1)) hi = lo = 0;
+        }
+        if (lo > 0 || hi < BN) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c < lo || c >= hi) s[c] = -INFINITY;
+        }
+        const float mx = row_max(s);
+        const float m_blk = mx * scale_log2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m == -INFINITY) {
+          m = m_blk;  // first visible block of this row: O is written fresh (or is still zero)
+          alpha = 0.f;
+        } else if (m_blk > m + kRescaleThreshold) {
+          alpha = ex2(m - m_blk);
+          m = m_blk;
+          rescale = true;
+        }
+        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
+#pragma unroll
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2(fmaf(s[h * 64 + 2 * i], scale_log2, neg_m));
+            const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], scale_log2, neg_m));
+            part[i & 3] += p0 + p1;
+            pk[i] = pack2<BF16>(p0, p1);
+          }
+          tmem_st32(tmem_addr(tbase, lane_base, s_col + h * 32), pk);
+        }
+        const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+        l = l * alpha + sum;
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O row *= alpha; O is stable: the PV of block j-1 completed before S_j
+          // (NQ = 2: same issuing thread, in order) or pv_done says so (NQ = 1).
+          if constexpr (C::NQ == 1) {
+            ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done, (t - 1) & 1, ctx, 34));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const float a = rescale ? alpha : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem_addr(tbase, lane_base, o_col + c * 32), r);
-          tmem_wait_ld();
-          reg_fence(r);
-          uint32_t pk[16];
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            const uint32_t ta = tmem_addr(tbase, lane_base, o_col + c * 32);
+            tmem_ld32(ta, r);
+            tmem_wait_ld();
+            reg_fence(r);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-          if (row < n) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+            tmem_st32(ta, r);
           }
         }
-        if (row < n) lse[(int64_t)head * n + row] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-        if (counter && rit == 0) atomicAdd(counter, (unsigned long long)(MASKED ? list_hdr[2 + q] : nb));
+        tmem_wait_st();
+        tc_fence_before();
+        // NQ = 1: one barrier per S buffer; with a single one the softmax could finish blocks j
+        // and j + 1 while the MMA warp still waits for V_j, and its parity wait on phase j would
+        // then see phase j + 1
+        mbar_arrive(B.p_full + (C::NQ == 2 ? q : (t & 1)));
       }
-    } else if (MASKED && ok && nb == 0 && row < n) {
-      // no listed key tile for this query tile: its rows see no key (O = 0, L = -inf)
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2);
+      // epilogue: O / l -> global (16-bit), L = (m + log2 l) ln 2
+      if (ok && nb > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(B.o_full + q, oq & 1, ctx, 40 + q));
+        if (ok) {
+          tc_fence_after();
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          uint8_t* orow = reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2;
 #pragma unroll 1
-      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-      lse[(int64_t)head * n + row] = -INFINITY;
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem_addr(tbase, lane_base, o_col + c * 32), r);
+            tmem_wait_ld();
+            reg_fence(r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+            if (row < n) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+          // every TMEM load of O is done (each chunk waited): the next item may overwrite it
+          tc_fence_before();
+          mbar_arrive(B.o_empty + q);
+          ++oq;
+          if (row < n) lse[(int64_t)head * n + row] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          if (counter && rit == 0) atomicAdd(counter, (unsigned long long)(MASKED ? list_hdr[2 + q] : nb));
+        }
+      } else if (MASKED && ok && nb == 0 && row < n) {
+        // no listed key tile for this query tile: its rows see no key (O = 0, L = -inf)
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2);
+#pragma unroll 1
+        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        lse[(int64_t)head * n + row] = -INFINITY;
+      }
+      tq += nb;
     }
   }
 
@@ -537,6 +622,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+}
+
+// Largest per-CTA work (key tiles) of a persistent causal grid of g CTAs over the items, in grid
+// order or snake order: the same item order and key-tile counts as the kernel.
+int64_t max_cta_tiles(int bh, int tiles_per_head, int n, int nq_tiles, int g, bool snake) {
+  std::vector<int64_t> load(g, 0);
+  const int64_t total = (int64_t)bh * tiles_per_head;
+  const int nblocks = (n + BN - 1) / BN;
+  for (int64_t r = 0; r * g < total; ++r)
+    for (int c = 0; c < g; ++c) {
+      const int64_t item = r * g + ((snake && (r & 1)) ? (g - 1 - c) : c);
+      if (item >= total) continue;
+      int head, rank;
+      grouped_work_item((int)item, bh, tiles_per_head, &head, &rank);
+      const int tile = tiles_per_head - 1 - rank;
+      for (int q = 0; q < nq_tiles; ++q) {
+        const int first = tile * nq_tiles * BM + q * BM;
+        if (first < n) load[c] += std::min(nblocks, (std::min(first + BM, n) - 1) / BN + 1);
+      }
+    }
+  return *std::max_element(load.begin(), load.end());
 }
 
 template <int D, bool BF16, bool MASKED>
@@ -555,9 +661,18 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
   if (e != cudaSuccess) return e;
   const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  kern<<<(unsigned)(a.bh * tiles), C::THREADS, smem, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
+  // one CTA per SM walking the items; masked launches keep one item per CTA (its tile list
+  // lives in shared memory)
+  const int64_t items = (int64_t)a.bh * tiles;
+  const int64_t grid = MASKED ? items : std::min<int64_t>(items, device_sm_count());
+  const int snake = (!MASKED && a.causal && grid < items &&
+                     max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, true) <
+                         max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, false))
+                        ? 1
+                        : 0;
+  kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
                                                                  a.causal, a.group, a.err, a.counter, a.window,
-                                                                 a.block_mask, a.mask_heads, a.heads);
+                                                                 a.block_mask, a.mask_heads, a.heads, snake);
   return cudaGetLastError();
 }
 

@@ -88,6 +88,8 @@ struct DecodeArgs {
 };
 // Streaming multiprocessors of a GB300, for sizing grids.
 constexpr int kSmCount = 152;
+// Streaming multiprocessors of the current device (cached per device; kSmCount if unknown).
+int device_sm_count();
 int decode_auto_splits(int b, int h, int hkv, int nq, int nk);
 int decode_tc_auto_splits(int b, int h, int hkv, int nq, int nk, int d);
 bool decode_tc_supported(int dtype, int d, int64_t q_rows);

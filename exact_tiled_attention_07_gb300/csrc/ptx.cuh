@@ -65,12 +65,27 @@ __device__ __forceinline__ bool elect_one_sync() {
 // lightest, all heads of the group per tile.  The block scheduler then runs a
 // longest-first list schedule per group while the CTAs running together touch at most a
 // group's heads, whose K/V (or Q/dO) stay in L2.  `heavy_rank` 0 is the heaviest tile.
+// %ctaid.x / %nctaid.x through volatile reads: the compiler cannot hoist them out of a loop and
+// keep them in registers, which matters in kernels at the register cap.
+__device__ __forceinline__ uint32_t cta_id_x() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(v));
+  return v;
+}
+__device__ __forceinline__ uint32_t grid_dim_x() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%nctaid.x;" : "=r"(v));
+  return v;
+}
+
 constexpr int kHeadGroup = 16;
-__device__ __forceinline__ void grouped_work_item(int bid, int heads, int tiles, int* head, int* heavy_rank) {
+__host__ __device__ __forceinline__ void grouped_work_item(int bid, int heads, int tiles, int* head,
+                                                           int* heavy_rank) {
   const int per_group = kHeadGroup * tiles;
   const int g = bid / per_group;
   const int r = bid - g * per_group;
-  const int gsize = min(kHeadGroup, heads - g * kHeadGroup);
+  const int rest = heads - g * kHeadGroup;
+  const int gsize = kHeadGroup < rest ? kHeadGroup : rest;
   *heavy_rank = r / gsize;
   *head = g * kHeadGroup + (r - *heavy_rank * gsize);
 }
