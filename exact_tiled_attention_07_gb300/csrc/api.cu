@@ -100,9 +100,12 @@ fa_status launched(cudaError_t e, const char* what) {
   return FA_OK;
 }
 
+// after the per-row vectors and the dQ accumulator: the backward's work-item queue counters
+constexpr size_t kSchedBytes = 256;
+
 size_t workspace_bytes_for(int B, int H, int N, int d) {
   const size_t bh = (size_t)B * H, npad = (size_t)padded_rows(N);
-  return bh * npad * 4 * (2 + (size_t)d);
+  return bh * npad * 4 * (2 + (size_t)d) + kSchedBytes;
 }
 
 fa_status carve(BwdArgs* a, void* ws, size_t ws_bytes, int B, int H, int N, int d) {
@@ -113,6 +116,7 @@ fa_status carve(BwdArgs* a, void* ws, size_t ws_bytes, int B, int H, int N, int 
   a->delta = base;
   a->lse2 = base + rows;
   a->dq_acc = base + 2 * rows;
+  a->sched = reinterpret_cast<unsigned*>(base + rows * (2 + (size_t)d));
   return FA_OK;
 }
 

@@ -34,8 +34,10 @@
 // future are skipped, §5.3) and only pairs crossing the diagonal are masked element-wise.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <vector>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -67,8 +69,9 @@ struct BwdCfg {
   static constexpr int OFF_STG = OFF_DS + DS_BYTES;              // dQ staging tile
   static constexpr int OFF_VEC = OFF_STG + STG_BYTES;            // [QSTAGES] x (L2[BM], D[BM]) fp32
   static constexpr int OFF_BAR = OFF_VEC + QSTAGES * 2 * BM * 4;
-  static constexpr int NBAR = 18;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int NBAR = 24;
+  // after the barriers: TMEM base, abort flag, the two work-item slots
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 32;
   // masked variant: the CTA's step list after the barriers (an int count, then uint16 entries
   // (query head of the group << 12 | 128-row query block), rounded up to 8 entries)
   static constexpr int OFF_LIST = SMEM;
@@ -81,6 +84,10 @@ struct BwdCfg {
   static constexpr int COMPUTE_THREADS = SPLIT ? 256 : 128;
   static constexpr int DRAIN_THREADS = SPLIT ? 256 : 128;
   static constexpr int CH_COLS = SPLIT ? 32 : 16;  // TMEM columns between packed 32-query chunks
+  static constexpr int EPI_THREADS = SPLIT ? 256 : 128;  // threads that read dK, dV out of TMEM
+  // the staging tile also carries an item's dV and dK as 16-bit [128 rows][64 columns] boxes with
+  // the 128-byte swizzle (d = 128: dV, then dK, two boxes each; d = 64: dV and dK side by side)
+  static_assert(STG_BYTES >= 2 * BN * 128 && OFF_STG % 1024 == 0, "staging tile");
   // TMEM columns: K_j as a 16-bit A operand (d/2 columns), S^T (P^T packed into the first 16
   // of each 32-query chunk's columns), dP^T (dS^T likewise), the dQ partial and the dV, dK
   // accumulators
@@ -107,7 +114,12 @@ enum BwdBar {
   B_KT_READY = 15,  // K_j copied into TMEM
   B_STG_FREE = 16,  // dQ staging tile free (the previous reduction has read it)
   B_STG_FULL = 17,  // both warpgroups wrote their half of the staging tile
+  B_KV_EMPTY = 18,  // the tensor core no longer reads this item's K_j, V_j (persistent)
+  B_ACC_EMPTY = 19, // this item's dK, dV have left TMEM (persistent)
+  B_ITEM_FULL = 20,   // [2] the producer published the next work item in its slot
+  B_ITEM_EMPTY = 22,  // [2] every consumer warp has read it
 };
+constexpr uint32_t kItemReaders = 9;  // the MMA warp and the eight compute warps
 
 // TMEM column of the packed 16-bit A operand (P^T or dS^T) for MMA k-step kk (16 queries),
 // chunk c of 32 queries starting at c * ch_cols: contiguous (16) when one warpgroup reads every
@@ -125,24 +137,37 @@ __device__ __forceinline__ void step_next(int& ii, int& g, int tiles_per_head) {
   }
 }
 
-template <int D>
-__device__ __forceinline__ void store_row16(void* base, int64_t row, const uint32_t (&pk)[16], int chunk) {
-  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(base) + row * D * 2 + chunk * 64);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-}
+// Work item of the persistent backward: one 128-key tile of one key/value head.
+struct BwdItem {
+  int kvh;          // key/value head
+  int k0;           // first key row
+  int i_start;      // first query tile reaching this key tile's diagonal (causal), else 0
+  int nsteps_head;  // query tiles per query head
+  int nsteps;       // steps: (query head of the group, query tile) pairs
+};
 
-// Masked variant (block mask and/or window): one warp lists, before the roles start, the
-// (query head of the group, 128-row query block) pairs that can see this key tile (block-mask
-// byte set and some pair inside the causal and window bounds); every role walks that list.
+// Persistent: a CTA (one per SM) takes work items from a queue (a ticket counter in the
+// workspace, items numbered heaviest first) until it is empty, so CTAs that finish early take
+// more, whatever the cause.  It keeps its TMEM, barriers and rings between items: the next
+// item's K_j, V_j load as soon as the tensor core no longer reads the current ones (kv_empty),
+// and the current item's dK, dV leave TMEM through the staging tile (TMA stores) while the next
+// item's first scores are computed; its first dV, dK GEMMs wait until they have (acc_empty).
+// Every barrier phase runs on counters that continue across items.  The producer warp draws
+// the tickets and publishes each item in a two-slot ring (item_full / item_empty).  The last
+// CTA to finish sets the counter back to zero, ready for the next launch.
+// Masked variant (block mask and/or window): one CTA per item; one warp lists, before the
+// roles start, the (query head of the group, 128-row query block) pairs that can see the key
+// tile (block-mask byte set and some pair inside the causal and window bounds); every role
+// walks that list.
 template <int D, bool BF16, bool MASKED>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2,
-                  const float* __restrict__ delta, void* __restrict__ dk_out, void* __restrict__ dv_out, int n,
-                  int npad, int bh_count, int ktiles, float scale, int causal, int group, unsigned long long* err,
-                  int window, const uint8_t* __restrict__ block_mask, int mask_heads, int heads) {
+                  const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                  const __grid_constant__ CUtensorMap tm_dv, const float* __restrict__ lse2,
+                  const float* __restrict__ delta, int n, int npad, int bh_count, int ktiles, float scale,
+                  int causal, int group, unsigned long long* err, int window,
+                  const uint8_t* __restrict__ block_mask, int mask_heads, int heads, unsigned* __restrict__ sched) {
   using C = BwdCfg<D>;
   constexpr int BM = C::BM;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -151,27 +176,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
   const ErrCtx ctx{err, abort_flag};
 
-  // work item: head-major (CTAs running together share Q/dO in L2); causal: heaviest (first)
-  // key tiles first within groups of heads
-  int kvh, kt;  // key/value head and key tile of this CTA
-  if (causal) {
-    grouped_work_item(blockIdx.x, bh_count, ktiles, &kvh, &kt);
-  } else {
-    kvh = blockIdx.x / ktiles;
-    kt = blockIdx.x - kvh * ktiles;
-  }
-  const int k0 = kt * BN;
   const int qtiles = (n + BM - 1) / BM;
-  const int i_start = causal ? kt * (BN / BM) : 0;  // first query tile reaching this key tile's diagonal
-  // steps: (query head of this key/value head's group, query tile) pairs; dK, dV sum over all
-  const int nsteps_head = qtiles - i_start;
-  int nsteps = group * nsteps_head;
+  const int64_t total_items = (int64_t)bh_count * ktiles;
+  // work item -> key/value head and key tile: head-major (CTAs running together share Q/dO in
+  // L2); causal: heaviest (first) key tiles first within groups of heads
+  auto tile_of = [&](int item, int* kvh, int* kt) {
+    if (causal) {
+      grouped_work_item(item, bh_count, ktiles, kvh, kt);
+    } else {
+      *kvh = item / ktiles;
+      *kt = item - *kvh * ktiles;
+    }
+  };
   int* list_hdr = reinterpret_cast<int*>(smem + C::OFF_LIST);
   uint16_t* slist = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST + 16);
   if constexpr (MASKED) {
     if (warp == C::PRODUCER_WARP) {
+      int kvh, kt;
+      tile_of((int)blockIdx.x, &kvh, &kt);
+      const int k0 = kt * BN;
       const int nblk = (n + 127) / 128;
       const int kmax = min(n, k0 + BN) - 1;
       int count = 0;
@@ -199,19 +225,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (lane == 0) list_hdr[0] = count;
     }
   }
-  // step i -> (query head within the group, first query row)
-  auto step_rows = [&](int i, int ii, int g, int* gm, int* q0) {
-    if constexpr (MASKED) {
-      const uint32_t e = slist[i / C::SUB];
-      *gm = (int)(e >> 12);
-      *q0 = (int)(e & 0xFFFu) * 128 + (i % C::SUB) * BM;
-    } else {
-      *gm = g;
-      *q0 = (i_start + ii) * BM;
-    }
-  };
-  // each role walks the steps with a (query tile ii, query head g of the group) cursor, advanced
-  // by step_next (no integer division on the per-step path)
   const float scale_log2 = scale * 1.4426950408889634f;
 
   if (threadIdx.x == 0) {
@@ -233,6 +246,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar + B_ACC_FULL, 1);
     mbar_init(bar + B_DRAIN, 1);
     mbar_init(bar + B_KT_READY, 128);
+    mbar_init(bar + B_KV_EMPTY, 1);
+    mbar_init(bar + B_ACC_EMPTY, C::EPI_THREADS);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar + B_ITEM_FULL + t, 1);
+      mbar_init(bar + B_ITEM_EMPTY + t, kItemReaders);
+    }
     fence_barrier_init();
   }
   if (warp == C::MMA_WARP) {
@@ -244,7 +263,83 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const bool start_ok = (*abort_flag == 0);
-  if constexpr (MASKED) nsteps = list_hdr[0] * C::SUB;
+
+  auto item_at = [&](int item) {
+    BwdItem w;
+    int kt;
+    tile_of(item, &w.kvh, &kt);
+    w.k0 = kt * BN;
+    w.i_start = causal ? kt * (BN / BM) : 0;
+    w.nsteps_head = qtiles - w.i_start;
+    w.nsteps = MASKED ? list_hdr[0] * C::SUB : group * w.nsteps_head;
+    return w;
+  };
+  // this CTA's r-th item, -1 when there is none.  Masked: the CTA's own item only.  Otherwise
+  // one warp's read of the producer's slot r % 2; every consumer warp reads every slot once.
+  // `good` turns false (and the item -1) when the bounded wait for the slot ran out.
+  auto next_item = [&](int r, bool& good) {
+    if constexpr (MASKED) {
+      return r == 0 ? (int)blockIdx.x : -1;
+    } else {
+      const int t = r & 1;
+      good = __all_sync(0xffffffffu, mbar_wait(bar + B_ITEM_FULL + t, (uint32_t)(r >> 1) & 1, ctx, 150)) && good;
+      const int item = good ? item_slot[t] : -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + B_ITEM_EMPTY + t);
+      return item;
+    }
+  };
+  // step i of an item -> (query head within the group, first query row)
+  auto step_rows = [&](const BwdItem& w, int i, int ii, int g, int* gm, int* q0) {
+    if constexpr (MASKED) {
+      const uint32_t e = slist[i / C::SUB];
+      *gm = (int)(e >> 12);
+      *q0 = (int)(e & 0xFFFu) * 128 + (i % C::SUB) * BM;
+    } else {
+      *gm = g;
+      *q0 = (w.i_start + ii) * BM;
+    }
+  };
+  // K_j rows -> TMEM (A operand of S^T = K Q^T): 16-byte chunks of the swizzled smem tile; row
+  // rit of the tile, TMEM lane quarter lane_base
+  auto k_to_tmem = [&](int rit, uint32_t lane_base) {
+    const uint32_t sw = (uint32_t)(rit & 7);
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb) {
+      const uint8_t* krow = smem + C::OFF_K + kb * (BN * 128) + rit * 128;
+      uint32_t w[32];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 x = *reinterpret_cast<const uint4*>(krow + (((uint32_t)ch ^ sw) << 4));
+        w[4 * ch] = x.x;
+        w[4 * ch + 1] = x.y;
+        w[4 * ch + 2] = x.z;
+        w[4 * ch + 3] = x.w;
+      }
+      tmem_st32(tmem_addr(tbase, lane_base, C::COL_K + kb * 32), w);
+    }
+    tmem_wait_st();
+  };
+  // 32 columns of a dK / dV accumulator row -> 16-bit pairs (x f)
+  auto load_acc32 = [&](uint32_t lane_base, uint32_t col, float f, uint32_t (&pk)[16]) {
+    uint32_t r[32];
+    tmem_ld32(tmem_addr(tbase, lane_base, col), r);
+    tmem_wait_ld();
+    reg_fence(r);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) pk[t] = pack2<BF16>(__uint_as_float(r[2 * t]) * f, __uint_as_float(r[2 * t + 1]) * f);
+  };
+  // 32 columns (chunk c) of row `row` of a [128 rows][64 columns] 16-bit box with the 128-byte
+  // swizzle, the layout of the dK / dV tensor maps' boxes
+  auto stage_row32 = [&](uint8_t* box, int row, int c, const uint32_t (&pk)[16]) {
+    uint8_t* rp = box + row * 128;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
+      *reinterpret_cast<uint4*>(rp + ((ch ^ (uint32_t)(row & 7)) << 4)) =
+          make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+    }
+  };
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
@@ -253,35 +348,58 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar + B_KV, 2 * C::KV_BYTES);
-      for (int kb = 0; kb < C::KB; ++kb) {
-        tma_load_3d(smem + C::OFF_K + kb * (BN * 128), &tm_k, bar + B_KV, kb * 64, k0, kvh);
-        tma_load_3d(smem + C::OFF_V + kb * (BN * 128), &tm_v, bar + B_KV, kb * 64, k0, kvh);
-      }
-      int issued = 0;
-      for (int i = 0, ii = 0, g = 0; i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
-        const int s = i % C::QSTAGES, use = i / C::QSTAGES;
-        if (use > 0 && !mbar_wait(bar + B_QD_EMPTY + s, (use - 1) & 1, ctx, 110)) break;
-        int gm, q0;
-        step_rows(i, ii, g, &gm, &q0);
-        const int qh = kvh * group + gm;
-        uint64_t* fb = bar + B_QD_FULL + s;
-        mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + 2 * BM * 4);
-        for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(smem + C::OFF_Q + s * C::QT_BYTES + kb * (BM * 128), &tm_q, fb, kb * 64, q0, qh);
-          tma_load_3d(smem + C::OFF_DO + s * C::QT_BYTES + kb * (BM * 128), &tm_do, fb, kb * 64, q0, qh);
+      uint32_t qpos = 0;  // query-tile ring loads issued (all items)
+      int kv_loads = 0;
+      bool ok = true;
+      for (int r = 0;; ++r) {
+        int item;
+        if constexpr (MASKED) {
+          item = r == 0 ? (int)blockIdx.x : -1;
+        } else {
+          // draw a ticket and publish the item (or -1: the queue is empty) once both readers of
+          // the slot's previous item have it
+          if (r >= 2 && !(ok = mbar_wait(bar + B_ITEM_EMPTY + (r & 1), (uint32_t)((r - 2) >> 1) & 1, ctx, 114))) break;
+          const unsigned ticket = atomicAdd(sched, 1u);
+          item = ticket < (unsigned)total_items ? (int)ticket : -1;
+          item_slot[r & 1] = item;
+          mbar_arrive(bar + B_ITEM_FULL + (r & 1));
         }
-        float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + s * 2 * BM;
-        bulk_load(vec, lse2 + (int64_t)qh * npad + q0, BM * 4, fb);
-        bulk_load(vec + BM, delta + (int64_t)qh * npad + q0, BM * 4, fb);
-        issued = i + 1;
+        if (item < 0) break;
+        const BwdItem w = item_at(item);
+        // K_j, V_j once the tensor core no longer reads the previous item's
+        if (r > 0 && !(ok = mbar_wait(bar + B_KV_EMPTY, (r - 1) & 1, ctx, 113))) break;
+        mbar_arrive_expect_tx(bar + B_KV, 2 * C::KV_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_3d(smem + C::OFF_K + kb * (BN * 128), &tm_k, bar + B_KV, kb * 64, w.k0, w.kvh);
+          tma_load_3d(smem + C::OFF_V + kb * (BN * 128), &tm_v, bar + B_KV, kb * 64, w.k0, w.kvh);
+        }
+        ++kv_loads;
+        for (int i = 0, ii = 0, g = 0; i < w.nsteps; ++i, step_next(ii, g, w.nsteps_head)) {
+          const int s = qpos % C::QSTAGES, use = qpos / C::QSTAGES;
+          if (use > 0 && !(ok = mbar_wait(bar + B_QD_EMPTY + s, (use - 1) & 1, ctx, 110))) break;
+          int gm, q0;
+          step_rows(w, i, ii, g, &gm, &q0);
+          const int qh = w.kvh * group + gm;
+          uint64_t* fb = bar + B_QD_FULL + s;
+          mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + 2 * BM * 4);
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(smem + C::OFF_Q + s * C::QT_BYTES + kb * (BM * 128), &tm_q, fb, kb * 64, q0, qh);
+            tma_load_3d(smem + C::OFF_DO + s * C::QT_BYTES + kb * (BM * 128), &tm_do, fb, kb * 64, q0, qh);
+          }
+          float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + s * 2 * BM;
+          bulk_load(vec, lse2 + (int64_t)qh * npad + q0, BM * 4, fb);
+          bulk_load(vec + BM, delta + (int64_t)qh * npad + q0, BM * 4, fb);
+          ++qpos;
+        }
+        if (!ok) break;
       }
+      // drain: every copy this thread started must land before the CTA may exit
       ErrCtx nctx = ctx;
       int no_abort = 0;
       nctx.abort = &no_abort;
-      mbar_wait(bar + B_KV, 0, nctx, 111);
-      for (int i = issued - 1; i >= 0 && i >= issued - C::QSTAGES; --i)
-        mbar_wait(bar + B_QD_FULL + i % C::QSTAGES, (i / C::QSTAGES) & 1, nctx, 112);
+      if (kv_loads > 0) mbar_wait(bar + B_KV, (kv_loads - 1) & 1, nctx, 111);
+      for (int64_t p = (int64_t)qpos - 1; p >= 0 && p >= (int64_t)qpos - C::QSTAGES; --p)
+        mbar_wait(bar + B_QD_FULL + p % C::QSTAGES, (uint32_t)(p / C::QSTAGES) & 1, nctx, 112);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
@@ -332,85 +450,105 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         __syncwarp();
       };
-      bool ok = wait(bar + B_KV, 0, 120);
-      if (ok) ok = wait(bar + B_KT_READY, 0, 126);
-      if (ok && nsteps > 0) {
-        ok = wait(bar + B_QD_FULL + 0, 0, 121);
-        if (ok) {
-          tc_fence_after();
-          issue_s(qs_of(0));
-          commit(bar + B_S_FULL);
-        }
-      }
-      for (int i = 0; ok && i < nsteps; ++i) {
-        const int s = i % C::QSTAGES;
-        const int s1 = (i + 1) % C::QSTAGES;
-        const uint32_t qs = qs_of(s), dos = dos_of(s);
-        // dP^T_i (its columns, holding dS^T_{i-1}, were last read by dK_{i-1}: same lane, in order)
-        issue_dp(dos);
-        commit(bar + B_DP_FULL);
-        // dV += P^T dO_i (P^T from TMEM, K = queries; dO_i as MN-major B)
-        {
-          uint64_t bd[BM / 16];
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) bd[kk] = make_sdesc_sw128(dos + kk * 2048, BM * 128, 1024);
-          if (!(ok = wait(bar + B_P_READY, i & 1, 123))) break;
-          tc_fence_after();
-          if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk)
-              umma_ts(tbase + C::COL_DV, tbase + C::COL_S + packed_col(kk, C::CH_COLS), bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          __syncwarp();
-        }
-        // S^T_{i+1}: overwrites P^T_i only after dV_i has read it (same issuing lane, in order)
-        if (i + 1 < nsteps) {
-          if (!(ok = wait(bar + B_QD_FULL + s1, ((i + 1) / C::QSTAGES) & 1, 121))) break;
-          tc_fence_after();
-          issue_s(qs_of(s1));
-          commit(bar + B_S_FULL);
-        }
-        // dK += dS^T Q_i (dS^T 16-bit in TMEM over the dP^T columns, Q_i MN-major)
-        {
-          uint64_t bd[BM / 16];
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) bd[kk] = make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024);
-          if (!(ok = wait(bar + B_DS_READY, i & 1, 124))) break;
-          tc_fence_after();
-          if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk)
-              umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + packed_col(kk, C::CH_COLS), bd[kk], idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          __syncwarp();
-        }
-        commit(bar + B_QD_EMPTY + s);
-        // dQ partial (the previous one drained from TMEM first)
-        {
-          uint64_t kd[BN / 16], sd[BN / 16];
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            kd[kk] = make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024);   // K as MN-major (d contiguous)
-            sd[kk] = make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024);  // dS^T as MN-major (queries contiguous)
-          }
-          if (i > 0) {
-            if (!(ok = wait(bar + B_DQ_FREE, (i - 1) & 1, 122))) break;
+      bool ok = true;
+      uint32_t gs = 0;  // steps issued (all items): ring slot and barrier phases
+      for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
+        const BwdItem w = item_at(item);
+        // this item's K_j, V_j in shared memory and K_j in TMEM
+        ok = wait(bar + B_KV, r & 1, 120);
+        if (ok) ok = wait(bar + B_KT_READY, r & 1, 126);
+        if (ok && w.nsteps > 0) {
+          ok = wait(bar + B_QD_FULL + gs % C::QSTAGES, (gs / C::QSTAGES) & 1, 121);
+          if (ok) {
             tc_fence_after();
+            issue_s(qs_of(gs % C::QSTAGES));
+            commit(bar + B_S_FULL);
           }
-          if (leader) {
+        }
+        // the previous item's dK, dV must have left TMEM before this item's first dV, dK
+        bool acc_free = (r == 0);
+        for (int i = 0; ok && i < w.nsteps; ++i, ++gs) {
+          const int s = gs % C::QSTAGES;
+          const uint32_t g1 = gs + 1;
+          const int s1 = g1 % C::QSTAGES;
+          const uint32_t qs = qs_of(s), dos = dos_of(s);
+          // dP^T_i (its columns, holding dS^T_{i-1}, were last read by dK_{i-1}: same lane, in order)
+          issue_dp(dos);
+          commit(bar + B_DP_FULL);
+          // dV += P^T dO_i (P^T from TMEM, K = queries; dO_i as MN-major B)
+          {
+            uint64_t bd[BM / 16];
+#pragma unroll
+            for (int kk = 0; kk < BM / 16; ++kk) bd[kk] = make_sdesc_sw128(dos + kk * 2048, BM * 128, 1024);
+            if (!(ok = wait(bar + B_P_READY, gs & 1, 123))) break;
+            if (!acc_free) {
+              if (!(ok = wait(bar + B_ACC_EMPTY, (r - 1) & 1, 127))) break;
+              acc_free = true;
+            }
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < BM / 16; ++kk)
+                umma_ts(tbase + C::COL_DV, tbase + C::COL_S + packed_col(kk, C::CH_COLS), bd[kk], idesc_kv,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            __syncwarp();
+          }
+          // S^T_{i+1}: overwrites P^T_i only after dV_i has read it (same issuing lane, in order)
+          if (i + 1 < w.nsteps) {
+            if (!(ok = wait(bar + B_QD_FULL + s1, (g1 / C::QSTAGES) & 1, 121))) break;
+            tc_fence_after();
+            issue_s(qs_of(s1));
+            commit(bar + B_S_FULL);
+          }
+          // dK += dS^T Q_i (dS^T 16-bit in TMEM over the dP^T columns, Q_i MN-major)
+          {
+            uint64_t bd[BM / 16];
+#pragma unroll
+            for (int kk = 0; kk < BM / 16; ++kk) bd[kk] = make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024);
+            if (!(ok = wait(bar + B_DS_READY, gs & 1, 124))) break;
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < BM / 16; ++kk)
+                umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + packed_col(kk, C::CH_COLS), bd[kk], idesc_kv,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            __syncwarp();
+          }
+          commit(bar + B_QD_EMPTY + s);
+          // dQ partial (the previous one, of this item or the last, drained from TMEM first)
+          {
+            uint64_t kd[BN / 16], sd[BN / 16];
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
-              if constexpr (C::DQT)
-                umma_ss(tbase + C::COL_DQ, kd[kk], sd[kk], idesc_q, kk > 0);
-              else
-                umma_ss(tbase + C::COL_DQ, sd[kk], kd[kk], idesc_q, kk > 0);
+              kd[kk] = make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024);   // K as MN-major (d contiguous)
+              sd[kk] = make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024);  // dS^T as MN-major (queries contiguous)
             }
+            if (gs > 0) {
+              if (!(ok = wait(bar + B_DQ_FREE, (gs - 1) & 1, 122))) break;
+              tc_fence_after();
+            }
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                if constexpr (C::DQT)
+                  umma_ss(tbase + C::COL_DQ, kd[kk], sd[kk], idesc_q, kk > 0);
+                else
+                  umma_ss(tbase + C::COL_DQ, sd[kk], kd[kk], idesc_q, kk > 0);
+              }
+            }
+            __syncwarp();
           }
-          __syncwarp();
+          commit(bar + B_DQ_FULL);
         }
-        commit(bar + B_DQ_FULL);
+        // an item without steps still takes its turn on acc_empty, so the phases stay in step
+        if (ok && !acc_free) ok = wait(bar + B_ACC_EMPTY, (r - 1) & 1, 127);
+        if (ok) {
+          commit(bar + B_ACC_FULL);  // this item's dK, dV accumulators are final
+          commit(bar + B_KV_EMPTY);  // and its K_j, V_j are no longer read
+        }
       }
-      if (ok) commit(bar + B_ACC_FULL);
       // drain: all MMAs complete before TMEM is released
       ErrCtx nctx = ctx;
       int no_abort = 0;
@@ -420,334 +558,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     __syncwarp();
   } else if (!C::SPLIT && warp < 4) {
-    // ---------------------------------------------------------------- WG0: P^T, dS^T, epilogue
+    // ---------------------------------------------------------------- WG0: K_j -> TMEM, P^T, dS^T
     const uint32_t lane_base = warp * 32;
     const int rit = warp * 32 + lane;  // key row within the tile
-    const int key = k0 + rit;
-    const bool key_ok = key < n;
     uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
     const uint32_t sw = (uint32_t)(rit & 7);
     bool ok = start_ok;
-    // K_j row -> TMEM (A operand of S^T = K Q^T): 16-byte chunks of the swizzled smem tile
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_KV, 0, ctx, 134));
-    if (ok) {
-#pragma unroll
-      for (int kb = 0; kb < C::KB; ++kb) {
-        const uint8_t* krow = smem + C::OFF_K + kb * (BN * 128) + rit * 128;
-        uint32_t w[32];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 x = *reinterpret_cast<const uint4*>(krow + (((uint32_t)ch ^ sw) << 4));
-          w[4 * ch] = x.x;
-          w[4 * ch + 1] = x.y;
-          w[4 * ch + 2] = x.z;
-          w[4 * ch + 3] = x.w;
-        }
-        tmem_st32(tmem_addr(tbase, lane_base, C::COL_K + kb * 32), w);
-      }
-      tmem_wait_st();
+    uint32_t gs = 0;  // steps processed (all items)
+    for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
+      const BwdItem w = item_at(item);
+      const int key = w.k0 + rit;
+      const bool key_ok = key < n;
+      // K_j -> TMEM: the previous item's last S^T (which read it) completed before its last step
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_KV, r & 1, ctx, 134));
+      if (!ok) break;
+      k_to_tmem(rit, lane_base);
       tc_fence_before();
       mbar_arrive(bar + B_KT_READY);
-    }
-    for (int i = 0, ii = 0, g = 0; ok && i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
-      const int s = i % C::QSTAGES;
-      int gm, q0;
-      step_rows(i, ii, g, &gm, &q0);
-      const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
-      const float* dvec = l2v + BM;
-      // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (i / C::QSTAGES) & 1, ctx, 133));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, i & 1, ctx, 130));
-      if (!ok) break;
-      tc_fence_after();
-      // visible queries q0 + qc: qc in [mask_below, mask_above) (causal: not before this key;
-      // window: |query - key| < window, an upper bound on the query with or without causal)
-      int mask_below = causal ? key - q0 : INT32_MIN, mask_above = INT32_MAX;
-      if constexpr (MASKED) {
-        if (window > 0) {
-          mask_below = max(mask_below, key - window + 1 - q0);
-          mask_above = key + window - q0;
-        }
-      }
-      // P^T row (this key against the BM queries), kept as packed 16-bit pairs: the same
-      // rounded values feed dV += P^T dO and dS = P o (dP - D)
-      uint32_t pk[BM / 2];
-#pragma unroll
-      for (int g = 0; g < BM / 64; ++g) {  // 64 columns per batch of TMEM loads
-      uint32_t sr[2][32];
-      tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + g * 64), sr[0]);
-      tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + g * 64 + 32), sr[1]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = g * 2 + cc;
-        uint32_t(&r)[32] = sr[cc];
-        reg_fence(r);
-#pragma unroll
-        for (int t = 0; t < 32; t += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(l2v + c * 32 + t);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          float e[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int qc = c * 32 + t + u;
-            const float x = ex2(fmaf(__uint_as_float(r[t + u]), scale_log2, -lv[u]));
-            e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? x : 0.f;
-          }
-          pk[(c * 32 + t) / 2] = pack2<BF16>(e[0], e[1]);
-          pk[(c * 32 + t) / 2 + 1] = pack2<BF16>(e[2], e[3]);
-        }
-      }
-      }
-#pragma unroll
-      for (int h = 0; h < BM / 64; ++h) {
-        uint32_t w[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) w[t] = pk[h * 32 + t];
-        tmem_st32(tmem_addr(tbase, lane_base, C::COL_S + h * 32), w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar + B_P_READY);
-      // dS^T = P^T o (dP^T - D); dp_full(i) also means the MMAs of step i-1 that read dS^T are done
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DP_FULL, i & 1, ctx, 131));
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int g = 0; g < BM / 64; ++g) {  // 64 columns per batch of TMEM loads
-      uint32_t dr[2][32];
-      tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + g * 64), dr[0]);
-      tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + g * 64 + 32), dr[1]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = g * 2 + cc;
-        uint32_t(&r)[32] = dr[cc];
-        reg_fence(r);
-        uint32_t dsk[16];
-#pragma unroll
-        for (int t = 0; t < 16; t += 2) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dvec + c * 32 + 2 * t);
-          const float2 p01 = unpack2<BF16>(pk[c * 16 + t]);
-          const float2 p23 = unpack2<BF16>(pk[c * 16 + t + 1]);
-          dsk[t] = pack2<BF16>(p01.x * (__uint_as_float(r[2 * t]) - d4.x), p01.y * (__uint_as_float(r[2 * t + 1]) - d4.y));
-          dsk[t + 1] = pack2<BF16>(p23.x * (__uint_as_float(r[2 * t + 2]) - d4.z),
-                                   p23.y * (__uint_as_float(r[2 * t + 3]) - d4.w));
-        }
-        // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
-        uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
-          *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
-              make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
-        }
-        // and packed into TMEM over dP^T columns already read (A operand of dK += dS^T Q)
-        tmem_st16(tmem_addr(tbase, lane_base, C::COL_DP + c * 16), dsk);
-      }
-      }
-      fence_proxy_async_smem();
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar + B_DS_READY);
-    }
-    // epilogue: dV, dK (x tau) from TMEM to global
-    if (ok && nsteps > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, 0, ctx, 132));
-      if (ok) {
-        tc_fence_after();
-#pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t col = which ? C::COL_DK : C::COL_DV;
-          const float f = which ? scale : 1.f;
-          void* dst = which ? dk_out : dv_out;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem_addr(tbase, lane_base, col + c * 32), r);
-            tmem_wait_ld();
-            reg_fence(r);
-            uint32_t pk[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-              pk[t] = pack2<BF16>(__uint_as_float(r[2 * t]) * f, __uint_as_float(r[2 * t + 1]) * f);
-            if (key_ok) store_row16<D>(dst, (int64_t)kvh * n + key, pk, c);
-          }
-        }
-      }
-    } else if (ok && nsteps == 0 && key_ok) {
-      // no query meets this key tile: zero gradients (not reachable for square causal masks)
-      uint32_t pk[16] = {};
-      for (int c = 0; c < D / 32; ++c) {
-        store_row16<D>(dk_out, (int64_t)kvh * n + key, pk, c);
-        store_row16<D>(dv_out, (int64_t)kvh * n + key, pk, c);
-      }
-    }
-
-  } else if (!C::SPLIT && warp < 8) {
-    // TMEM lane = d index (DQT) or query row; the partial goes to a staging tile in the layout
-    // of the dQ accumulator's tensor map and one thread adds it to global memory (TMA reduce).
-    const uint32_t lane_base = (warp & 3) * 32;
-    const int rr = (warp & 3) * 32 + lane;
-    const bool leader = (warp == 4 && lane == 0);
-    bool ok = start_ok;
-    // Every warp runs every step and passes both named barriers in each; once a bounded wait
-    // has run out (the abort flag then ends every later wait at once) the warp still passes
-    // them, staging stale TMEM columns that are never reduced, so none is left waiting.
-    for (int i = 0, ii = 0, g = 0; i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
-      int gm, q0;
-      step_rows(i, ii, g, &gm, &q0);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, i & 1, ctx, 140)) && ok;
-      tc_fence_after();
-      uint32_t vr[2][32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + c * 32), vr[c]);
-      tmem_wait_ld();
-      reg_fence(vr[0]);
-      reg_fence(vr[1]);
-      const uint32_t* v = &vr[0][0];
-      tc_fence_before();
-      mbar_arrive(bar + B_DQ_FREE);
-      uint8_t* stg = smem + C::OFF_STG;
-      if (leader) bulk_wait_group_read<0>();  // the previous reduction has finished reading the tile
-      named_bar_sync(1, 128);
-      if constexpr (C::DQT) {
-        // [BM queries][D] fp32, row-major: column rr (this thread's d) of each query row
-        float* st = reinterpret_cast<float*>(stg) + rr;
-#pragma unroll
-        for (int q = 0; q < BM; ++q) st[q * D] = __uint_as_float(v[q]);
-      } else {
-        // [128 queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns; row rr
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          uint8_t* bx = stg + (j >> 3) * (BM * 128) + rr * 128;
-          *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ (uint32_t)(rr & 7)) << 4)) =
-              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (leader && ok) {
-        const int qh = kvh * group + gm;
-        if constexpr (C::DQT) {
-          tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
-        } else {
-          tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
-          tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, qh);
-        }
-        bulk_commit_group();
-      }
-    }
-    if (leader) bulk_wait_group<0>();  // every reduction issued here has completed
-
-  } else if (warp < 8) {
-    if constexpr (C::SPLIT) {
-      // ---------------------------------------------------------------- WG0, WG1: P^T, dS^T, dQ drain
-      // (d = 64, 128 queries per step) Both warpgroups own the same 128 key rows (TMEM lane
-      // quarter warp % 4) and each takes half of every step's 32-query chunks for P^T and dS^T;
-      // after its dS^T half of step i each drains its half of the dQ partial of step i - 1 (that
-      // MMA completed before dP^T_i, which the dS^T half has just read).  WG0 also copies K_j
-      // into TMEM at the start and writes dK, dV at the end.
-      constexpr bool SPLIT = C::SPLIT;
-      const int wg = warp >> 2;
-      const uint32_t lane_base = (warp & 3) * 32;
-      const int rit = (warp & 3) * 32 + lane;  // key row within the tile (and TMEM lane)
-      const int key = k0 + rit;
-      const bool key_ok = key < n;
-      uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
-      const uint32_t sw = (uint32_t)(rit & 7);
-      constexpr int NCH = SPLIT ? BM / 64 : BM / 32;  // 32-query chunks a computing warpgroup takes
-      const int c0 = SPLIT ? wg * NCH : 0;
-      constexpr int DCOLS = SPLIT ? 32 : 64;  // TMEM columns of a dQ partial one thread drains
-      const int dcol0 = SPLIT ? wg * 32 : 0;
-      const bool leader = (warp == (SPLIT ? 0 : 4) && lane == 0);  // issues the dQ reductions
-      uint8_t* stg = smem + C::OFF_STG;
-      bool ok = start_ok;
-      if (wg == 0) {
-        // K_j row -> TMEM (A operand of S^T = K Q^T): 16-byte chunks of the swizzled smem tile
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_KV, 0, ctx, 134));
-        if (ok) {
-#pragma unroll
-          for (int kb = 0; kb < C::KB; ++kb) {
-            const uint8_t* krow = smem + C::OFF_K + kb * (BN * 128) + rit * 128;
-            uint32_t w[32];
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-              const uint4 x = *reinterpret_cast<const uint4*>(krow + (((uint32_t)ch ^ sw) << 4));
-              w[4 * ch] = x.x;
-              w[4 * ch + 1] = x.y;
-              w[4 * ch + 2] = x.z;
-              w[4 * ch + 3] = x.w;
-            }
-            tmem_st32(tmem_addr(tbase, lane_base, C::COL_K + kb * 32), w);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(bar + B_KT_READY);
-        }
-      }
-      // dQ partial k -> staging tile (this warpgroup's half) -> one TMA reduce-add into the fp32
-      // accumulator.  The staging handshake uses mbarriers (bounded waits), not named barriers,
-      // so a warp that gave up cannot leave the others waiting.
-      auto drain = [&](int k, int q0, int qh) {
-        bool good = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, k & 1, ctx, 140));
-        if (!good) return false;
-        tc_fence_after();
-        uint32_t vr[DCOLS / 32][32];  // this thread's TMEM columns of the partial
-#pragma unroll
-        for (int c = 0; c < DCOLS / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + dcol0 + c * 32), vr[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < DCOLS / 32; ++c) reg_fence(vr[c]);
-        const uint32_t* v = &vr[0][0];
-        tc_fence_before();
-        mbar_arrive(bar + B_DQ_FREE);
-        if (leader) {
-          bulk_wait_group_read<0>();  // the previous reduction has finished reading the tile
-          mbar_arrive(bar + B_STG_FREE);
-        }
-        good = __all_sync(0xffffffffu, mbar_wait(bar + B_STG_FREE, k & 1, ctx, 141));
-        if (!good) return false;
-        if constexpr (C::DQT) {
-          // [BM queries][D] fp32 row-major; TMEM lane = d (rit), columns = this thread's queries
-          float* st = reinterpret_cast<float*>(stg) + rit;
-#pragma unroll
-          for (int qq = 0; qq < DCOLS; ++qq) st[(dcol0 + qq) * D] = __uint_as_float(v[qq]);
-        } else {
-          // [128 queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns; TMEM lane =
-          // query row (rit), columns = this thread's d (one box per 32)
-#pragma unroll
-          for (int j = 0; j < DCOLS / 4; ++j) {
-            uint8_t* bx = stg + (dcol0 / 32 + j / 8) * (BM * 128) + rit * 128;
-            *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ sw) << 4)) =
-                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar + B_STG_FULL);
-        if (leader) {
-          if (!mbar_wait(bar + B_STG_FULL, k & 1, ctx, 142)) return false;
-          if constexpr (C::DQT) {
-            tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
-          } else {
-            tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
-            tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, qh);
-          }
-          bulk_commit_group();
-        }
-        return true;
-      };
-      int prev_q0 = 0, prev_qh = 0;
-      for (int i = 0, ii = 0, g = 0; ok && i < nsteps; ++i, step_next(ii, g, nsteps_head)) {
-        const int s = i % C::QSTAGES;
+      for (int i = 0, ii = 0, g = 0; ok && i < w.nsteps; ++i, ++gs, step_next(ii, g, w.nsteps_head)) {
+        const int s = gs % C::QSTAGES;
         int gm, q0;
-        step_rows(i, ii, g, &gm, &q0);
-
+        step_rows(w, i, ii, g, &gm, &q0);
         const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
         const float* dvec = l2v + BM;
         // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
-        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (i / C::QSTAGES) & 1, ctx, 133));
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, i & 1, ctx, 130));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (gs / C::QSTAGES) & 1, ctx, 133));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, gs & 1, ctx, 130));
         if (!ok) break;
         tc_fence_after();
         // visible queries q0 + qc: qc in [mask_below, mask_above) (causal: not before this key;
@@ -759,18 +595,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mask_above = key + window - q0;
           }
         }
-        // P^T of this key against this half's queries, kept as packed 16-bit pairs: the same
+        // P^T row (this key against the BM queries), kept as packed 16-bit pairs: the same
         // rounded values feed dV += P^T dO and dS = P o (dP - D)
-        uint32_t pk[NCH * 16];
-        {
-          uint32_t sr[NCH][32];
+        uint32_t pk[BM / 2];
 #pragma unroll
-          for (int cl = 0; cl < NCH; ++cl) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + (c0 + cl) * 32), sr[cl]);
+        for (int g = 0; g < BM / 64; ++g) {  // 64 columns per batch of TMEM loads
+          uint32_t sr[2][32];
+          tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + g * 64), sr[0]);
+          tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + g * 64 + 32), sr[1]);
           tmem_wait_ld();
 #pragma unroll
-          for (int cl = 0; cl < NCH; ++cl) {
-            const int c = c0 + cl;
-            uint32_t(&r)[32] = sr[cl];
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = g * 2 + cc;
+            uint32_t(&r)[32] = sr[cc];
             reg_fence(r);
 #pragma unroll
             for (int t = 0; t < 32; t += 4) {
@@ -783,41 +620,42 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 const float x = ex2(fmaf(__uint_as_float(r[t + u]), scale_log2, -lv[u]));
                 e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? x : 0.f;
               }
-              pk[cl * 16 + t / 2] = pack2<BF16>(e[0], e[1]);
-              pk[cl * 16 + t / 2 + 1] = pack2<BF16>(e[2], e[3]);
+              pk[(c * 32 + t) / 2] = pack2<BF16>(e[0], e[1]);
+              pk[(c * 32 + t) / 2 + 1] = pack2<BF16>(e[2], e[3]);
             }
           }
         }
 #pragma unroll
-        for (int cl = 0; cl < NCH; ++cl) {
-          uint32_t w[16];
+        for (int h = 0; h < BM / 64; ++h) {
+          uint32_t wv[32];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) w[t] = pk[cl * 16 + t];
-          tmem_st16(tmem_addr(tbase, lane_base, C::COL_S + (c0 + cl) * C::CH_COLS), w);
+          for (int t = 0; t < 32; ++t) wv[t] = pk[h * 32 + t];
+          tmem_st32(tmem_addr(tbase, lane_base, C::COL_S + h * 32), wv);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar + B_P_READY);
         // dS^T = P^T o (dP^T - D); dp_full(i) also means the MMAs of step i-1 that read dS^T are done
-        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DP_FULL, i & 1, ctx, 131));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DP_FULL, gs & 1, ctx, 131));
         if (!ok) break;
         tc_fence_after();
-        {
-          uint32_t dr[NCH][32];
 #pragma unroll
-          for (int cl = 0; cl < NCH; ++cl) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + (c0 + cl) * 32), dr[cl]);
+        for (int g = 0; g < BM / 64; ++g) {  // 64 columns per batch of TMEM loads
+          uint32_t dr[2][32];
+          tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + g * 64), dr[0]);
+          tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + g * 64 + 32), dr[1]);
           tmem_wait_ld();
 #pragma unroll
-          for (int cl = 0; cl < NCH; ++cl) {
-            const int c = c0 + cl;
-            uint32_t(&r)[32] = dr[cl];
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = g * 2 + cc;
+            uint32_t(&r)[32] = dr[cc];
             reg_fence(r);
             uint32_t dsk[16];
 #pragma unroll
             for (int t = 0; t < 16; t += 2) {
               const float4 d4 = *reinterpret_cast<const float4*>(dvec + c * 32 + 2 * t);
-              const float2 p01 = unpack2<BF16>(pk[cl * 16 + t]);
-              const float2 p23 = unpack2<BF16>(pk[cl * 16 + t + 1]);
+              const float2 p01 = unpack2<BF16>(pk[c * 16 + t]);
+              const float2 p23 = unpack2<BF16>(pk[c * 16 + t + 1]);
               dsk[t] = pack2<BF16>(p01.x * (__uint_as_float(r[2 * t]) - d4.x),
                                    p01.y * (__uint_as_float(r[2 * t + 1]) - d4.y));
               dsk[t + 1] = pack2<BF16>(p23.x * (__uint_as_float(r[2 * t + 2]) - d4.z),
@@ -831,56 +669,332 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
                   make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
             }
-            // and packed into TMEM over this chunk's dP^T columns, already read (A operand of
-            // dK += dS^T Q)
-            tmem_st16(tmem_addr(tbase, lane_base, C::COL_DP + c * C::CH_COLS), dsk);
+            // and packed into TMEM over dP^T columns already read (A operand of dK += dS^T Q)
+            tmem_st16(tmem_addr(tbase, lane_base, C::COL_DP + c * 16), dsk);
           }
         }
         fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar + B_DS_READY);
-        if constexpr (SPLIT) {
-          if (i > 0 && !(ok = drain(i - 1, prev_q0, prev_qh))) break;
-        }
-        prev_q0 = q0;
-        prev_qh = kvh * group + gm;
       }
-      if (SPLIT && ok && nsteps > 0) ok = drain(nsteps - 1, prev_q0, prev_qh);
-      if (leader) bulk_wait_group<0>();  // every reduction issued here has completed
-      // epilogue (WG0): dV, dK (x tau) from TMEM to global
-      if (wg == 0 && ok && nsteps > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, 0, ctx, 132));
-        if (ok) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int which = 0; which < 2; ++which) {
-            const uint32_t col = which ? C::COL_DK : C::COL_DV;
-            const float f = which ? scale : 1.f;
-            void* dst = which ? dk_out : dv_out;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(tmem_addr(tbase, lane_base, col + c * 32), r);
-              tmem_wait_ld();
-              reg_fence(r);
-              uint32_t pk[16];
+    }
+
+  } else if (!C::SPLIT && warp < 8) {
+    // ---------------------------------------------------------------- WG1: dQ drain, epilogue
+    // TMEM lane = d index; the dQ partial goes to a staging tile in the layout of the dQ
+    // accumulator's tensor map and one thread adds it to global memory (TMA reduce).  After an
+    // item's last partial, its dV and dK (x tau) go through the same staging tile to global
+    // memory (TMA stores), while warpgroup 0 starts the next item.
+    const uint32_t lane_base = (warp & 3) * 32;
+    const int rr = (warp & 3) * 32 + lane;  // d index of a dQ partial; key row of dK, dV
+    const bool leader = (warp == 4 && lane == 0);
+    uint8_t* stg = smem + C::OFF_STG;
+    bool ok = start_ok;
+    uint32_t gs = 0;  // dQ partials drained (all items)
+    // Every warp runs every step of every item and passes every named barrier; once a bounded
+    // wait has run out (the abort flag then ends every later wait at once) the warp still passes
+    // them, staging stale TMEM columns that are never stored, so none is left waiting.  Whether
+    // to take another item is decided by all four warps together (a reducing named barrier), so
+    // they leave the loop at the same item.
+    for (int r = 0;; ++r) {
+      bool got = true;
+      const int item = next_item(r, got);
+      if (!named_bar_and(1, 128, got && item >= 0)) break;
+      const BwdItem w = item_at(item);
+      for (int i = 0, ii = 0, g = 0; i < w.nsteps; ++i, ++gs, step_next(ii, g, w.nsteps_head)) {
+        int gm, q0;
+        step_rows(w, i, ii, g, &gm, &q0);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, gs & 1, ctx, 140)) && ok;
+        tc_fence_after();
+        uint32_t vr[2][32];
 #pragma unroll
-              for (int t = 0; t < 16; ++t)
-                pk[t] = pack2<BF16>(__uint_as_float(r[2 * t]) * f, __uint_as_float(r[2 * t + 1]) * f);
-              if (key_ok) store_row16<D>(dst, (int64_t)kvh * n + key, pk, c);
+        for (int c = 0; c < 2; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + c * 32), vr[c]);
+        tmem_wait_ld();
+        reg_fence(vr[0]);
+        reg_fence(vr[1]);
+        const uint32_t* v = &vr[0][0];
+        tc_fence_before();
+        mbar_arrive(bar + B_DQ_FREE);
+        if (leader) bulk_wait_group_read<0>();  // the previous bulk copy has finished reading the tile
+        named_bar_sync(1, 128);
+        // [BM queries][D] fp32, row-major: column rr (this thread's d) of each query row
+        float* st = reinterpret_cast<float*>(stg) + rr;
+#pragma unroll
+        for (int q = 0; q < BM; ++q) st[q * D] = __uint_as_float(v[q]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader && ok) {
+          tma_reduce_add_3d(&tm_dq, stg, 0, q0, w.kvh * group + gm);
+          bulk_commit_group();
+        }
+      }
+      // epilogue of this item: dV, dK rows rr -> 16-bit -> staging ([2 boxes][128 rows][64
+      // columns], the layout of the dK / dV tensor maps) -> TMA stores (rows past N are not
+      // written).  An item without steps (masked) stores zeros.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, r & 1, ctx, 132)) && ok;
+      const bool acc = ok && w.nsteps > 0;
+      if (acc) tc_fence_after();
+      uint32_t pkk[D / 2];  // this row of dK x tau, packed
+      if (leader) bulk_wait_group_read<0>();  // the last dQ reduction has read the staging tile
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t pv[16] = {};
+        if (acc) load_acc32(lane_base, C::COL_DV + c * 32, 1.f, pv);
+        stage_row32(stg + (c >> 1) * (BN * 128), rr, c, pv);
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t pv[16] = {};
+        if (acc) load_acc32(lane_base, C::COL_DK + c * 32, scale, pv);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) pkk[c * 16 + t] = pv[t];
+      }
+      tc_fence_before();
+      mbar_arrive(bar + B_ACC_EMPTY);  // the accumulators may be overwritten
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (leader) {
+        if (ok) {
+          for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_dv, stg + b * (BN * 128), b * 64, w.k0, w.kvh);
+          bulk_commit_group();
+        }
+        bulk_wait_group_read<0>();
+      }
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t pv[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) pv[t] = pkk[c * 16 + t];
+        stage_row32(stg + (c >> 1) * (BN * 128), rr, c, pv);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (leader && ok) {
+        for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_dk, stg + b * (BN * 128), b * 64, w.k0, w.kvh);
+        bulk_commit_group();
+      }
+    }
+    if (leader) bulk_wait_group<0>();  // every reduction and store issued here has completed
+
+  } else if (warp < 8) {
+    if constexpr (C::SPLIT) {
+      // ---------------------------------------------------------------- WG0, WG1: P^T, dS^T, dQ drain
+      // (d = 64, 128 queries per step) Both warpgroups own the same 128 key rows (TMEM lane
+      // quarter warp % 4) and each takes half of every step's 32-query chunks for P^T and dS^T;
+      // after its dS^T half of step i each drains its half of the dQ partial of step i - 1 (that
+      // MMA completed before dP^T_i, which the dS^T half has just read).  WG0 also copies K_j
+      // into TMEM at the start of an item; at its end WG0 stores dV and WG1 dK.
+      constexpr bool SPLIT = C::SPLIT;
+      const int wg = warp >> 2;
+      const uint32_t lane_base = (warp & 3) * 32;
+      const int rit = (warp & 3) * 32 + lane;  // key row within the tile (and TMEM lane)
+      uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
+      const uint32_t sw = (uint32_t)(rit & 7);
+      constexpr int NCH = SPLIT ? BM / 64 : BM / 32;  // 32-query chunks a computing warpgroup takes
+      const int c0 = SPLIT ? wg * NCH : 0;
+      constexpr int DCOLS = SPLIT ? 32 : 64;  // TMEM columns of a dQ partial one thread drains
+      const int dcol0 = SPLIT ? wg * 32 : 0;
+      const bool leader = (warp == 0 && lane == 0);  // issues the dQ reductions and the stores
+      uint8_t* stg = smem + C::OFF_STG;
+      bool ok = start_ok;
+      uint32_t stg_uses = 0;  // staging-tile handshakes (dQ partials and epilogues, all items)
+      // take the staging tile: free once the previous bulk copy has read it (bounded waits on
+      // mbarriers, not named barriers, so a warp that gave up cannot leave the others waiting)
+      auto stage_begin = [&]() {
+        if (leader) {
+          bulk_wait_group_read<0>();
+          mbar_arrive(bar + B_STG_FREE);
+        }
+        return __all_sync(0xffffffffu, mbar_wait(bar + B_STG_FREE, stg_uses & 1, ctx, 141));
+      };
+      // both warpgroups have written their part: the leader may copy it out
+      auto stage_end = [&]() {
+        fence_proxy_async_smem();
+        mbar_arrive(bar + B_STG_FULL);
+        return !leader || mbar_wait(bar + B_STG_FULL, stg_uses & 1, ctx, 142);
+      };
+      // dQ partial k -> staging tile (this warpgroup's half) -> one TMA reduce-add into the fp32
+      // accumulator
+      auto drain = [&](uint32_t k, int q0, int qh) {
+        bool good = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, k & 1, ctx, 140));
+        if (!good) return false;
+        tc_fence_after();
+        uint32_t vr[DCOLS / 32][32];  // this thread's TMEM columns of the partial
+#pragma unroll
+        for (int c = 0; c < DCOLS / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + dcol0 + c * 32), vr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < DCOLS / 32; ++c) reg_fence(vr[c]);
+        const uint32_t* v = &vr[0][0];
+        tc_fence_before();
+        mbar_arrive(bar + B_DQ_FREE);
+        if (!stage_begin()) return false;
+        // [128 queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns; TMEM lane =
+        // query row (rit), columns = this thread's d (one box per 32)
+#pragma unroll
+        for (int j = 0; j < DCOLS / 4; ++j) {
+          uint8_t* bx = stg + (dcol0 / 32 + j / 8) * (BM * 128) + rit * 128;
+          *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ sw) << 4)) =
+              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        good = stage_end();
+        if (leader && good) {
+          tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
+          tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, qh);
+          bulk_commit_group();
+        }
+        ++stg_uses;
+        return good;
+      };
+      uint32_t gs = 0;  // steps processed (all items)
+      for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
+        const BwdItem w = item_at(item);
+        const int key = w.k0 + rit;
+        const bool key_ok = key < n;
+        if (wg == 0) {
+          // K_j -> TMEM: the previous item's last S^T (which read it) completed before its last step
+          ok = __all_sync(0xffffffffu, mbar_wait(bar + B_KV, r & 1, ctx, 134));
+          if (!ok) break;
+          k_to_tmem(rit, lane_base);
+          tc_fence_before();
+          mbar_arrive(bar + B_KT_READY);
+        }
+        int prev_q0 = 0, prev_qh = 0;
+        for (int i = 0, ii = 0, g = 0; ok && i < w.nsteps; ++i, ++gs, step_next(ii, g, w.nsteps_head)) {
+          const int s = gs % C::QSTAGES;
+          int gm, q0;
+          step_rows(w, i, ii, g, &gm, &q0);
+          const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
+          const float* dvec = l2v + BM;
+          // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
+          ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (gs / C::QSTAGES) & 1, ctx, 133));
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, gs & 1, ctx, 130));
+          if (!ok) break;
+          tc_fence_after();
+          // visible queries q0 + qc: qc in [mask_below, mask_above) (causal: not before this key;
+          // window: |query - key| < window, an upper bound on the query with or without causal)
+          int mask_below = causal ? key - q0 : INT32_MIN, mask_above = INT32_MAX;
+          if constexpr (MASKED) {
+            if (window > 0) {
+              mask_below = max(mask_below, key - window + 1 - q0);
+              mask_above = key + window - q0;
             }
           }
+          // P^T of this key against this half's queries, kept as packed 16-bit pairs: the same
+          // rounded values feed dV += P^T dO and dS = P o (dP - D)
+          uint32_t pk[NCH * 16];
+          {
+            uint32_t sr[NCH][32];
+#pragma unroll
+            for (int cl = 0; cl < NCH; ++cl) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + (c0 + cl) * 32), sr[cl]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int cl = 0; cl < NCH; ++cl) {
+              const int c = c0 + cl;
+              uint32_t(&r)[32] = sr[cl];
+              reg_fence(r);
+#pragma unroll
+              for (int t = 0; t < 32; t += 4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(l2v + c * 32 + t);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                float e[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int qc = c * 32 + t + u;
+                  const float x = ex2(fmaf(__uint_as_float(r[t + u]), scale_log2, -lv[u]));
+                  e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? x : 0.f;
+                }
+                pk[cl * 16 + t / 2] = pack2<BF16>(e[0], e[1]);
+                pk[cl * 16 + t / 2 + 1] = pack2<BF16>(e[2], e[3]);
+              }
+            }
+          }
+#pragma unroll
+          for (int cl = 0; cl < NCH; ++cl) {
+            uint32_t wv[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) wv[t] = pk[cl * 16 + t];
+            tmem_st16(tmem_addr(tbase, lane_base, C::COL_S + (c0 + cl) * C::CH_COLS), wv);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar + B_P_READY);
+          // dS^T = P^T o (dP^T - D); dp_full(i) also means the MMAs of step i-1 that read dS^T are done
+          ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DP_FULL, gs & 1, ctx, 131));
+          if (!ok) break;
+          tc_fence_after();
+          {
+            uint32_t dr[NCH][32];
+#pragma unroll
+            for (int cl = 0; cl < NCH; ++cl) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + (c0 + cl) * 32), dr[cl]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int cl = 0; cl < NCH; ++cl) {
+              const int c = c0 + cl;
+              uint32_t(&r)[32] = dr[cl];
+              reg_fence(r);
+              uint32_t dsk[16];
+#pragma unroll
+              for (int t = 0; t < 16; t += 2) {
+                const float4 d4 = *reinterpret_cast<const float4*>(dvec + c * 32 + 2 * t);
+                const float2 p01 = unpack2<BF16>(pk[cl * 16 + t]);
+                const float2 p23 = unpack2<BF16>(pk[cl * 16 + t + 1]);
+                dsk[t] = pack2<BF16>(p01.x * (__uint_as_float(r[2 * t]) - d4.x),
+                                     p01.y * (__uint_as_float(r[2 * t + 1]) - d4.y));
+                dsk[t + 1] = pack2<BF16>(p23.x * (__uint_as_float(r[2 * t + 2]) - d4.z),
+                                         p23.y * (__uint_as_float(r[2 * t + 3]) - d4.w));
+              }
+              // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
+              uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
+                *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
+                    make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
+              }
+              // and packed into TMEM over this chunk's dP^T columns, already read (A operand of
+              // dK += dS^T Q)
+              tmem_st16(tmem_addr(tbase, lane_base, C::COL_DP + c * C::CH_COLS), dsk);
+            }
+          }
+          fence_proxy_async_smem();
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar + B_DS_READY);
+          if (i > 0 && !(ok = drain(gs - 1, prev_q0, prev_qh))) break;
+          prev_q0 = q0;
+          prev_qh = w.kvh * group + gm;
         }
-      } else if (wg == 0 && ok && nsteps == 0 && key_ok) {
-        // no query meets this key tile: zero gradients (not reachable for square causal masks)
-        uint32_t pk[16] = {};
-        for (int c = 0; c < D / 32; ++c) {
-          store_row16<D>(dk_out, (int64_t)kvh * n + key, pk, c);
-          store_row16<D>(dv_out, (int64_t)kvh * n + key, pk, c);
+        if (ok && w.nsteps > 0) ok = drain(gs - 1, prev_q0, prev_qh);
+        if (!ok) break;
+        // epilogue of this item: WG0 dV, WG1 dK (x tau), each a [128 rows][64 columns] 16-bit
+        // box of the staging tile, then TMA stores (rows past N are not written).  An item
+        // without steps (masked) stores zeros.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, r & 1, ctx, 132));
+        if (!ok) break;
+        uint32_t pa[2][16] = {};
+        if (w.nsteps > 0) {
+          tc_fence_after();
+          load_acc32(lane_base, (wg ? C::COL_DK : C::COL_DV), wg ? scale : 1.f, pa[0]);
+          load_acc32(lane_base, (wg ? C::COL_DK : C::COL_DV) + 32, wg ? scale : 1.f, pa[1]);
         }
+        tc_fence_before();
+        mbar_arrive(bar + B_ACC_EMPTY);  // the accumulators may be overwritten
+        if (!(ok = stage_begin())) break;
+        stage_row32(stg + wg * (BN * 128), rit, 0, pa[0]);
+        stage_row32(stg + wg * (BN * 128), rit, 1, pa[1]);
+        ok = stage_end();
+        if (leader && ok) {
+          tma_store_3d(&tm_dv, stg, 0, w.k0, w.kvh);
+          tma_store_3d(&tm_dk, stg + BN * 128, 0, w.k0, w.kvh);
+          bulk_commit_group();
+        }
+        ++stg_uses;
       }
-
+      if (leader) bulk_wait_group<0>();  // every reduction and store issued here has completed
     }
   }
   tc_fence_before();
@@ -889,18 +1003,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  if constexpr (!MASKED) {
+    // this CTA draws no more tickets; the last one to get here empties the queue for the next
+    // launch (every CTA has drawn its last ticket by then)
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+        atomicExch(sched, 0u);
+        atomicExch(sched + 1, 0u);
+      }
+    }
+  }
 }
 
 template <int D, bool BF16, bool MASKED>
 cudaError_t launch_bwd_d(const BwdArgs& a) {
   using C = BwdCfg<D>;
   const int npad = (int)padded_rows(a.n);
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   const int bh_kv = a.bh / a.group;
   if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, C::BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) ||
       !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN) ||
       !make_tmap_16bit_3d(&tdo, a.dout, BF16, D, a.n, a.bh, C::BM) ||
-      !make_tmap_f32_3d(&tdq, a.dq_acc, D, npad, a.bh, C::DQT ? D : 32, C::BM, !C::DQT))
+      !make_tmap_f32_3d(&tdq, a.dq_acc, D, npad, a.bh, C::DQT ? D : 32, C::BM, !C::DQT) ||
+      !make_tmap_16bit_3d(&tdk, a.dk, BF16, D, a.n, bh_kv, BN) || !make_tmap_16bit_3d(&tdv, a.dv, BF16, D, a.n, bh_kv, BN))
     return cudaErrorInvalidValue;
   auto kern = bwd_tc_kernel<D, BF16, MASKED>;
   const int nblk = (a.n + 127) / 128;
@@ -909,10 +1035,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int ktiles = (a.n + BN - 1) / BN;
-  kern<<<(unsigned)(bh_kv * ktiles), C::THREADS, smem, a.stream>>>(tq, tk, tv, tdo, tdq, a.lse2, a.delta, a.dk, a.dv,
-                                                                   a.n, npad, bh_kv, ktiles, a.scale, a.causal, a.group,
-                                                                   a.err, a.window, a.block_mask, a.mask_heads,
-                                                                   a.heads);
+  const int64_t items = (int64_t)bh_kv * ktiles;
+  const int64_t grid = MASKED ? items : std::min<int64_t>(items, device_sm_count());
+  if (!MASKED && !a.sched) return cudaErrorInvalidValue;
+  kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a.lse2, a.delta, a.n, npad,
+                                                       bh_kv, ktiles, a.scale, a.causal, a.group, a.err, a.window,
+                                                       a.block_mask, a.mask_heads, a.heads, a.sched);
   return cudaGetLastError();
 }
 

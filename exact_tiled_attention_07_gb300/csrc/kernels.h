@@ -53,6 +53,7 @@ struct BwdArgs {
   float* delta;
   float* lse2;
   float* dq_acc;
+  unsigned* sched = nullptr;  // [2] work-item queue of the tensor-core backward: next ticket, CTAs done
   int bh;
   int n;
   int d;

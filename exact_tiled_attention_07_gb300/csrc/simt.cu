@@ -306,7 +306,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) bwd_pre(const T* __restrict__ O, const T* __restrict__ dO,
                                                const float* __restrict__ lse, float* __restrict__ delta,
                                                float* __restrict__ lse2, float* __restrict__ dq_acc, int n, int npad,
-                                               int d, int64_t total_rows) {
+                                               int d, int64_t total_rows, unsigned* __restrict__ sched) {
+  if (sched && blockIdx.x == 0 && threadIdx.x < 2) sched[threadIdx.x] = 0u;  // the backward's item queue
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= total_rows) return;
@@ -346,7 +347,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) bwd_pre_vec(const T* __restrict__ O, const T* __restrict__ dO,
                                                    const float* __restrict__ lse, float* __restrict__ delta,
                                                    float* __restrict__ lse2, float* __restrict__ dq_acc, int n,
-                                                   int npad, int d, int64_t total_rows) {
+                                                   int npad, int d, int64_t total_rows, unsigned* __restrict__ sched) {
+  if (sched && blockIdx.x == 0 && threadIdx.x < 2) sched[threadIdx.x] = 0u;  // the backward's item queue
   const int tpr = d / 8;  // threads per row: 8, 16 or 32 (power of two)
   const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t grow = gt / tpr;
@@ -436,12 +438,12 @@ cudaError_t pre_t(const BwdArgs& a) {
   if (sizeof(T) == 2 && (a.d == 64 || a.d == 128 || a.d == 256)) {
     const int64_t threads = rows * (a.d / 8);
     bwd_pre_vec<T><<<(unsigned)((threads + 255) / 256), 256, 0, a.stream>>>(
-        (const T*)a.o, (const T*)a.dout, a.lse, a.delta, a.lse2, a.dq_acc, a.n, npad, a.d, rows);
+        (const T*)a.o, (const T*)a.dout, a.lse, a.delta, a.lse2, a.dq_acc, a.n, npad, a.d, rows, a.sched);
     return cudaGetLastError();
   }
   const int64_t blocks = (rows * 32 + 255) / 256;
   bwd_pre<T><<<(unsigned)blocks, 256, 0, a.stream>>>((const T*)a.o, (const T*)a.dout, a.lse, a.delta, a.lse2,
-                                                     a.dq_acc, a.n, npad, a.d, rows);
+                                                     a.dq_acc, a.n, npad, a.d, rows, a.sched);
   return cudaGetLastError();
 }
 

@@ -85,7 +85,8 @@ FA_API fa_status fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O
 
 /*
  * Bytes of device workspace fa_bwd needs: per head, with Np = N rounded up to 128,
- * D [Np] fp32, L*log2(e) [Np] fp32 and an fp32 dQ accumulator [Np][d].
+ * D [Np] fp32, L*log2(e) [Np] fp32 and an fp32 dQ accumulator [Np][d]; then 256 bytes for
+ * the counters of the tensor-core backward's work-item queue.
  * Returns 0 for invalid sizes.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
@@ -117,7 +118,7 @@ FA_API fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const v
 /*
  * Stage 1 of fa_bwd: D_i = sum_k dO_ik O_ik (the N x d identity that replaces the N x N
  * row sum of P o dP, "Lecture 8" §5.4), L_i log2(e) for the exp2-domain recomputation,
- * and a zeroed dQ accumulator, all into `workspace`.
+ * a zeroed dQ accumulator and zeroed work-queue counters, all into `workspace`.
  */
 FA_API fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* L, void* workspace, size_t workspace_bytes,
                             int B, int H, int N, int d, fa_dtype dtype, void* stream);
@@ -125,6 +126,9 @@ FA_API fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* L
 /*
  * Stage 2 of fa_bwd: recompute S and P block by block and produce dK, dV (written) and
  * the unscaled dQ sum (accumulated in `workspace`). Needs stage 1 on the same workspace.
+ * The tensor-core kernel's CTAs draw work items from the queue counters, which stage 1 set
+ * to zero and which this stage leaves at zero when it completes; two calls must not run at
+ * the same time on one workspace.
  */
 FA_API fa_status fa_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,

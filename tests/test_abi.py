@@ -52,10 +52,11 @@ def test_status_strings(lib):
 def test_workspace_size_is_linear_in_n(lib):
     lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
     ws = lambda b, h, n, d: lib.fa_bwd_workspace_size(b, h, n, d)
-    # D + L*log2e + fp32 dQ accumulator over N rounded up to 128: nothing N x N
-    assert ws(1, 1, 128, 64) == 128 * 4 * 66
-    assert ws(2, 3, 129, 128) == 6 * 256 * 4 * 130
-    assert ws(8, 16, 4096, 128) == 8 * 16 * 4096 * 4 * 130
+    # D + L*log2e + fp32 dQ accumulator over N rounded up to 128, then 256 bytes of queue
+    # counters: nothing N x N
+    assert ws(1, 1, 128, 64) == 128 * 4 * 66 + 256
+    assert ws(2, 3, 129, 128) == 6 * 256 * 4 * 130 + 256
+    assert ws(8, 16, 4096, 128) == 8 * 16 * 4096 * 4 * 130 + 256
     assert ws(1, 8, 65536, 64) < 65536 * 65536  # vs. one N x N byte matrix
     assert ws(1, 1, 16, 0) == 0 and ws(1, 1, 16, 300) == 0
 
