@@ -407,13 +407,24 @@ def run_gpu(args, w: Workload):
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     d2h = sum(t.numel() * t.element_size() for t in outs)
     ins = [(dev[k_], pinned[k_]) for k_ in pinned]
+    if not w.fwd_only:
+        # one C-ABI call over the host buffers: chunks of heads copied in, computed and copied
+        # out on the library's streams, overlapping the copies of one chunk with its neighbours'
+        # computation
+        ws_host = torch.empty(binding.fa_fwd_bwd_host_workspace_size(w.B, w.H, w.H, w.N, w.d, q.dtype,
+                                                                     args.e2e_chunk),
+                              dtype=torch.uint8, device=device)
 
-    def e2e_step():
-        for d_, h_ in ins:
-            d_.copy_(h_, non_blocking=True)
-        step()
-        for h_, d_ in zip(host_out, outs):
-            h_.copy_(d_, non_blocking=True)
+        def e2e_step():
+            binding.fa_fwd_bwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["do"], *host_out, ws_host, scale,
+                                    causal, args.e2e_chunk, stream)
+    else:
+        def e2e_step():
+            for d_, h_ in ins:
+                d_.copy_(h_, non_blocking=True)
+            step()
+            for h_, d_ in zip(host_out, outs):
+                h_.copy_(d_, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -429,7 +440,9 @@ def run_gpu(args, w: Workload):
     e2e_ms = e_s.elapsed_time(e_e) / args.steps
     e2e_ms = max_over_ranks(e2e_ms, dist, device)
     e2e = {"value": aggregate_tflops(flops_rank, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "call": "fa_fwd_bwd_host" if not w.fwd_only else "copies + fa_fwd",
+           "chunk_kv_heads": args.e2e_chunk if not w.fwd_only else None}
 
     # ---------------- per-pass figures, including the non-causal variant of the same shape
     targets = None
@@ -570,6 +583,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-targets", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
+    ap.add_argument("--e2e-chunk", type=int, default=0,
+                    help="key/value heads per chunk of the end-to-end host-buffer call (0: automatic)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]

@@ -21,6 +21,7 @@ __all__ = [
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
     "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait",
+    "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size",
     "attention_forward", "attention_backward", "attention_decode",
     "attention_forward_fp8", "quantize_fp8", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
@@ -36,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
     "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait",
+    "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size",
 )
 
 _lib = None
@@ -83,6 +85,9 @@ def load_library():
         lib.fa_bwd_masked.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, vp, i, i, vp]
         lib.fa_fwd_fp8.argtypes = [vp] * 8 + [i, i, i, i, f, i, i, vp]
         lib.fa_selftest_bounded_wait.argtypes = [i, i, vp]
+        lib.fa_fwd_bwd_host_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        lib.fa_fwd_bwd_host_workspace_size.restype = sz
+        lib.fa_fwd_bwd_host.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
         lib.fa_uses_tensor_cores.argtypes = [i, i, i]
@@ -91,7 +96,7 @@ def load_library():
         lib.fa_last_error_message.argtypes = []
         lib.fa_last_error_message.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_quantize_fp8", "fa_fwd_fp8",
-                     "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait",
+                     "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait", "fa_fwd_bwd_host",
                      "fa_bwd_noalloc", "fa_bwd_preprocess",
                      "fa_bwd_main", "fa_bwd_dq_convert",
                      "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
@@ -220,6 +225,35 @@ def fa_bwd_noalloc(Q, K, V, O, dO, L, dQ, dK, dV, scale, causal, stream=None):
     _same(Q, K, V, O, dO, dQ, dK, dV)
     _check(load_library().fa_bwd_noalloc(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV), B, H, N,
                                          d, float(scale), int(bool(causal)), _dt(Q), _stream(stream)))
+
+
+def fa_fwd_bwd_host_workspace_size(B, H, Hkv, N, d, dtype, chunk=0) -> int:
+    return int(load_library().fa_fwd_bwd_host_workspace_size(B, H, Hkv, N, d, DTYPE_CODES[dtype], int(chunk)))
+
+
+def fa_fwd_bwd_host(Q, K, V, dO, O, L, dQ, dK, dV, workspace, scale, causal, chunk=0, stream=None):
+    """Forward + backward with CPU tensors in and out (page-locked for the copies to overlap) and
+    a device workspace of fa_fwd_bwd_host_workspace_size bytes."""
+    B, H, N, d = _shape4(Q)
+    Bk, Hkv, Nk, dk = _shape4(K)
+    if (Bk, Nk, dk) != (B, N, d) or Hkv < 1 or H % Hkv:
+        raise ValueError("K must be [B, Hkv, N, d] with H a multiple of Hkv")
+    for t in (Q, K, V, dO, O, L, dQ, dK, dV):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("fa_fwd_bwd_host takes contiguous host (CPU) tensors")
+    for t in (V, dK, dV):
+        if t.shape != K.shape or t.dtype != Q.dtype:
+            raise ValueError("V, dK, dV must be [B, Hkv, N, d] of Q's dtype")
+    for t in (dO, O, dQ):
+        if t.shape != Q.shape or t.dtype != Q.dtype:
+            raise ValueError("dO, O, dQ must be [B, H, N, d] of Q's dtype")
+    if L.dtype != torch.float32 or L.numel() != B * H * N:
+        raise ValueError("L must be an fp32 tensor of B*H*N elements")
+    if workspace.device.type != "cuda":
+        raise ValueError("the workspace is device memory")
+    _check(load_library().fa_fwd_bwd_host(_p(Q), _p(K), _p(V), _p(dO), _p(O), _p(L), _p(dQ), _p(dK), _p(dV),
+                                          _p(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N,
+                                          d, float(scale), int(bool(causal)), _dt(Q), int(chunk), _stream(stream)))
 
 
 def fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d, splits=0) -> int:

@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["api.cu", "simt.cu", "fwd_tc.cu", "bwd_tc.cu", "noalloc.cu", "decode.cu", "decode_tc.cu", "fp8.cu", "selftest.cu"]
+SOURCES = ["api.cu", "simt.cu", "fwd_tc.cu", "bwd_tc.cu", "noalloc.cu", "decode.cu", "decode_tc.cu", "fp8.cu", "selftest.cu",
+           "pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           "--expt-relaxed-constexpr"]

@@ -165,6 +165,30 @@ FA_API fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, con
                                 int causal, fa_dtype dtype, void* stream);
 
 /*
+ * Forward and backward with every tensor in HOST memory (Q, K, V, dO in; O, L, dQ, dK, dV
+ * out; the layouts of fa_fwd_gqa / fa_bwd_gqa): the computation of fa_fwd_gqa followed by
+ * fa_bwd_gqa, with the copies between host and device done here. Attention heads are
+ * independent ("Lecture 8" §5.1: one N x d problem per head), so the batch is cut into chunks
+ * of key/value heads (each with its H / Hkv query heads) that are copied in, computed and
+ * copied out on three internal streams: the copies of one chunk overlap the computation of
+ * its neighbours. (The pages have no counterpart of this entry point; it exists for callers
+ * whose data is in host memory.)
+ *   chunk      key/value heads per chunk (counted over B x Hkv); 0 chooses about eight chunks
+ *   workspace  device scratch of fa_fwd_bwd_host_workspace_size(...) bytes for the same
+ *              arguments, 256-byte aligned, owned by the caller (two slots of chunk buffers)
+ *   stream     the call is ordered after earlier work on `stream`, and work enqueued on
+ *              `stream` afterwards runs after its last copy out; the host does not wait.
+ *              Host buffers must stay valid (and, for the copies to overlap, page-locked)
+ *              until then.
+ * Calls from several host threads on one device are serialised on the internal streams.
+ */
+FA_API size_t fa_fwd_bwd_host_workspace_size(int B, int H, int Hkv, int N, int d, fa_dtype dtype, int chunk);
+FA_API fa_status fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const void* dO, void* O, float* L,
+                                 void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H,
+                                 int Hkv, int N, int d, float scale, int causal, fa_dtype dtype, int chunk,
+                                 void* stream);
+
+/*
  * Decode attention over a key/value cache with the cache split across thread blocks
  * ("Lecture 8" §8.2: the cache is cut into pieces processed in parallel and the partial
  * results are combined with the online-softmax merge of Exercise 3).

@@ -153,3 +153,36 @@ def test_selftest_timeout_range(lib):
     lib.fa_selftest_bounded_wait.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     assert lib.fa_selftest_bounded_wait(0, 0, None) == 1
     assert lib.fa_selftest_bounded_wait(5000, 0, None) == 1
+
+
+def test_host_pipeline_workspace_size_host_rules(lib):
+    f = lib.fa_fwd_bwd_host_workspace_size
+    f.argtypes = [ctypes.c_int] * 7
+    f.restype = ctypes.c_size_t
+    bf16 = 0
+    # invalid shapes, dtype or chunk: 0; nothing to do: 0
+    assert f(1, 4, 3, 128, 64, bf16, 0) == 0
+    assert f(1, 4, 2, 128, 0, bf16, 0) == 0
+    assert f(1, 4, 2, 128, 64, 7, 0) == 0
+    assert f(1, 4, 2, 128, 64, bf16, -1) == 0
+    assert f(0, 4, 2, 128, 64, bf16, 0) == 0
+    # two slots; one key/value head (2 query heads) of N = 128, d = 64, bf16 per slot:
+    # Q, dO, O, dQ 2 x 16 KB each; K, V, dK, dV 16 KB each; L 1 KB; backward workspace
+    one = f(1, 4, 2, 128, 64, bf16, 1)
+    ws = lib.fa_bwd_workspace_size
+    ws.argtypes = [ctypes.c_int] * 4
+    ws.restype = ctypes.c_size_t
+    assert one == 2 * (4 * 32768 + 4 * 16384 + 1024 + ws(1, 2, 128, 64))
+    # chunks larger than the problem are clipped; the automatic choice is about eight chunks
+    assert f(1, 4, 2, 128, 64, bf16, 5) == f(1, 4, 2, 128, 64, bf16, 2)
+    assert f(8, 16, 16, 4096, 128, bf16, 0) == f(8, 16, 16, 4096, 128, bf16, 16)
+
+
+def test_host_pipeline_rejects_null_host_pointers_before_any_cuda_call(lib):
+    f = lib.fa_fwd_bwd_host
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp] * 10 + [ctypes.c_size_t, i, i, i, i, i, ctypes.c_float, i, i, i, vp]
+    f.restype = ctypes.c_int
+    assert f(*([None] * 10), 0, 1, 2, 2, 128, 64, 0.125, 1, 0, 0, None) != 0
+    lib.fa_last_error_message.restype = ctypes.c_char_p
+    assert b"null" in lib.fa_last_error_message()
