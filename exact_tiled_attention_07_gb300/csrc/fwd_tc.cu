@@ -38,6 +38,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include "kernels.h"
@@ -70,8 +71,9 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = NQ * Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + STAGES * TILE_BYTES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 3;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 3 + 4;
+  // after the barriers: TMEM base, abort flag, the two work-item slots
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 32;
   // masked variant: the CTA's key-tile list after the barriers (4 ints, then uint16 tile
   // indices and uint8 visibility flags, nb rounded up to 16 entries each)
   static constexpr int OFF_LIST = SMEM;
@@ -89,6 +91,8 @@ struct FwdSmemBars {
   uint64_t* drain;    // [1]
   uint64_t* o_empty;  // [2] the softmax has read O_q of its last item
   uint64_t* q_empty;  // [1] every S = Q K^T of the last item is done (Q may be overwritten)
+  uint64_t* item_full;   // [2] the producer published a work item in this slot (queue mode)
+  uint64_t* item_empty;  // [2] every consumer warp has read it
 };
 
 // Masked variant (block mask and/or window, "Lecture 8" §5.7 block-sparse attention): one warp
@@ -97,13 +101,13 @@ struct FwdSmemBars {
 // score in it) with a flag per query tile; the producer, the MMA warp and the softmax walk
 // that list.  A query tile processes every listed tile up to its own last visible one, the
 // ones it cannot see fully masked, so both tiles keep the same ping-pong schedule.
-template <int D, bool BF16, bool MASKED>
+template <int D, bool BF16, bool MASKED, bool QUEUE>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, float* __restrict__ lse, int n,
                   int bh_count, int tiles_per_head, float scale_log2, int causal, int group, unsigned long long* err,
                   unsigned long long* counter, int window, const uint8_t* __restrict__ block_mask, int mask_heads,
-                  int heads, int snake) {
+                  int heads, int snake, unsigned* __restrict__ sched) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -121,8 +125,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   B.drain = B.pv_done + 1;
   B.o_empty = B.drain + 1;
   B.q_empty = B.o_empty + 2;
+  B.item_full = B.q_empty + 1;
+  B.item_empty = B.item_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
+  // queue mode: items come from a ticket counter (sched) through the producer (never masked)
+  constexpr bool queue = QUEUE && !MASKED;
   const ErrCtx ctx{err, abort_flag};
 
   // work items: head-major (CTAs running together share K/V in L2); causal: heaviest (last)
@@ -234,6 +243,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     mbar_init(B.o_empty + 0, 128);
     mbar_init(B.o_empty + 1, 128);
     mbar_init(B.q_empty, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(B.item_full + t, 1);
+      mbar_init(B.item_empty + t, C::SOFTMAX_WARPS + 1);  // the softmax warps and the MMA warp
+    }
     fence_barrier_init();
   }
   if (warp == C::MMA_WARP) {
@@ -253,6 +266,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int g = (int)grid_dim_x(), c = (int)cta_id_x();
     const int64_t item = (int64_t)r * g + ((snake && (r & 1)) ? (g - 1 - c) : c);
     return item < total_items ? (int)item : -1;
+  };
+  // this CTA's r-th item for a consumer warp: queue mode reads the producer's slot r % 2 (every
+  // consumer warp reads every slot once; `good` turns false, and the item -1, when the bounded
+  // wait ran out), otherwise the static order above
+  auto next_item = [&](int r, bool& good) {
+    if constexpr (!queue) return nth_item(r);
+    const int t = r & 1;
+    good = __all_sync(0xffffffffu, mbar_wait(B.item_full + t, (uint32_t)(r >> 1) & 1, ctx, 50)) && good;
+    const int item = good ? item_slot[t] : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.item_empty + t);
+    return item;
   };
   // the item with, for masked launches, the key-tile counts of its list
   auto item_at = [&](int item) {
@@ -275,7 +300,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       uint32_t ring_pos = 0;  // ring loads issued so far (all items)
       int q_loads = 0;
       bool ok = true;
-      for (int r = 0, item = nth_item(0); ok && item >= 0; item = nth_item(++r)) {
+      // the r-th item: queue mode draws a ticket (items are numbered heaviest first) and publishes
+      // it, or -1 once the queue is empty, when every reader of the slot's previous item has it
+      auto draw = [&](int r) {
+        if constexpr (!queue) return nth_item(r);
+        if (r >= 2 && !(ok = mbar_wait(B.item_empty + (r & 1), (uint32_t)((r - 2) >> 1) & 1, ctx, 14))) return -1;
+        const unsigned ticket = atomicAdd(sched, 1u);
+        const int item = ticket < (unsigned)total_items ? (int)ticket : -1;
+        item_slot[r & 1] = item;
+        mbar_arrive(B.item_full + (r & 1));
+        return item;
+      };
+      for (int r = 0, item = draw(0); ok && item >= 0; item = draw(++r)) {
         const Item w = item_at(item);
         const int nmax = max(w.nq[0], w.nq[1]);
         // Q of this item once the previous item's S = Q K^T are done
@@ -365,7 +401,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // the first P V of query tile q in an item overwrites O_q: the softmax must have read it
       auto o_free = [&](int q) { return oq[q] == 0 || wait(B.o_empty + q, (oq[q] - 1) & 1, 26 + q); };
       bool ok = true;
-      for (int r = 0, item = nth_item(0); ok && item >= 0; item = nth_item(++r)) {
+      for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
         const Item w = item_at(item);
         const int* nq = w.nq;
         const int nmax = max(nq[0], nq[1]);
@@ -466,7 +502,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     int tq = 0;  // key tiles this query tile processed (all items): S / P phases
     int oq = 0;  // items with a result: O phases
     bool ok = start_ok;
-    for (int r = 0, item = nth_item(0); ok && item >= 0; item = nth_item(++r)) {
+    for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
       const Item w = item_at(item);
       const int head = w.head;
       const int row = w.qrow0 + q * BM + rit;
@@ -622,10 +658,74 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  if (queue && threadIdx.x == 0) {  // (queue: a compile-time constant)
+    // this CTA draws no more tickets; the last one to get here empties the queue for the next
+    // launch that uses it (every CTA has drawn its last ticket by then)
+    __threadfence();
+    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(sched, 0u);
+      atomicExch(sched + 1, 0u);
+    }
+  }
 }
 
 // Largest per-CTA work (key tiles) of a persistent causal grid of g CTAs over the items, in grid
 // order or snake order: the same item order and key-tile counts as the kernel.
+// Work-item queues of the persistent forward (the call has no workspace): a few pairs of
+// counters (next ticket, CTAs done) in device memory that the library owns.  A launch takes a
+// slot that no earlier launch still uses: the event recorded on the stream right after a slot's
+// last launch has completed, so that launch has finished and its last CTA has set the counters
+// back to zero.  A stream being captured into a graph, or all slots busy, gets no slot and the
+// static order instead.
+constexpr int kQueueSlots = 32;
+constexpr int kMaxQueueDevices = 64;
+__device__ unsigned g_fwd_queue[kQueueSlots][2];
+
+struct QueuePool {
+  unsigned* base = nullptr;
+  cudaEvent_t done[kQueueSlots] = {};
+  bool used[kQueueSlots] = {};    // a launch was recorded on done[i]
+  bool broken[kQueueSlots] = {};  // recording failed: never reused
+  int next = 0;
+};
+QueuePool g_qpool[kMaxQueueDevices];
+std::mutex g_qpool_mu;  // held from choosing a slot until its launch is recorded
+
+// A free slot of the current device's pool (its index; *counters its device address), or -1.
+int acquire_queue_slot(cudaStream_t stream, QueuePool** pool, unsigned** counters) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxQueueDevices) return -1;
+  QueuePool& p = g_qpool[dev];
+  if (!p.base) {
+    void* b = nullptr;
+    if (cudaGetSymbolAddress(&b, g_fwd_queue) != cudaSuccess || !b) return -1;
+    p.base = static_cast<unsigned*>(b);
+  }
+  for (int t = 0; t < kQueueSlots; ++t) {
+    const int i = (p.next + t) % kQueueSlots;
+    if (p.broken[i]) continue;
+    if (!p.done[i] && cudaEventCreateWithFlags(&p.done[i], cudaEventDisableTiming) != cudaSuccess) {
+      p.done[i] = nullptr;
+      return -1;
+    }
+    if (p.used[i]) {
+      const cudaError_t q = cudaEventQuery(p.done[i]);
+      if (q == cudaErrorNotReady) {
+        if (cudaPeekAtLastError() == cudaErrorNotReady) (void)cudaGetLastError();
+        continue;
+      }
+      if (q != cudaSuccess) return -1;
+    }
+    p.next = (i + 1) % kQueueSlots;
+    *pool = &p;
+    *counters = p.base + 2 * i;
+    return i;
+  }
+  return -1;
+}
+
 int64_t max_cta_tiles(int bh, int tiles_per_head, int n, int nq_tiles, int g, bool snake) {
   std::vector<int64_t> load(g, 0);
   const int64_t total = (int64_t)bh * tiles_per_head;
@@ -653,12 +753,9 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
   if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) ||
       !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN))
     return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<D, BF16, MASKED>;
   const int nblocks = (a.n + BN - 1) / BN;
   const int smem = C::SMEM + (MASKED ? C::list_bytes(nblocks) : 0);
   if (smem > 232448) return cudaErrorInvalidValue;  // key-tile list too long for shared memory
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
   const float scale_log2 = a.scale * 1.4426950408889634f;
   // one CTA per SM walking the items; masked launches keep one item per CTA (its tile list
@@ -670,10 +767,34 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
                          max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, false))
                         ? 1
                         : 0;
+  // with more items than CTAs: the queue when a slot is free (CTAs that finish early take more
+  // items, whatever the cause), else the static order
+  std::unique_lock<std::mutex> lk(g_qpool_mu, std::defer_lock);
+  QueuePool* pool = nullptr;
+  unsigned* sched = nullptr;
+  int slot = -1;
+  if (!MASKED && grid < items) {
+    lk.lock();
+    slot = acquire_queue_slot(a.stream, &pool, &sched);
+  }
+  auto kern = fwd_tc_kernel<D, BF16, MASKED, false>;
+  if constexpr (!MASKED) {
+    if (slot >= 0) kern = fwd_tc_kernel<D, BF16, false, true>;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
-                                                                 a.causal, a.group, a.err, a.counter, a.window,
-                                                                 a.block_mask, a.mask_heads, a.heads, snake);
-  return cudaGetLastError();
+                                                       a.causal, a.group, a.err, a.counter, a.window, a.block_mask,
+                                                       a.mask_heads, a.heads, snake, slot >= 0 ? sched : nullptr);
+  e = cudaGetLastError();
+  if (slot >= 0 && e == cudaSuccess) {
+    e = cudaEventRecord(pool->done[slot], a.stream);
+    if (e == cudaSuccess)
+      pool->used[slot] = true;
+    else
+      pool->broken[slot] = true;  // the launch may still run: never hand this slot out again
+  }
+  return e;
 }
 
 template <int D, bool BF16>

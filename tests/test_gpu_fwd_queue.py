@@ -1,0 +1,83 @@
+"""The persistent forward's work-item queues (a library-owned pool of counter slots).
+
+A launch takes a slot only once the previous launch on it has finished; with every slot busy,
+or on a stream being captured into a CUDA graph, it runs the static order instead.  Whichever
+path runs, each item is computed the same way, so O and L equal a reference launch bit for bit.
+"""
+
+import pytest
+
+from exact_tiled_attention_07_gb300.inputs import Workload, make_inputs
+from helpers import to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_tiled_attention_07_gb300 import binding, build
+
+    build.build()
+    return binding
+
+
+@pytest.fixture(scope="module")
+def problem(fa):
+    w = Workload("queue", 2, 8, 1536, 128, "bf16", True, "normal", 9700)
+    x = make_inputs(w, with_do=False)
+    dev = {key: to_device(val, w.dtype) for key, val in x.items()}
+    o, lse = fa.attention_forward(dev["q"], dev["k"], dev["v"], causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    return w, dev, o, lse
+
+
+def _launch(fa, w, dev):
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty(dev["q"].shape[:3], dtype=torch.float32, device="cuda")
+    fa.fa_fwd(dev["q"], dev["k"], dev["v"], o, lse, w.scale, True)
+    return o, lse
+
+
+def test_more_launches_in_flight_than_queue_slots(fa, problem):
+    w, dev, o_ref, l_ref = problem
+    torch.cuda._sleep(50_000_000)  # holds the stream, so the launches below are all still pending
+    outs = [_launch(fa, w, dev) for _ in range(40)]  # more than the 32 slots: the rest run static
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    for o, lse in outs:
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_launches_on_two_streams_at_once(fa, problem):
+    w, dev, o_ref, l_ref = problem
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for _ in range(6):
+        for s in streams:
+            with torch.cuda.stream(s):
+                outs.append(_launch(fa, w, dev))
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    for o, lse in outs:
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_forward_captured_in_a_cuda_graph(fa, problem):
+    w, dev, o_ref, l_ref = problem
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty(dev["q"].shape[:3], dtype=torch.float32, device="cuda")
+    fa.fa_fwd(dev["q"], dev["k"], dev["v"], o, lse, w.scale, True)  # warm up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.fa_fwd(dev["q"], dev["k"], dev["v"], o, lse, w.scale, True)
+    o.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
