@@ -446,7 +446,10 @@ fa_status fa_quantize_fp8(const void* X, void* X8, float* scales, int B, int H, 
   if (d != 64 && d != 128 && d != 256)
     return fail(FA_ERR_UNSUPPORTED, "fa_quantize_fp8 supports d in {64, 128, 256}, got %d", d);
   if ((st = check_ptrs({X, X8, scales}, "fa_quantize_fp8")) != FA_OK) return st;
+  DeviceSyms syms;
+  if ((st = device_syms(&syms)) != FA_OK) return st;
   QuantArgs a{X, X8, scales, B * H, N, d, (int)dtype, static_cast<cudaStream_t>(stream)};
+  a.err = syms.err;
   return launched(launch_quantize_fp8(a), "fa_quantize_fp8");
 }
 

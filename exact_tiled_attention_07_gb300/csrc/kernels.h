@@ -107,6 +107,7 @@ struct QuantArgs {
   float* scales;
   int bh, n, d, dtype;
   cudaStream_t stream;
+  unsigned long long* err = nullptr;  // device error word (bounded waits of the streaming kernel)
 };
 cudaError_t launch_quantize_fp8(const QuantArgs& a);
 

@@ -67,6 +67,39 @@ def test_quantize_all_zero_block_and_saturation(fa):
     assert int(x8[0, 0, 255, 127].item()) == 0x7E
 
 
+def test_quantize_quotients_at_and_beside_e4m3_midpoints(fa):
+    """Quotients x / s on, and up to 6 fp32 ulps either side of, every midpoint between two
+    E4M3 values (where the rounding decision flips, including the subnormal range), with a scale
+    that is not a power of two: the codes must still be those of the correctly rounded fp32
+    quotient, bit for bit."""
+    amax = np.float32(300.7)
+    s = np.float32(amax / np.float32(F8.E4M3_MAX))  # the scale this block's maximum gives
+    vals = F8.e4m3_values()
+    mids = (vals[:-1] + vals[1:]) / 2
+    xs = []
+    for m in mids:
+        x0 = np.float32(np.float64(m) * np.float64(s))
+        lo = hi = x0
+        xs.append(x0)
+        for _ in range(6):
+            lo = np.nextafter(lo, np.float32(-np.inf), dtype=np.float32)
+            hi = np.nextafter(hi, np.float32(np.inf), dtype=np.float32)
+            xs.extend([lo, hi])
+    xs = np.array(xs, dtype=np.float32)
+    assert np.abs(xs).max() < amax
+    block = np.zeros(128 * 128, dtype=np.float32)
+    block[0] = amax
+    block[1:1 + xs.size] = xs
+    block[1 + xs.size:1 + 2 * xs.size] = -xs
+    x = block.reshape(1, 1, 128, 128)
+    codes, scales = F8.quantize_blocks(x)
+    assert scales[0, 0, 0] == s
+    x8, sc = fa.quantize_fp8(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert sc[0, 0, 0].item() == s
+    np.testing.assert_array_equal(x8.cpu().numpy(), _codes_to_bytes(codes).numpy())
+
+
 def _fp8_case(b, h, n, seed, spread=True):
     q, k, v = (_draw((b, h, n, 128), seed + i, spread) for i in range(3))
     qc, qs = F8.quantize_blocks(q)
