@@ -310,18 +310,23 @@ struct Fp8Cfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = NQ * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_RING + STAGES * TILE_BYTES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 1;
-  static constexpr int OFF_RED = OFF_BAR + NBAR * 8 + 16;  // 8 floats: per-warp partial maxima
-  static constexpr int SMEM = OFF_RED + 8 * 4;
+  // q_full, kv_full/empty ring, s/p/o_full [2] each, drain, o_empty [2], q_empty, item_full/empty [2]
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 1 + 2 + 1 + 4;
+  static constexpr int OFF_RED = OFF_BAR + NBAR * 8 + 32;  // [2][8] floats: per-warp partial maxima
+  static constexpr int SMEM = OFF_RED + 16 * 4;
 };
 
-template <bool OUT_BF16>
+// Persistent like the 16-bit forward: a CTA per SM walks work items (head, two query tiles),
+// from the queue when the launch has a slot (QUEUE) or in grid order; q_empty lets an item's Q
+// load once the last S of the previous item is issued, o_empty lets an item's first P V overwrite
+// O once the softmax has read it, and every phase runs on counters that continue across items.
+template <bool OUT_BF16, bool QUEUE>
 __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ q_scales,
                    const float* __restrict__ k_scales, const float* __restrict__ v_scales, void* __restrict__ out,
                    float* __restrict__ lse, int n, int bh_count, int tiles_per_head, float scale_log2, int causal,
-                   int group, unsigned long long* err, unsigned long long* counter) {
+                   int group, unsigned long long* err, unsigned long long* counter, unsigned* __restrict__ sched) {
   using C = Fp8Cfg;
   constexpr int D = C::D;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -336,36 +341,66 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
   uint64_t* p_full = s_full + 2;                // [2]
   uint64_t* o_full = p_full + 2;                // [2]
   uint64_t* drain = o_full + 2;
+  uint64_t* o_empty = drain + 1;                // [2] the softmax has read O_q of its last item
+  uint64_t* q_empty = o_empty + 2;              // every S of the last item is issued and done
+  uint64_t* item_full = q_empty + 1;            // [2] (queue mode)
+  uint64_t* item_empty = item_full + 2;         // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);                   // [2][8]
   const ErrCtx ctx{err, abort_flag};
 
-  int head, tile;
-  if (causal) {
-    int rank;
-    grouped_work_item(blockIdx.x, bh_count, tiles_per_head, &head, &rank);
-    tile = tiles_per_head - 1 - rank;
-  } else {
-    head = blockIdx.x / tiles_per_head;
-    tile = blockIdx.x - head * tiles_per_head;
-  }
-  const int kvhead = head / group;
   const int nblk = (n + BN - 1) / BN;  // 128-row blocks per head: key tiles and scale entries
-  const int qrow0 = tile * (C::NQ * BM);
-  int nq[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int first = qrow0 + q * BM;
-    if (first >= n) {
-      nq[q] = 0;
-    } else if (causal) {
-      nq[q] = min(nblk, (min(first + BM, n) - 1) / BN + 1);
+  const int total_items = bh_count * tiles_per_head;
+  struct Item {
+    int head, kvhead, qrow0;
+    int nq[2];  // key tiles of each query tile
+  };
+  // work items: head-major (CTAs running together share K/V in L2); causal: heaviest (last)
+  // query tiles first within groups of heads
+  auto item_of = [&](int item) {
+    Item w;
+    int tile;
+    if (causal) {
+      int rank;
+      grouped_work_item(item, bh_count, tiles_per_head, &w.head, &rank);
+      tile = tiles_per_head - 1 - rank;
     } else {
-      nq[q] = nblk;
+      w.head = item / tiles_per_head;
+      tile = item - w.head * tiles_per_head;
     }
-  }
-  const int nmax = max(nq[0], nq[1]);
+    w.kvhead = w.head / group;
+    w.qrow0 = tile * (C::NQ * BM);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int first = w.qrow0 + q * BM;
+      if (first >= n) {
+        w.nq[q] = 0;
+      } else if (causal) {
+        w.nq[q] = min(nblk, (min(first + BM, n) - 1) / BN + 1);
+      } else {
+        w.nq[q] = nblk;
+      }
+    }
+    return w;
+  };
+  // the static order: rounds of gridDim.x items (the grid size and CTA index read afresh each time)
+  auto nth_item = [&](int r) {
+    const int64_t item = (int64_t)r * (int)grid_dim_x() + (int)cta_id_x();
+    return item < total_items ? (int)item : -1;
+  };
+  // a consumer warp's r-th item: queue mode reads the producer's slot r % 2 (every consumer warp
+  // reads every slot once; `good` turns false, and the item -1, when the bounded wait ran out)
+  auto next_item = [&](int r, bool& good) {
+    if constexpr (!QUEUE) return nth_item(r);
+    const int t = r & 1;
+    good = __all_sync(0xffffffffu, mbar_wait(item_full + t, (uint32_t)(r >> 1) & 1, ctx, 250)) && good;
+    const int item = good ? item_slot[t] : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(item_empty + t);
+    return item;
+  };
 
   if (threadIdx.x == 0) {
     if ((smem_u32(smem) & 1023u) != 0) report_error(err, DERR_BAD_SMEM_ALIGN, 0);
@@ -379,8 +414,12 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       mbar_init(s_full + q, 1);
       mbar_init(p_full + q, 128);
       mbar_init(o_full + q, 1);
+      mbar_init(o_empty + q, 128);
+      mbar_init(item_full + q, 1);
+      mbar_init(item_empty + q, 9);  // the eight softmax warps and the MMA warp
     }
     mbar_init(drain, 1);
+    mbar_init(q_empty, 1);
     fence_barrier_init();
   }
   if (warp == C::MMA_WARP) {
@@ -399,24 +438,46 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(q_full, C::NQ * C::TILE_BYTES);
-      for (int q = 0; q < C::NQ; ++q)
-        tma_load_3d(smem + C::OFF_Q + q * C::TILE_BYTES, &tm_q, q_full, 0, qrow0 + q * BM, head);
-      int issued = 0;
-      for (int idx = 0; idx < 2 * nmax; ++idx) {
-        const int slot = idx % C::STAGES, use = idx / C::STAGES;
-        if (use > 0 && !mbar_wait(kv_empty + slot, (use - 1) & 1, ctx, 210)) break;
-        mbar_arrive_expect_tx(kv_full + slot, C::TILE_BYTES);
-        tma_load_3d(smem + C::OFF_RING + slot * C::TILE_BYTES, (idx & 1) ? &tm_v : &tm_k, kv_full + slot, 0,
-                    (idx >> 1) * BN, kvhead);
-        issued = idx + 1;
+      uint32_t ring_pos = 0;  // ring loads issued (all items)
+      int q_loads = 0;
+      bool ok = true;
+      // the r-th item: queue mode draws a ticket and publishes the item, or -1 once the queue is
+      // empty, when every reader of the slot's previous item has it
+      auto draw = [&](int r) {
+        if constexpr (!QUEUE) return nth_item(r);
+        if (r >= 2 && !(ok = mbar_wait(item_empty + (r & 1), (uint32_t)((r - 2) >> 1) & 1, ctx, 214))) return -1;
+        const unsigned ticket = atomicAdd(sched, 1u);
+        const int item = ticket < (unsigned)total_items ? (int)ticket : -1;
+        item_slot[r & 1] = item;
+        mbar_arrive(item_full + (r & 1));
+        return item;
+      };
+      for (int r = 0, item = draw(0); ok && item >= 0; item = draw(++r)) {
+        const Item w = item_of(item);
+        const int nmax = max(w.nq[0], w.nq[1]);
+        // Q of this item once the previous item's S = Q K^T are done
+        if (q_loads > 0 && !(ok = mbar_wait(q_empty, (q_loads - 1) & 1, ctx, 213))) break;
+        mbar_arrive_expect_tx(q_full, C::NQ * C::TILE_BYTES);
+        for (int q = 0; q < C::NQ; ++q)
+          tma_load_3d(smem + C::OFF_Q + q * C::TILE_BYTES, &tm_q, q_full, 0, w.qrow0 + q * BM, w.head);
+        ++q_loads;
+        for (int idx = 0; idx < 2 * nmax; ++idx) {
+          const uint32_t g = ring_pos;
+          const int slot = g % C::STAGES, use = g / C::STAGES;
+          if (use > 0 && !(ok = mbar_wait(kv_empty + slot, (use - 1) & 1, ctx, 210))) break;
+          mbar_arrive_expect_tx(kv_full + slot, C::TILE_BYTES);
+          tma_load_3d(smem + C::OFF_RING + slot * C::TILE_BYTES, (idx & 1) ? &tm_v : &tm_k, kv_full + slot, 0,
+                      (idx >> 1) * BN, w.kvhead);
+          ++ring_pos;
+        }
       }
+      // drain: every copy this thread started must land before the CTA may exit
       ErrCtx nctx = ctx;
       int no_abort = 0;
       nctx.abort = &no_abort;
-      mbar_wait(q_full, 0, nctx, 211);
-      for (int idx = issued - 1; idx >= 0 && idx >= issued - C::STAGES; --idx)
-        mbar_wait(kv_full + idx % C::STAGES, (idx / C::STAGES) & 1, nctx, 212);
+      if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, nctx, 211);
+      for (int g = (int)ring_pos - 1; g >= 0 && g >= (int)ring_pos - C::STAGES; --g)
+        mbar_wait(kv_full + g % C::STAGES, (g / C::STAGES) & 1, nctx, 212);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
@@ -428,11 +489,17 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       const uint32_t idesc_pv = make_idesc_f16(BM, D, false, false, true);
       const uint32_t q_base = smem_u32(smem + C::OFF_Q);
       const uint32_t ring = smem_u32(smem + C::OFF_RING);
-      auto slot_of = [&](int idx) { return idx % C::STAGES; };
+      uint32_t ring_pos = 0;  // ring entry of the item's first K tile (all items so far)
+      int tq[2] = {0, 0};     // key tiles processed by each query tile (all items): P phases
+      int oq[2] = {0, 0};     // items with a result for each query tile: O phases
+      int items = 0;
+      auto slot_of = [&](int idx) { return (int)((ring_pos + idx) % C::STAGES); };
       auto wait = [&](uint64_t* b, uint32_t parity, uint32_t site) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, ctx, site));
       };
-      auto wait_full = [&](int idx) { return wait(kv_full + slot_of(idx), (idx / C::STAGES) & 1, 220); };
+      auto wait_full = [&](int idx) {
+        return wait(kv_full + slot_of(idx), ((ring_pos + idx) / C::STAGES) & 1, 220);
+      };
       auto commit = [&](uint64_t* b) {
         if (leader) umma_commit(b);
         __syncwarp();
@@ -467,40 +534,56 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         }
         __syncwarp();
       };
-      bool ok = wait(q_full, 0, 221);
-      if (ok) tc_fence_after();
-      if (ok && nmax > 0) {
-        ok = wait_full(0);
-        if (ok) {
+      // the first P V of query tile q in an item overwrites O_q: the softmax must have read it
+      auto o_free = [&](int q) { return oq[q] == 0 || wait(o_empty + q, (oq[q] - 1) & 1, 226 + q); };
+      bool ok = true;
+      for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
+        const Item w = item_of(item);
+        const int* nq = w.nq;
+        const int nmax = max(nq[0], nq[1]);
+        if (!(ok = wait(q_full, items & 1, 221))) break;
+        tc_fence_after();
+        if (nmax > 0) {
+          if (!(ok = wait_full(0))) break;
           tc_fence_after();
           if (nq[0] > 0) { issue_qk(0, 0, C::S_COL0); commit(s_full + 0); }
           if (nq[1] > 0) { issue_qk(1, 0, C::S_COL1); commit(s_full + 1); }
           commit(kv_empty + slot_of(0));
         }
-      }
-      for (int j = 0; ok && j < nmax; ++j) {
-        const int vidx = 2 * j + 1, kidx = 2 * j + 2;
-        if (!(ok = wait_full(vidx))) break;
-        if (j < nq[0]) {
-          if (!(ok = wait(p_full + 0, j & 1, 222))) break;
-          tc_fence_after();
-          issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
+        if (nmax <= 1) commit(q_empty);  // every S of the item is issued
+        for (int j = 0; ok && j < nmax; ++j) {
+          const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+          if (!(ok = wait_full(vidx))) break;
+          if (j < nq[0]) {
+            if (!(ok = wait(p_full + 0, (tq[0] + j) & 1, 222))) break;
+            if (j == 0 && !(ok = o_free(0))) break;
+            tc_fence_after();
+            issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
+          }
+          if (j + 1 < nmax) {
+            if (!(ok = wait_full(kidx))) break;
+            tc_fence_after();
+          }
+          if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); commit(s_full + 0); }
+          if (j < nq[1]) {
+            if (!(ok = wait(p_full + 1, (tq[1] + j) & 1, 223))) break;
+            if (j == 0 && !(ok = o_free(1))) break;
+            tc_fence_after();
+            issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
+          }
+          commit(kv_empty + slot_of(vidx));
+          if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); commit(s_full + 1); }
+          if (j + 1 < nmax) commit(kv_empty + slot_of(kidx));
+          if (j == nmax - 2) commit(q_empty);  // the item's last S are issued
+          if (j == nq[0] - 1) commit(o_full + 0);
+          if (j == nq[1] - 1) commit(o_full + 1);
         }
-        if (j + 1 < nmax) {
-          if (!(ok = wait_full(kidx))) break;
-          tc_fence_after();
+        ring_pos += 2 * nmax;
+        for (int q = 0; q < 2; ++q) {
+          tq[q] += nq[q];
+          oq[q] += nq[q] > 0 ? 1 : 0;
         }
-        if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); commit(s_full + 0); }
-        if (j < nq[1]) {
-          if (!(ok = wait(p_full + 1, j & 1, 223))) break;
-          tc_fence_after();
-          issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
-        }
-        commit(kv_empty + slot_of(vidx));
-        if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); commit(s_full + 1); }
-        if (j + 1 < nmax) commit(kv_empty + slot_of(kidx));
-        if (j == nq[0] - 1) commit(o_full + 0);
-        if (j == nq[1] - 1) commit(o_full + 1);
+        ++items;
       }
       ErrCtx nctx = ctx;
       int no_abort = 0;
@@ -515,126 +598,149 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     const int quarter = warp & 3;
     const uint32_t lane_base = quarter * 32;
     const int rit = quarter * 32 + lane;
-    const int row = qrow0 + q * BM + rit;
-    const int nb = nq[q];
     const uint32_t s_col = q ? C::S_COL1 : C::S_COL0;
     const uint32_t o_col = q ? C::O_COL1 : C::O_COL0;
-    const float* ks = k_scales + (int64_t)kvhead * nblk;
-    const float* vs = v_scales + (int64_t)kvhead * nblk;
-    // the head's largest V scale (both warpgroups, one named barrier)
-    float svmax = 0.f;
-    for (int i = threadIdx.x; i < nblk; i += 256) svmax = fmaxf(svmax, vs[i]);
-    for (int o = 16; o > 0; o >>= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, o));
-    if (lane == 0) red[warp] = svmax;
-    named_bar_sync(1, 256);
-    svmax = red[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) svmax = fmaxf(svmax, red[w]);
-    const float inv_svmax = 1.f / svmax;
-    const int qblk = min((qrow0 + q * BM) / BM, nblk - 1);
-    const float sq_log2 = scale_log2 * q_scales[(int64_t)head * nblk + qblk];
-    float m = -INFINITY;
-    float l = 0.f;
+    int tq = 0;  // key tiles this query tile processed (all items): S / P phases
+    int oq = 0;  // items with a result: O phases
     bool ok = start_ok;
-    float sk_next = nb > 0 ? ks[0] : 0.f, sv_next = nb > 0 ? vs[0] : 0.f;
-    for (int j = 0; ok && j < nb; ++j) {
-      const float st = sq_log2 * sk_next;      // tau log2(e) sq sk: S units -> log2 units
-      const float pv = sv_next * inv_svmax;   // sv / sv_max, folded into P
-      if (j + 1 < nb) {
-        sk_next = ks[j + 1];
-        sv_next = vs[j + 1];
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full + q, j & 1, ctx, 230 + q));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[BN / 32][32];
+    // The eight softmax warps meet at a named barrier per item (the head's largest V scale), so
+    // they decide together, through that barrier's reduction, whether to take another item: a
+    // warp whose bounded wait ran out cannot leave the others waiting there.
+    for (int r = 0;; ++r) {
+      bool got = ok;
+      const int item = next_item(r, got);
+      const bool have = got && item >= 0;
+      const Item w = item_of(have ? item : 0);
+      // the head's largest V scale (both warpgroups; partial maxima in red[r % 2])
+      const float* vs = v_scales + (int64_t)w.kvhead * nblk;
+      float svmax = 0.f;
+      if (have)
+        for (int i = threadIdx.x; i < nblk; i += 256) svmax = fmaxf(svmax, vs[i]);
+      for (int o = 16; o > 0; o >>= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, o));
+      float* rd = red + (r & 1) * 8;
+      if (lane == 0) rd[warp] = svmax;
+      if (!named_bar_and(1, 256, have)) break;
+      svmax = rd[0];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, s_col + c * 32), sr[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
-      float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
-      int limit = n - j * BN;
-      if (causal) limit = min(limit, row - j * BN + 1);
-      if (limit < BN) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c >= limit) s[c] = -INFINITY;
-      }
-      const float mx = row_max(s);
-      const float m_blk = mx * st;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (m == -INFINITY) {
-        m = m_blk;
-        alpha = 0.f;
-      } else if (m_blk > m + kRescaleThreshold) {
-        alpha = ex2(m - m_blk);
-        m = m_blk;
-        rescale = true;
-      }
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2(fmaf(s[4 * i], st, neg_m));
-        const float p1 = ex2(fmaf(s[4 * i + 1], st, neg_m));
-        const float p2 = ex2(fmaf(s[4 * i + 2], st, neg_m));
-        const float p3 = ex2(fmaf(s[4 * i + 3], st, neg_m));
-        part[i & 3] += (p0 + p1) + (p2 + p3);
-        pk[i] = pack4_e4m3(p0 * pv, p1 * pv, p2 * pv, p3 * pv);
-      }
-      const float sum = (part[0] + part[1]) + (part[2] + part[3]);
-      tmem_st32(tmem_addr(tbase, lane_base, s_col), pk);
-      l = l * alpha + sum;
-      if (__any_sync(0xffffffffu, rescale)) {
-        const float a = rescale ? alpha : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          const uint32_t ta = tmem_addr(tbase, lane_base, o_col + c * 32);
-          tmem_ld32(ta, r);
-          tmem_wait_ld();
-          reg_fence(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-          tmem_st32(ta, r);
+      for (int i = 1; i < 8; ++i) svmax = fmaxf(svmax, rd[i]);
+      const float inv_svmax = 1.f / svmax;
+      const int head = w.head;
+      const int row = w.qrow0 + q * BM + rit;
+      const int nb = w.nq[q];
+      const float* ks = k_scales + (int64_t)w.kvhead * nblk;
+      const int qblk = min((w.qrow0 + q * BM) / BM, nblk - 1);
+      const float sq_log2 = scale_log2 * q_scales[(int64_t)head * nblk + qblk];
+      float m = -INFINITY;
+      float l = 0.f;
+      float sk_next = nb > 0 ? ks[0] : 0.f, sv_next = nb > 0 ? vs[0] : 0.f;
+      for (int j = 0; ok && j < nb; ++j) {
+        const int t = tq + j;
+        const float st = sq_log2 * sk_next;     // tau log2(e) sq sk: S units -> log2 units
+        const float pv = sv_next * inv_svmax;  // sv / sv_max, folded into P
+        if (j + 1 < nb) {
+          sk_next = ks[j + 1];
+          sv_next = vs[j + 1];
         }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full + q);
-    }
-    if (ok && nb > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(o_full + q, 0, ctx, 240 + q));
-      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full + q, t & 1, ctx, 230 + q));
+        if (!ok) break;
         tc_fence_after();
-        const float inv = l > 0.f ? svmax / l : 0.f;
-        uint8_t* orow = reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2;
+        uint32_t sr[BN / 32][32];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, s_col + c * 32), sr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
+        float s[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+        int limit = n - j * BN;
+        if (causal) limit = min(limit, row - j * BN + 1);
+        if (limit < BN) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= limit) s[c] = -INFINITY;
+        }
+        const float mx = row_max(s);
+        const float m_blk = mx * st;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m == -INFINITY) {
+          m = m_blk;
+          alpha = 0.f;
+        } else if (m_blk > m + kRescaleThreshold) {
+          alpha = ex2(m - m_blk);
+          m = m_blk;
+          rescale = true;
+        }
+        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(s[4 * i], st, neg_m));
+          const float p1 = ex2(fmaf(s[4 * i + 1], st, neg_m));
+          const float p2 = ex2(fmaf(s[4 * i + 2], st, neg_m));
+          const float p3 = ex2(fmaf(s[4 * i + 3], st, neg_m));
+          part[i & 3] += (p0 + p1) + (p2 + p3);
+          pk[i] = pack4_e4m3(p0 * pv, p1 * pv, p2 * pv, p3 * pv);
+        }
+        const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+        tmem_st32(tmem_addr(tbase, lane_base, s_col), pk);
+        l = l * alpha + sum;
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O row *= alpha; O is stable: the PV of block j-1 completed before S_j (same issuing
+          // thread, in order)
+          const float a = rescale ? alpha : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem_addr(tbase, lane_base, o_col + c * 32), r);
-          tmem_wait_ld();
-          reg_fence(r);
-          uint32_t pk[16];
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            const uint32_t ta = tmem_addr(tbase, lane_base, o_col + c * 32);
+            tmem_ld32(ta, rr);
+            tmem_wait_ld();
+            reg_fence(rr);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack2<OUT_BF16>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-          if (row < n) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * a);
+            tmem_st32(ta, rr);
           }
         }
-        if (row < n) lse[(int64_t)head * n + row] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-        if (counter && rit == 0) atomicAdd(counter, (unsigned long long)nb);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full + q);
       }
+      // epilogue: O sv_max / l -> global (16-bit), L = (m + log2 l) ln 2
+      if (ok && nb > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(o_full + q, oq & 1, ctx, 240 + q));
+        if (ok) {
+          tc_fence_after();
+          const float inv = l > 0.f ? svmax / l : 0.f;
+          uint8_t* orow = reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tmem_addr(tbase, lane_base, o_col + c * 32), rr);
+            tmem_wait_ld();
+            reg_fence(rr);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack2<OUT_BF16>(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
+            if (row < n) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+          // every TMEM load of O is done: the next item may overwrite it
+          tc_fence_before();
+          mbar_arrive(o_empty + q);
+          ++oq;
+          if (row < n) lse[(int64_t)head * n + row] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          if (counter && rit == 0) atomicAdd(counter, (unsigned long long)nb);
+        }
+      }
+      tq += nb;
     }
   }
 
@@ -643,6 +749,15 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
   if (warp == C::MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
+  }
+  if (QUEUE && threadIdx.x == 0) {
+    // this CTA draws no more tickets; the last one to get here empties the queue for the next
+    // launch that uses it (every CTA has drawn its last ticket by then)
+    __threadfence();
+    if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(sched, 0u);
+      atomicExch(sched + 1, 0u);
+    }
   }
 }
 
@@ -654,14 +769,20 @@ cudaError_t launch_fwd_fp8_t(const Fp8FwdArgs& a) {
   if (!make_tmap_8bit_3d(&tq, a.q8, C::D, a.n, a.bh, BM) || !make_tmap_8bit_3d(&tk, a.k8, C::D, a.n, bh_kv, BN) ||
       !make_tmap_8bit_3d(&tv, a.v8, C::D, a.n, bh_kv, BN))
     return cudaErrorInvalidValue;
-  auto kern = fwd_fp8_kernel<OUT_BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
   const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
-  kern<<<(unsigned)(a.bh * tiles), C::THREADS, C::SMEM, a.stream>>>(
-      tq, tk, tv, a.q_scales, a.k_scales, a.v_scales, a.o, a.lse, a.n, a.bh, tiles,
-      a.scale * 1.4426950408889634f, a.causal, a.group, a.err, a.counter);
-  return cudaGetLastError();
+  const int64_t items = (int64_t)a.bh * tiles;
+  const int64_t grid = std::min<int64_t>(items, device_sm_count());
+  QueueSlot qs;
+  if (grid < items) qs = queue_slot_take(a.stream);
+  auto kern = qs.slot >= 0 ? fwd_fp8_kernel<OUT_BF16, true> : fwd_fp8_kernel<OUT_BF16, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e == cudaSuccess) {
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, a.q_scales, a.k_scales, a.v_scales, a.o,
+                                                            a.lse, a.n, a.bh, tiles, a.scale * 1.4426950408889634f,
+                                                            a.causal, a.group, a.err, a.counter, qs.counters);
+    e = cudaGetLastError();
+  }
+  return queue_slot_done(qs, e, a.stream);
 }
 
 }  // namespace

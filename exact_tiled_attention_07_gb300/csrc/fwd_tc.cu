@@ -671,61 +671,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
 // Largest per-CTA work (key tiles) of a persistent causal grid of g CTAs over the items, in grid
 // order or snake order: the same item order and key-tile counts as the kernel.
-// Work-item queues of the persistent forward (the call has no workspace): a few pairs of
-// counters (next ticket, CTAs done) in device memory that the library owns.  A launch takes a
-// slot that no earlier launch still uses: the event recorded on the stream right after a slot's
-// last launch has completed, so that launch has finished and its last CTA has set the counters
-// back to zero.  A stream being captured into a graph, or all slots busy, gets no slot and the
-// static order instead.
-constexpr int kQueueSlots = 32;
-constexpr int kMaxQueueDevices = 64;
-__device__ unsigned g_fwd_queue[kQueueSlots][2];
-
-struct QueuePool {
-  unsigned* base = nullptr;
-  cudaEvent_t done[kQueueSlots] = {};
-  bool used[kQueueSlots] = {};    // a launch was recorded on done[i]
-  bool broken[kQueueSlots] = {};  // recording failed: never reused
-  int next = 0;
-};
-QueuePool g_qpool[kMaxQueueDevices];
-std::mutex g_qpool_mu;  // held from choosing a slot until its launch is recorded
-
-// A free slot of the current device's pool (its index; *counters its device address), or -1.
-int acquire_queue_slot(cudaStream_t stream, QueuePool** pool, unsigned** counters) {
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxQueueDevices) return -1;
-  QueuePool& p = g_qpool[dev];
-  if (!p.base) {
-    void* b = nullptr;
-    if (cudaGetSymbolAddress(&b, g_fwd_queue) != cudaSuccess || !b) return -1;
-    p.base = static_cast<unsigned*>(b);
-  }
-  for (int t = 0; t < kQueueSlots; ++t) {
-    const int i = (p.next + t) % kQueueSlots;
-    if (p.broken[i]) continue;
-    if (!p.done[i] && cudaEventCreateWithFlags(&p.done[i], cudaEventDisableTiming) != cudaSuccess) {
-      p.done[i] = nullptr;
-      return -1;
-    }
-    if (p.used[i]) {
-      const cudaError_t q = cudaEventQuery(p.done[i]);
-      if (q == cudaErrorNotReady) {
-        if (cudaPeekAtLastError() == cudaErrorNotReady) (void)cudaGetLastError();
-        continue;
-      }
-      if (q != cudaSuccess) return -1;
-    }
-    p.next = (i + 1) % kQueueSlots;
-    *pool = &p;
-    *counters = p.base + 2 * i;
-    return i;
-  }
-  return -1;
-}
-
 int64_t max_cta_tiles(int bh, int tiles_per_head, int n, int nq_tiles, int g, bool snake) {
   std::vector<int64_t> load(g, 0);
   const int64_t total = (int64_t)bh * tiles_per_head;
@@ -769,32 +714,20 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
                         : 0;
   // with more items than CTAs: the queue when a slot is free (CTAs that finish early take more
   // items, whatever the cause), else the static order
-  std::unique_lock<std::mutex> lk(g_qpool_mu, std::defer_lock);
-  QueuePool* pool = nullptr;
-  unsigned* sched = nullptr;
-  int slot = -1;
-  if (!MASKED && grid < items) {
-    lk.lock();
-    slot = acquire_queue_slot(a.stream, &pool, &sched);
-  }
+  QueueSlot qs;
+  if (!MASKED && grid < items) qs = queue_slot_take(a.stream);
   auto kern = fwd_tc_kernel<D, BF16, MASKED, false>;
   if constexpr (!MASKED) {
-    if (slot >= 0) kern = fwd_tc_kernel<D, BF16, false, true>;
+    if (qs.slot >= 0) kern = fwd_tc_kernel<D, BF16, false, true>;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
-                                                       a.causal, a.group, a.err, a.counter, a.window, a.block_mask,
-                                                       a.mask_heads, a.heads, snake, slot >= 0 ? sched : nullptr);
-  e = cudaGetLastError();
-  if (slot >= 0 && e == cudaSuccess) {
-    e = cudaEventRecord(pool->done[slot], a.stream);
-    if (e == cudaSuccess)
-      pool->used[slot] = true;
-    else
-      pool->broken[slot] = true;  // the launch may still run: never hand this slot out again
+  if (e == cudaSuccess) {
+    kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
+                                                         a.causal, a.group, a.err, a.counter, a.window, a.block_mask,
+                                                         a.mask_heads, a.heads, snake, qs.counters);
+    e = cudaGetLastError();
   }
-  return e;
+  return queue_slot_done(qs, e, a.stream);
 }
 
 template <int D, bool BF16>
@@ -803,6 +736,93 @@ cudaError_t launch_fwd_dm(const FwdArgs& a) {
 }
 
 }  // namespace
+
+namespace {
+
+// Work-item queues of the persistent forwards (16-bit and FP8; the calls have no workspace): a few pairs of
+// counters (next ticket, CTAs done) in device memory that the library owns.  A launch takes a
+// slot that no earlier launch still uses: the event recorded on the stream right after a slot's
+// last launch has completed, so that launch has finished and its last CTA has set the counters
+// back to zero.  A stream being captured into a graph, or all slots busy, gets no slot and the
+// static order instead.
+constexpr int kQueueSlots = 32;
+constexpr int kMaxQueueDevices = 64;
+__device__ unsigned g_fwd_queue[kQueueSlots][2];
+
+struct QueuePool {
+  unsigned* base = nullptr;
+  cudaEvent_t done[kQueueSlots] = {};
+  bool used[kQueueSlots] = {};    // a launch was recorded on done[i]
+  bool broken[kQueueSlots] = {};  // recording failed: never reused
+  int next = 0;
+};
+QueuePool g_qpool[kMaxQueueDevices];
+std::mutex g_qpool_mu;  // held from choosing a slot until its launch is recorded
+
+// A free slot of the current device's pool (its index; *counters its device address), or -1.
+int acquire_queue_slot(cudaStream_t stream, QueuePool** pool, unsigned** counters, int* device) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxQueueDevices) return -1;
+  *device = dev;
+  QueuePool& p = g_qpool[dev];
+  if (!p.base) {
+    void* b = nullptr;
+    if (cudaGetSymbolAddress(&b, g_fwd_queue) != cudaSuccess || !b) return -1;
+    p.base = static_cast<unsigned*>(b);
+  }
+  for (int t = 0; t < kQueueSlots; ++t) {
+    const int i = (p.next + t) % kQueueSlots;
+    if (p.broken[i]) continue;
+    if (!p.done[i] && cudaEventCreateWithFlags(&p.done[i], cudaEventDisableTiming) != cudaSuccess) {
+      p.done[i] = nullptr;
+      return -1;
+    }
+    if (p.used[i]) {
+      const cudaError_t q = cudaEventQuery(p.done[i]);
+      if (q == cudaErrorNotReady) {
+        if (cudaPeekAtLastError() == cudaErrorNotReady) (void)cudaGetLastError();
+        continue;
+      }
+      if (q != cudaSuccess) return -1;
+    }
+    p.next = (i + 1) % kQueueSlots;
+    *pool = &p;
+    *counters = p.base + 2 * i;
+    return i;
+  }
+  return -1;
+}
+
+}  // namespace
+
+QueueSlot queue_slot_take(cudaStream_t stream) {
+  QueueSlot q;
+  g_qpool_mu.lock();
+  QueuePool* pool = nullptr;
+  q.slot = acquire_queue_slot(stream, &pool, &q.counters, &q.device);
+  if (q.slot < 0) {
+    q.counters = nullptr;
+    g_qpool_mu.unlock();
+  }
+  return q;
+}
+
+cudaError_t queue_slot_done(const QueueSlot& q, cudaError_t launch_status, cudaStream_t stream) {
+  if (q.slot < 0) return launch_status;
+  QueuePool& p = g_qpool[q.device];
+  cudaError_t e = launch_status;
+  if (e == cudaSuccess) {
+    e = cudaEventRecord(p.done[q.slot], stream);
+    if (e == cudaSuccess)
+      p.used[q.slot] = true;
+    else
+      p.broken[q.slot] = true;  // the launch may still run: never hand this slot out again
+  }
+  g_qpool_mu.unlock();
+  return e;
+}
 
 bool fwd_masked_fits(int n, int d) {
   const int nb = (n + BN - 1) / BN;

@@ -111,6 +111,19 @@ struct QuantArgs {
 };
 cudaError_t launch_quantize_fp8(const QuantArgs& a);
 
+// Work-item queue slots of the persistent forwards (a library-owned pool of counter pairs).
+// queue_slot_take picks a slot that no unfinished launch uses (slot -1, counters null: none
+// free, or the stream is being captured into a graph) and holds the pool's lock until
+// queue_slot_done, which must follow the launch at once with its status: it records the slot's
+// completion event on the stream and returns the launch status (or the recording error).
+struct QueueSlot {
+  int slot = -1;
+  int device = 0;
+  unsigned* counters = nullptr;
+};
+QueueSlot queue_slot_take(cudaStream_t stream);
+cudaError_t queue_slot_done(const QueueSlot& q, cudaError_t launch_status, cudaStream_t stream);
+
 // FP8 forward: Q8, K8, V8 [bh][n][d] E4M3 codes with block scales; O [bh][n][d] in out_dtype
 // (bf16 or fp16), L [bh][n] fp32.
 struct Fp8FwdArgs {
