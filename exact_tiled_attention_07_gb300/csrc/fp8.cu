@@ -636,7 +636,8 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       for (int j = 0; ok && j < nb; ++j) {
         const int t = tq + j;
         const float st = sq_log2 * sk_next;     // tau log2(e) sq sk: S units -> log2 units
-        const float pv = sv_next * inv_svmax;  // sv / sv_max, folded into P
+        const float pv = sv_next * inv_svmax;  // sv / sv_max (<= 1), folded into P's exponent
+        const float lpv = __log2f(pv);
         if (j + 1 < nb) {
           sk_next = ks[j + 1];
           sv_next = vs[j + 1];
@@ -674,7 +675,9 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           m = m_blk;
           rescale = true;
         }
-        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        // P sv / sv_max = exp2(S st - m + log2(sv / sv_max)): the V factor rides in the exponent,
+        // and the row sum of P is that of the scaled values divided by the factor once per tile
+        const float neg_m = ((m == -INFINITY) ? 0.f : -m) + lpv;
         float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
         uint32_t pk[32];
 #pragma unroll
@@ -684,9 +687,9 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           const float p2 = ex2(fmaf(s[4 * i + 2], st, neg_m));
           const float p3 = ex2(fmaf(s[4 * i + 3], st, neg_m));
           part[i & 3] += (p0 + p1) + (p2 + p3);
-          pk[i] = pack4_e4m3(p0 * pv, p1 * pv, p2 * pv, p3 * pv);
+          pk[i] = pack4_e4m3(p0, p1, p2, p3);
         }
-        const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+        const float sum = ((part[0] + part[1]) + (part[2] + part[3])) / pv;
         tmem_st32(tmem_addr(tbase, lane_base, s_col), pk);
         l = l * alpha + sum;
         if (__any_sync(0xffffffffu, rescale)) {
