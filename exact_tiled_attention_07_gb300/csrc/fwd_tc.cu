@@ -739,12 +739,13 @@ cudaError_t launch_fwd_dm(const FwdArgs& a) {
 
 namespace {
 
-// Work-item queues of the persistent forwards (16-bit and FP8; the calls have no workspace): a few pairs of
-// counters (next ticket, CTAs done) in device memory that the library owns.  A launch takes a
-// slot that no earlier launch still uses: the event recorded on the stream right after a slot's
-// last launch has completed, so that launch has finished and its last CTA has set the counters
-// back to zero.  A stream being captured into a graph, or all slots busy, gets no slot and the
-// static order instead.
+// Work-item queues of the persistent forwards (16-bit and FP8; the calls have no workspace): a
+// few pairs of counters (next ticket, CTAs done) in device memory that the library owns.  A
+// stream keeps the slot of its last launch (launches on one stream run one after the other, so
+// that launch has finished, and its last CTA has set the counters back to zero, before the next
+// one starts).  A stream without a slot takes one that no unfinished launch uses: the event
+// recorded on the stream right after the slot's last launch has completed.  A stream being
+// captured into a graph, or finding every slot busy, gets no slot and the static order instead.
 constexpr int kQueueSlots = 32;
 constexpr int kMaxQueueDevices = 64;
 __device__ unsigned g_fwd_queue[kQueueSlots][2];
@@ -754,6 +755,8 @@ struct QueuePool {
   cudaEvent_t done[kQueueSlots] = {};
   bool used[kQueueSlots] = {};    // a launch was recorded on done[i]
   bool broken[kQueueSlots] = {};  // recording failed: never reused
+  bool owned[kQueueSlots] = {};   // owner[i] holds the stream of the slot's last launch
+  unsigned long long owner[kQueueSlots] = {};
   int next = 0;
 };
 QueuePool g_qpool[kMaxQueueDevices];
@@ -766,12 +769,28 @@ int acquire_queue_slot(cudaStream_t stream, QueuePool** pool, unsigned** counter
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxQueueDevices) return -1;
   *device = dev;
+  // streams are told apart by their ids, which (unlike handles) are never reused
+  unsigned long long sid = 0;
+  if (cudaStreamGetId(stream, &sid) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
   QueuePool& p = g_qpool[dev];
   if (!p.base) {
     void* b = nullptr;
     if (cudaGetSymbolAddress(&b, g_fwd_queue) != cudaSuccess || !b) return -1;
     p.base = static_cast<unsigned*>(b);
   }
+  // the stream's own slot: launches on one stream run one after the other, so the slot's last
+  // launch has finished (and reset the counters) before this one starts
+  for (int i = 0; i < kQueueSlots; ++i) {
+    if (p.owned[i] && p.owner[i] == sid && !p.broken[i]) {
+      *pool = &p;
+      *counters = p.base + 2 * i;
+      return i;
+    }
+  }
+  // else a slot whose last launch (on any stream) has completed; it changes owner
   for (int t = 0; t < kQueueSlots; ++t) {
     const int i = (p.next + t) % kQueueSlots;
     if (p.broken[i]) continue;
@@ -788,6 +807,8 @@ int acquire_queue_slot(cudaStream_t stream, QueuePool** pool, unsigned** counter
       if (q != cudaSuccess) return -1;
     }
     p.next = (i + 1) % kQueueSlots;
+    p.owned[i] = true;
+    p.owner[i] = sid;
     *pool = &p;
     *counters = p.base + 2 * i;
     return i;

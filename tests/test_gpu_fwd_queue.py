@@ -1,7 +1,8 @@
 """The persistent forward's work-item queues (a library-owned pool of counter slots).
 
-A launch takes a slot only once the previous launch on it has finished; with every slot busy,
-or on a stream being captured into a CUDA graph, it runs the static order instead.  Whichever
+A stream keeps the slot of its last launch; a stream without one takes a slot only once the
+previous launch on it has finished; with every slot busy, or on a stream being captured into a
+CUDA graph, a launch runs the static order instead.  Whichever
 path runs, each item is computed the same way, so O and L equal a reference launch bit for bit.
 """
 
@@ -42,10 +43,26 @@ def _launch(fa, w, dev):
     return o, lse
 
 
-def test_more_launches_in_flight_than_queue_slots(fa, problem):
+def test_back_to_back_launches_on_one_stream_reuse_its_slot(fa, problem):
     w, dev, o_ref, l_ref = problem
     torch.cuda._sleep(50_000_000)  # holds the stream, so the launches below are all still pending
-    outs = [_launch(fa, w, dev) for _ in range(40)]  # more than the 32 slots: the rest run static
+    outs = [_launch(fa, w, dev) for _ in range(40)]
+    torch.cuda.synchronize()
+    fa.fa_check_device_error()
+    for o, lse in outs:
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_more_streams_with_pending_launches_than_queue_slots(fa, problem):
+    """40 streams, each holding a pending launch behind a sleep: more than the 32 slots, so the
+    last streams find every slot busy and run the static order."""
+    w, dev, o_ref, l_ref = problem
+    streams = [torch.cuda.Stream() for _ in range(40)]
+    outs = []
+    for s in streams:
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(20_000_000)
+            outs.append(_launch(fa, w, dev))
     torch.cuda.synchronize()
     fa.fa_check_device_error()
     for o, lse in outs:
