@@ -8,10 +8,11 @@
 //     dK_j += dS^T Q_i,   dQ_i += dS K_j      (tau applied to dK here and to dQ on conversion)
 // with D_i = sum_k dO_ik O_ik precomputed by the preprocess kernel (the §5.4 identity).
 //
-// One CTA owns a 128-key tile of one key/value head for its whole life (with grouped-query
-// attention it visits every query head of that key/value head): K_j, V_j stay in shared
-// memory and the dK_j, dV_j accumulators stay in TMEM, while query tiles (Q_i, dO_i, L_i,
-// D_i) stream through a three-stage TMA ring.  Working transposed puts keys on TMEM lanes, so
+// A work item is a 128-key tile of one key/value head (with grouped-query attention it visits
+// every query head of that key/value head): while a CTA works on it, K_j, V_j stay in shared
+// memory and the dK_j, dV_j accumulators stay in TMEM, and query tiles (Q_i, dO_i, L_i, D_i)
+// stream through a three-stage TMA ring.  The grid is persistent (one CTA per SM, items from a
+// queue; see the kernel).  Working transposed puts keys on TMEM lanes, so
 // one thread owns one key row: P^T and dS^T need no cross-thread reduction.  K_j, P^T and
 // dS^T sit in TMEM as A operands (S^T = K Q^T, dV += P^T dO, dK += dS^T Q), which spares
 // the shared-memory read of A that an all-smem MMA pays; dS^T also goes to shared memory

@@ -5,8 +5,9 @@
 // & FlashAttention" §5.3 tiled forward, §5.4 what is kept for the backward; "FlashAttention
 // and GPU memory" §07/§08).
 //
-// Work split (FA2 order, "Lecture 8" §8.1): one CTA owns NQ query tiles of 128 rows of one
-// head and streams 128-key tiles K_j, V_j through a shared-memory ring.  Roles:
+// Work split (FA2 order, "Lecture 8" §8.1): a work item is NQ query tiles of 128 rows of one
+// head; the CTA working on it streams 128-key tiles K_j, V_j through a shared-memory ring.
+// Roles:
 //   * softmax warpgroup q (4 warps, one thread per query row): reads S_q from TMEM,
 //     applies the causal/ragged mask, runs the online softmax in the exp2 domain (§5.2),
 //     writes P (16-bit) back into TMEM over S, rescales the O accumulator in TMEM when the
@@ -27,12 +28,14 @@
 // Causal: key tiles wholly in the future of a query tile are never loaded or multiplied
 // (§5.3 closing paragraph); only diagonal tiles are masked element-wise.
 //
-// Persistent: a CTA (one per SM) walks work items (head, NQ query tiles), round by round
-// across the grid: in grid order, or for causal launches whose items a host-side estimate
-// balances better that way, backwards in odd rounds (heavy and light items pair up).  The K/V ring, S/P and O barriers keep their phases across items; q_empty (all of
-// an item's S = Q K^T issued and done) lets the next item's Q load while the item finishes,
-// and o_empty (the softmax has read O) lets the next item's first P V overwrite O, so one
-// item's epilogue overlaps the next item's loads and first S tiles.
+// Persistent: a CTA (one per SM) walks work items (head, NQ query tiles).  It takes them from
+// a queue (a ticket counter drawn by the producer warp and published to the other roles) when
+// the launch has a counter slot, else round by round across the grid: in grid order, or for
+// causal launches whose items a host-side estimate balances better that way, backwards in odd
+// rounds (heavy and light items pair up).  The K/V ring, S/P and O barriers keep their phases
+// across items; q_empty (all of an item's S = Q K^T issued and done) lets the next item's Q
+// load while the item finishes, and o_empty (the softmax has read O) lets the next item's first
+// P V overwrite O, so one item's epilogue overlaps the next item's loads and first S tiles.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <algorithm>
