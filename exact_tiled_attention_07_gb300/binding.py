@@ -20,8 +20,8 @@ __all__ = [
     "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
-    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait",
-    "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size",
+    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_fp8_gqa", "fa_fwd_masked", "fa_bwd_masked",
+    "fa_selftest_bounded_wait", "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size",
     "attention_forward", "attention_backward", "attention_decode",
     "attention_forward_fp8", "quantize_fp8", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
@@ -36,8 +36,8 @@ EXPORTED_SYMBOLS = (
     "fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert",
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
-    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait",
-    "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size",
+    "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_fp8_gqa", "fa_fwd_masked", "fa_bwd_masked",
+    "fa_selftest_bounded_wait", "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size",
 )
 
 _lib = None
@@ -84,6 +84,7 @@ def load_library():
         lib.fa_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, i, i, vp]
         lib.fa_bwd_masked.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, vp, i, i, vp]
         lib.fa_fwd_fp8.argtypes = [vp] * 8 + [i, i, i, i, f, i, i, vp]
+        lib.fa_fwd_fp8_gqa.argtypes = [vp] * 8 + [i, i, i, i, i, f, i, i, vp]
         lib.fa_selftest_bounded_wait.argtypes = [i, i, vp]
         lib.fa_fwd_bwd_host_workspace_size.argtypes = [i, i, i, i, i, i, i]
         lib.fa_fwd_bwd_host_workspace_size.restype = sz
@@ -96,6 +97,7 @@ def load_library():
         lib.fa_last_error_message.argtypes = []
         lib.fa_last_error_message.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_bwd", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_quantize_fp8", "fa_fwd_fp8",
+                     "fa_fwd_fp8_gqa",
                      "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait", "fa_fwd_bwd_host",
                      "fa_bwd_noalloc", "fa_bwd_preprocess",
                      "fa_bwd_main", "fa_bwd_dq_convert",
@@ -287,21 +289,35 @@ def fa_quantize_fp8(X, X8, scales, stream=None):
 
 
 def fa_fwd_fp8(Q8, K8, V8, q_scales, k_scales, v_scales, O, L, scale, causal, stream=None):
-    """Forward on E4M3 codes with block scales; O [B, H, N, d] bf16 or fp16, L [B, H, N] fp32."""
+    """Forward on E4M3 codes with block scales; O [B, H, N, d] bf16 or fp16, L [B, H, N] fp32.
+    K8, V8 (and their scales) may have fewer heads than Q8 (grouped-query: fa_fwd_fp8_gqa)."""
     B, H, N, d = _shape4(Q8)
+    Hkv = _shape4(K8)[1]
     nb = (N + 127) // 128
-    for t in (Q8, K8, V8):
-        if t.dtype != torch.uint8 or tuple(t.shape) != (B, H, N, d) or not t.is_contiguous():
-            raise ValueError("Q8, K8, V8 must be contiguous uint8 tensors of one shape")
-    for t in (q_scales, k_scales, v_scales):
-        if t.dtype != torch.float32 or t.numel() != B * H * nb or not t.is_contiguous():
-            raise ValueError("block scales must be contiguous fp32 tensors of B*H*ceil(N/128) elements")
+    for t, heads in ((Q8, H), (K8, Hkv), (V8, Hkv)):
+        if t.dtype != torch.uint8 or tuple(t.shape) != (B, heads, N, d) or not t.is_contiguous():
+            raise ValueError("Q8 [B, H, N, d] and K8, V8 [B, Hkv, N, d] must be contiguous uint8 tensors")
+    if Hkv < 1 or H % Hkv:
+        raise ValueError("H must be a multiple of the key/value heads Hkv")
+    for t, heads in ((q_scales, H), (k_scales, Hkv), (v_scales, Hkv)):
+        if t.dtype != torch.float32 or t.numel() != B * heads * nb or not t.is_contiguous():
+            raise ValueError("block scales must be contiguous fp32 tensors of B*heads*ceil(N/128) elements")
     if tuple(O.shape) != (B, H, N, d) or not O.is_contiguous():
         raise ValueError("O must be a contiguous [B, H, N, d] tensor")
     if L.dtype != torch.float32 or L.numel() != B * H * N or not L.is_contiguous():
         raise ValueError("L must be a contiguous fp32 tensor of B*H*N elements")
+    if Hkv != H:
+        _check(load_library().fa_fwd_fp8_gqa(_p(Q8), _p(K8), _p(V8), _p(q_scales), _p(k_scales), _p(v_scales), _p(O),
+                                             _p(L), B, H, Hkv, N, d, float(scale), int(bool(causal)), _dt(O),
+                                             _stream(stream)))
+        return
     _check(load_library().fa_fwd_fp8(_p(Q8), _p(K8), _p(V8), _p(q_scales), _p(k_scales), _p(v_scales), _p(O), _p(L),
                                      B, H, N, d, float(scale), int(bool(causal)), _dt(O), _stream(stream)))
+
+
+def fa_fwd_fp8_gqa(Q8, K8, V8, q_scales, k_scales, v_scales, O, L, scale, causal, stream=None):
+    """fa_fwd_fp8 with K8, V8 of Hkv heads (H a multiple of Hkv); the same checks."""
+    fa_fwd_fp8(Q8, K8, V8, q_scales, k_scales, v_scales, O, L, scale, causal, stream)
 
 
 def _mask_args(block_mask, H):

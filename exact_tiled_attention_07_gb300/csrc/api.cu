@@ -453,14 +453,15 @@ fa_status fa_quantize_fp8(const void* X, void* X8, float* scales, int B, int H, 
   return launched(launch_quantize_fp8(a), "fa_quantize_fp8");
 }
 
-fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, const float* q_scales, const float* k_scales,
-                     const float* v_scales, void* O, float* L, int B, int H, int N, int d, float scale, int causal,
-                     fa_dtype out_dtype, void* stream) {
+fa_status fa_fwd_fp8_gqa(const void* Q8, const void* K8, const void* V8, const float* q_scales,
+                         const float* k_scales, const float* v_scales, void* O, float* L, int B, int H, int Hkv, int N,
+                         int d, float scale, int causal, fa_dtype out_dtype, void* stream) {
   if (out_dtype != FA_BF16 && out_dtype != FA_FP16)
     return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8 writes O as bf16 or fp16, not dtype %d", (int)out_dtype);
   bool empty;
   fa_status st = check_common(B, H, N, d, out_dtype, &empty);
   if (st != FA_OK || empty) return st;
+  if ((st = check_heads(H, Hkv)) != FA_OK) return st;
   if (!fwd_fp8_supported(d)) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8 supports d = 128, got %d", d);
   if ((st = check_ptrs({Q8, K8, V8, q_scales, k_scales, v_scales, O, L}, "fa_fwd_fp8")) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
@@ -484,7 +485,15 @@ fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, const float
   a.err = syms.err;
   a.counter = syms.counter;
   a.stream = static_cast<cudaStream_t>(stream);
+  a.group = H / Hkv;
   return launched(launch_fwd_fp8(a), "fa_fwd_fp8");
+}
+
+fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, const float* q_scales, const float* k_scales,
+                     const float* v_scales, void* O, float* L, int B, int H, int N, int d, float scale, int causal,
+                     fa_dtype out_dtype, void* stream) {
+  return fa_fwd_fp8_gqa(Q8, K8, V8, q_scales, k_scales, v_scales, O, L, B, H, H, N, d, scale, causal, out_dtype,
+                        stream);
 }
 
 fa_status fa_check_device_error(void* stream) {

@@ -271,7 +271,15 @@ FA_API fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, cons
                             int d, float scale, int causal, fa_dtype out_dtype, void* stream);
 
 /*
- * Synchronises `stream` and reports device-side failures/*
+ * fa_fwd_fp8 with grouped-query / multi-query attention: K8, V8 and their block scales hold
+ * Hkv heads ([B][Hkv][N][d], [B][Hkv][ceil(N / 128)]); query head h reads key/value head
+ * h / (H / Hkv). H must be a positive multiple of Hkv.
+ */
+FA_API fa_status fa_fwd_fp8_gqa(const void* Q8, const void* K8, const void* V8, const float* q_scales,
+                                const float* k_scales, const float* v_scales, void* O, float* L, int B, int H,
+                                int Hkv, int N, int d, float scale, int causal, fa_dtype out_dtype, void* stream);
+
+/*
  * Synchronises `stream` and reports device-side failures of earlier calls on the
  * current device: FA_ERR_CUDA for a CUDA error, FA_ERR_TIMEOUT / FA_ERR_DEVICE for a
  * failure a kernel recorded. The recorded failure is cleared.

@@ -182,3 +182,25 @@ def test_fp8_argument_checks(fa):
     s = torch.ones(1, dtype=torch.float32, device="cuda")
     with pytest.raises(fa.FAError, match="d = 128"):
         fa.attention_forward_fp8(z, z, z, s, s, s)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("h,hkv", [(4, 2), (4, 1)])
+def test_fp8_forward_grouped_query_heads(fa, causal, h, hkv):
+    """fa_fwd_fp8_gqa: query head i reads key/value head i / (H / Hkv); against the fp64 oracle
+    of grouped-query attention on the dequantised inputs."""
+    n = 300
+    q = _draw((2, h, n, 128), 70 + h + hkv)
+    k, v = (_draw((2, hkv, n, 128), 80 + i + hkv) for i in range(2))
+    (qc, qs), (kc, ks), (vc, vs) = (F8.quantize_blocks(t) for t in (q, k, v))
+    dev = [_codes_to_bytes(c).cuda() for c in (qc, kc, vc)] + [torch.from_numpy(x).cuda() for x in (qs, ks, vs)]
+    scale = 128 ** -0.5
+    o, lse = fa.attention_forward_fp8(*dev[:3], *dev[3:], scale=scale, causal=causal)
+    fa.fa_check_device_error()
+    deq = [F8.dequantize_blocks(c, x) for c, x in ((qc, qs), (kc, ks), (vc, vs))]
+    from oracle import gqa as G
+    o_ref, l_ref = G.attn_fwd64_gqa(deq[0], deq[1], deq[2], scale, causal)
+    _check_o(to_f64(o), o_ref, np.abs(deq[2]).max())
+    kx = np.repeat(deq[1], h // hkv, axis=1)
+    rows = list(np.ndindex(2, h, n))
+    _check_l(to_f64(lse).reshape(-1), l_ref.reshape(-1), _smax_rows(deq[0], kx, scale, causal, rows))
