@@ -514,16 +514,18 @@ def run_gpu(args, w: Workload):
     others = None
     if not args.no_targets and rank == 0:
         others = {}
-        for wname in ("gpt2m_fp16", "long_causal_bf16"):
+        for wname in ("gpt2m_fp16", "long_causal_bf16", "hd256_bf16"):
             ow = WORKLOADS[wname]
-            ox = make_inputs(ow)
+            ox = make_inputs(ow, with_do=not ow.fwd_only)
             od = {k_: _dev_tensor(v_, ow.dtype, device)[0] for k_, v_ in ox.items()}
             del ox
             oo = torch.empty_like(od["q"])
             ol = torch.empty((ow.B, ow.H, ow.N), dtype=torch.float32, device=device)
-            odq, odk, odv = torch.empty_like(od["q"]), torch.empty_like(od["k"]), torch.empty_like(od["v"])
-            ows = torch.empty(binding.fa_bwd_workspace_size(ow.B, ow.H, ow.N, ow.d), dtype=torch.uint8,
-                              device=device)
+            odq = odk = odv = ows = None
+            if not ow.fwd_only:
+                odq, odk, odv = torch.empty_like(od["q"]), torch.empty_like(od["k"]), torch.empty_like(od["v"])
+                ows = torch.empty(binding.fa_bwd_workspace_size(ow.B, ow.H, ow.N, ow.d), dtype=torch.uint8,
+                                  device=device)
 
             def ofwd():
                 binding.fa_fwd(od["q"], od["k"], od["v"], oo, ol, ow.scale, ow.causal)
@@ -533,7 +535,8 @@ def run_gpu(args, w: Workload):
 
             entry = {"config": workload_config(ow)}
             reps = max(3, min(args.steps, 10))
-            for pname, fns in (("fwd", (ofwd,)), ("bwd", (obwd,)), ("fwd+bwd", (ofwd, obwd))):
+            legs = (("fwd", (ofwd,)),) if ow.fwd_only else (("fwd", (ofwd,)), ("bwd", (obwd,)), ("fwd+bwd", (ofwd, obwd)))
+            for pname, fns in legs:
                 for _ in range(2):
                     for fn in fns:
                         fn()

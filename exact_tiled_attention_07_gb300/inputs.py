@@ -80,13 +80,24 @@ WORKLOADS = {
 
 def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bfloat16 (nearest, ties to even); returns the uint16 bit patterns."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    nan = np.isnan(x)
-    lsb = (u >> 16) & 1
-    r = ((u + np.uint32(0x7FFF) + lsb) >> 16).astype(np.uint16)
-    if nan.any():
-        r = np.where(nan, np.uint16(0x7FC0), r)
-    return r
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    flat_u = x.reshape(-1).view(np.uint32)
+    flat_x = x.reshape(-1)
+    r = np.empty(flat_u.shape, dtype=np.uint16)
+    step = 1 << 22  # slices small enough that the temporaries stay in cache
+    for i in range(0, flat_u.size, step):
+        u = flat_u[i:i + step]
+        t = u >> np.uint32(16)  # (u + 0x7FFF + lsb) >> 16
+        t &= np.uint32(1)
+        t += np.uint32(0x7FFF)
+        t += u
+        t >>= np.uint32(16)
+        ri = r[i:i + step]
+        ri[...] = t
+        nan = np.isnan(flat_x[i:i + step])
+        if nan.any():
+            ri[nan] = np.uint16(0x7FC0)
+    return r.reshape(x.shape)
 
 
 def f32_from_bf16_bits(bits: np.ndarray) -> np.ndarray:

@@ -31,3 +31,21 @@ def test_decode_inputs_are_seeded_and_rounded():
     assert not np.array_equal(a["k"], a["v"])
     w2 = DecodeWorkload("small", 2, 4, 2, 3, 50, 64, "bf16", 8)
     assert not np.array_equal(make_decode_inputs(w2)["q"], a["q"])
+
+
+def test_bf16_rounding_matches_torch():
+    """Round to nearest even, as torch's float32 -> bfloat16 conversion: random bit patterns
+    (every exponent, infinities, NaNs, subnormals) and exact ties."""
+    import torch
+
+    from exact_tiled_attention_07_gb300.inputs import bf16_bits_from_f32
+
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2**32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    ties = (rng.integers(0, 2**16, size=4096, dtype=np.uint64).astype(np.uint32) << 16) | np.uint32(0x8000)
+    x = np.concatenate([bits, ties]).view(np.float32)
+    ours = bf16_bits_from_f32(x)
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(x)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.all(ours[nan] == 0x7FC0)
