@@ -18,7 +18,9 @@
 // With NQ = 2 (d = 64, 128) the two query tiles ping-pong: while one warpgroup does its
 // softmax the tensor core runs the other tile's GEMMs (the interleave of "FlashAttention
 // and GPU memory" §11).  With NQ = 1 (d = 256: O alone fills half of TMEM) S is
-// double-buffered instead, so S_{j+1} is computed during the softmax of block j.
+// double-buffered instead, so S_{j+1} is computed during the softmax of block j; the ring then
+// holds 64-column blocks of the tiles, in the order the tensor core uses them (K0 K1 V0 K2 V1
+// ...), so that K_{j+2} streams in while P_j V_j runs.
 //
 // Lazy rescaling: the reference maximum m used in exp2(x - m) is only raised when the new
 // block maximum exceeds it by more than 8 (log2 units); until then P <= 2^8.  The final
@@ -61,7 +63,13 @@ struct FwdCfg {
   static constexpr int KB = D / 64;                 // 64-column (128-byte) blocks per row
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int TILE_BYTES = BN * D * 2;
-  static constexpr int STAGES = (D == 64) ? 8 : (D == 128 ? 4 : 2);
+  // ring entries: a whole K or V tile at d = 64, 128; at d = 256 one 64-column block of a tile
+  // (16 KB), so that the blocks of K are released one by one as their MMAs finish.  The d = 256
+  // ring holds two tiles (8 entries; 10 entries, with the tiles that wrap round the end split into
+  // N = 128 halves, ran 4-7 % slower)
+  static constexpr int RB = (D == 256) ? KB : 1;  // ring entries per tile
+  static constexpr int ENTRY_BYTES = TILE_BYTES / RB;
+  static constexpr int STAGES = (D == 64) ? 8 : (D == 128 ? 4 : 8);
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
   static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
   static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
@@ -73,7 +81,7 @@ struct FwdCfg {
   // shared memory
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = NQ * Q_BYTES;
-  static constexpr int OFF_BAR = OFF_RING + STAGES * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + STAGES * ENTRY_BYTES;
   static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 3 + 4;
   // after the barriers: TMEM base, abort flag, the two work-item slots
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 32;
@@ -293,6 +301,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   };
   // key tile at position t of an item's sequence
   auto tile_at = [&](int t) { return MASKED ? (int)jlist[t] : t; };
+  // order of an item's K and V tiles in the ring (n key tiles): K0 V0 K1 V1 ... with two query
+  // tiles (both tiles' GEMMs use a pair in turn); with one (S double-buffered) the order in which
+  // the tensor core uses them, K0 K1 V0 K2 V1 ... K(n-1) V(n-2) V(n-1), so that the ring is
+  // released and refilled first in, first out
+  auto ring_tile = [&](int idx, int n_, bool* is_v, int* j) {
+    if constexpr (C::NQ == 2) {
+      *is_v = idx & 1;
+      *j = idx >> 1;
+    } else if (idx == 0) {
+      *is_v = false;
+      *j = 0;
+    } else if (idx == 2 * n_ - 1) {
+      *is_v = true;
+      *j = n_ - 1;
+    } else {
+      *is_v = !(idx & 1);
+      *j = (idx & 1) ? (idx + 1) >> 1 : (idx - 2) >> 1;
+    }
+  };
+  // ring positions of K_j and V_j within the item (the inverse of ring_tile)
+  auto k_pos = [&](int j, int n_) { return C::NQ == 2 ? 2 * j : (j == 0 ? 0 : 2 * j - 1); };
+  auto v_pos = [&](int j, int n_) { return C::NQ == 2 ? 2 * j + 1 : (j == n_ - 1 ? 2 * n_ - 1 : 2 * j + 2); };
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
@@ -325,16 +355,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             tma_load_3d(smem + C::OFF_Q + q * C::Q_BYTES + kb * (BM * 128), &tm_q, B.q_full, kb * 64,
                         w.qrow0 + q * BM, w.head);
         ++q_loads;
-        for (int idx = 0; idx < 2 * nmax; ++idx) {
-          const uint32_t g = ring_pos;
-          const int slot = g % C::STAGES, use = g / C::STAGES;
-          if (use > 0 && !(ok = mbar_wait(B.kv_empty + slot, (use - 1) & 1, ctx, 10))) break;
-          mbar_arrive_expect_tx(B.kv_full + slot, C::TILE_BYTES);
-          uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
-          const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, kb * 64, tile_at(idx >> 1) * BN, w.kvhead);
-          ++ring_pos;
+        for (int idx = 0; ok && idx < 2 * nmax; ++idx) {
+          bool is_v;
+          int j;
+          ring_tile(idx, nmax, &is_v, &j);
+          const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+          for (int e = 0; e < C::RB; ++e) {
+            const uint32_t g = ring_pos;
+            const int slot = g % C::STAGES, use = g / C::STAGES;
+            if (use > 0 && !(ok = mbar_wait(B.kv_empty + slot, (use - 1) & 1, ctx, 10))) break;
+            mbar_arrive_expect_tx(B.kv_full + slot, C::ENTRY_BYTES);
+            uint8_t* dst = smem + C::OFF_RING + slot * C::ENTRY_BYTES;
+            constexpr int kbs = C::KB / C::RB;  // 64-column blocks per entry
+            for (int kb = 0; kb < kbs; ++kb)
+              tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, (e * kbs + kb) * 64, tile_at(j) * BN,
+                          w.kvhead);
+            ++ring_pos;
+          }
         }
       }
       // drain: every copy this thread started must land before the CTA may exit
@@ -356,50 +393,96 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const uint32_t idesc_pv = make_idesc_f16(BM, D, BF16, false, true);
       const uint32_t q_base = smem_u32(smem + C::OFF_Q);
       const uint32_t ring = smem_u32(smem + C::OFF_RING);
-      uint32_t ring_pos = 0;    // ring entry of the item's first K tile (all items so far)
+      uint32_t ring_pos = 0;    // ring entry of the item's first tile (all items so far)
       int tq[2] = {0, 0};       // key tiles processed by each query tile (all items): P phases
       int oq[2] = {0, 0};       // items with a result for each query tile: O phases
       int items = 0;
-      auto slot_of = [&](int idx) { return (int)((ring_pos + idx) % C::STAGES); };
+      // ring slot of entry e of the tile at position idx of the item
+      auto slot_of = [&](int idx, int e = 0) { return (int)((ring_pos + idx * C::RB + e) % C::STAGES); };
       auto wait = [&](uint64_t* b, uint32_t parity, uint32_t site) {
         return __all_sync(0xffffffffu, mbar_wait(b, parity, ctx, site));
       };
+      // every entry of the tile at position idx has landed
       auto wait_full = [&](int idx) {
-        return wait(B.kv_full + slot_of(idx), ((ring_pos + idx) / C::STAGES) & 1, 20);
+        bool good = true;
+#pragma unroll
+        for (int e = 0; e < C::RB; ++e)
+          good = good && wait(B.kv_full + slot_of(idx, e), ((ring_pos + idx * C::RB + e) / C::STAGES) & 1, 20);
+        return good;
       };
       auto commit = [&](uint64_t* b) {
         if (leader) umma_commit(b);
         __syncwarp();
       };
-      // S = Q_q K^T into TMEM columns s_col
+      // S = Q_q K^T into TMEM columns s_col.  With block entries (d = 256) each 64-column block
+      // of K is released as soon as its four MMAs are done.
       auto issue_qk = [&](int q, int kidx, uint32_t s_col) {
-        const uint32_t kt = ring + slot_of(kidx) * C::TILE_BYTES;
         const uint32_t qt = q_base + q * C::Q_BYTES;
-        uint64_t ad[D / 16], bd[D / 16];
+        if constexpr (C::RB == 1) {
+          const uint32_t kt = ring + slot_of(kidx) * C::ENTRY_BYTES;
+          uint64_t ad[D / 16], bd[D / 16];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int k0 = kk * 16;
-          ad[kk] = make_sdesc_sw128(qt + (k0 / 64) * (BM * 128) + (k0 % 64) * 2, 16, 1024);
-          bd[kk] = make_sdesc_sw128(kt + (k0 / 64) * (BN * 128) + (k0 % 64) * 2, 16, 1024);
-        }
-        if (leader) {
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int k0 = kk * 16;
+            ad[kk] = make_sdesc_sw128(qt + (k0 / 64) * (BM * 128) + (k0 % 64) * 2, 16, 1024);
+            bd[kk] = make_sdesc_sw128(kt + (k0 / 64) * (BN * 128) + (k0 % 64) * 2, 16, 1024);
+          }
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + s_col, ad[kk], bd[kk], idesc_qk, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + s_col, ad[kk], bd[kk], idesc_qk, kk > 0);
+          }
+          __syncwarp();
+        } else {
+#pragma unroll
+          for (int e = 0; e < C::RB; ++e) {
+            const int slot = slot_of(kidx, e);
+            const uint32_t kt = ring + slot * C::ENTRY_BYTES;
+            uint64_t ad[4], bd[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              ad[i] = make_sdesc_sw128(qt + e * (BM * 128) + i * 32, 16, 1024);
+              bd[i] = make_sdesc_sw128(kt + i * 32, 16, 1024);
+            }
+            if (leader) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) umma_ss(tbase + s_col, ad[i], bd[i], idesc_qk, (e > 0 || i > 0) ? 1u : 0u);
+              umma_commit(B.kv_empty + slot);
+            }
+            __syncwarp();
+          }
         }
-        __syncwarp();
       };
-      // O += P V with P (16-bit, packed pairs) in TMEM columns [p_col, p_col + 64)
+      // O += P V with P (16-bit, packed pairs) in TMEM columns [p_col, p_col + 64).  With block
+      // entries (d = 256) a tile starts at a multiple of its entries and the ring holds a whole
+      // number of tiles, so the blocks of V are adjacent (one N = 256 MMA per 16 keys, as for a
+      // whole tile); they are released together.
       auto issue_pv = [&](uint32_t o_col, uint32_t p_col, int vidx, bool acc) {
-        const uint32_t vt = ring + slot_of(vidx) * C::TILE_BYTES;
-        uint64_t bd[BN / 16];
+        if constexpr (C::RB == 1) {
+          const uint32_t vt = ring + slot_of(vidx) * C::ENTRY_BYTES;
+          uint64_t bd[BN / 16];
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) bd[kk] = make_sdesc_sw128(vt + kk * 2048, BN * 128, 1024);
-        if (leader) {
+          for (int kk = 0; kk < BN / 16; ++kk) bd[kk] = make_sdesc_sw128(vt + kk * 2048, BN * 128, 1024);
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            umma_ts(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BN / 16; ++kk)
+              umma_ts(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          }
+          __syncwarp();
+        } else {
+          static_assert(C::STAGES % C::RB == 0, "a tile's blocks never wrap round the ring");
+          const uint32_t vt = ring + slot_of(vidx, 0) * C::ENTRY_BYTES;
+          uint64_t bd[BN / 16];
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) bd[kk] = make_sdesc_sw128(vt + kk * 2048, C::ENTRY_BYTES, 1024);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              umma_ts(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int e = 0; e < C::RB; ++e) umma_commit(B.kv_empty + slot_of(vidx, e));
+          }
+          __syncwarp();
         }
-        __syncwarp();
       };
       // the first P V of query tile q in an item overwrites O_q: the softmax must have read it
       auto o_free = [&](int q) { return oq[q] == 0 || wait(B.o_empty + q, (oq[q] - 1) & 1, 26 + q); };
@@ -451,36 +534,33 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const int nb = nq[0];
           auto buf = [&](int j) { return ((tq[0] + j) & 1) ? C::S_COL1 : C::S_COL0; };
           for (int j = 0; ok && j < 2 && j < nb; ++j) {
-            if (!(ok = wait_full(2 * j))) break;
+            if (!(ok = wait_full(k_pos(j, nb)))) break;
             tc_fence_after();
-            issue_qk(0, 2 * j, buf(j));
+            issue_qk(0, k_pos(j, nb), buf(j));  // releases K_j's ring entries
             commit(B.s_full + ((tq[0] + j) & 1));
-            commit(B.kv_empty + slot_of(2 * j));
           }
           if (ok && nb <= 2) commit(B.q_empty);
           for (int j = 0; ok && j < nb; ++j) {
-            const int vidx = 2 * j + 1;
+            const int vidx = v_pos(j, nb);
             const int t = tq[0] + j;
             if (!(ok = wait_full(vidx))) break;
             if (!(ok = wait(B.p_full + (t & 1), (t >> 1) & 1, 24))) break;
             if (j == 0 && !(ok = o_free(0))) break;
             tc_fence_after();
-            issue_pv(C::O_COL0, buf(j), vidx, j > 0);
+            issue_pv(C::O_COL0, buf(j), vidx, j > 0);  // releases V_j's ring entries
             commit(B.pv_done);
-            commit(B.kv_empty + slot_of(vidx));
             if (j + 2 < nb) {
-              const int kidx = 2 * (j + 2);
+              const int kidx = k_pos(j + 2, nb);
               if (!(ok = wait_full(kidx))) break;
               tc_fence_after();
               issue_qk(0, kidx, buf(j));  // in order after P_j V_j, which reads this buffer
               commit(B.s_full + (t & 1));
-              commit(B.kv_empty + slot_of(kidx));
               if (j + 2 == nb - 1) commit(B.q_empty);
             }
             if (j == nb - 1) commit(B.o_full + 0);
           }
         }
-        ring_pos += 2 * nmax;
+        ring_pos += 2 * nmax * C::RB;
         for (int q = 0; q < 2; ++q) {
           tq[q] += nq[q];
           oq[q] += nq[q] > 0 ? 1 : 0;
