@@ -8,8 +8,8 @@ for causal).  Inputs are larger than L2 (each [B,H,N,d] tensor is 134 MB).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU oracle (the
-reference arm of this build) on a bounded sample of the same workload.
+Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU oracle (there is no reference code
+to run, so the oracle is the reference arm) on a bounded sample of the same workload.
 """
 
 from __future__ import annotations
@@ -152,7 +152,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle arm (the reference of this build) and the cpu_baseline leg
+# CPU oracle arm (the reference arm) and the cpu_baseline leg
 # ---------------------------------------------------------------------------
 
 
