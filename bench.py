@@ -178,7 +178,7 @@ def oracle_heads(w: Workload, target_s: float, max_heads: int):
     return heads, elapsed
 
 
-def oracle_sample(w: Workload, target_s: float = 12.0, max_heads: int = 16):
+def oracle_sample(w: Workload, target_s: float = 12.0, max_heads: int = 64):
     """The cpu_baseline leg: the oracle as it stands, on whole heads of the workload (~target_s)."""
     heads, elapsed = oracle_heads(w, target_s, max_heads)
     pass_ = "fwd" if w.fwd_only else "fwd+bwd"
