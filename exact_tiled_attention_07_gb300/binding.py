@@ -141,6 +141,33 @@ def _dt(t):
         raise ValueError(f"unsupported dtype {t.dtype}") from None
 
 
+def _on_device(*ts):
+    """Every tensor given (None is skipped) is a contiguous CUDA tensor on the current device:
+    the library takes raw device pointers and launches on the current device, so a host tensor
+    or one on another GPU would hand the kernels an address they cannot use."""
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("device arguments must be CUDA tensors (the library takes device pointers)")
+        if not t.is_contiguous():
+            raise ValueError("device arguments must be contiguous")
+        if dev is None:
+            dev, cur = t.device.index, torch.cuda.current_device()
+            if dev != cur:
+                raise ValueError(f"tensors are on cuda:{dev} but the current device is cuda:{cur}; "
+                                 f"call within torch.cuda.device({dev})")
+        elif t.device.index != dev:
+            raise ValueError("all device arguments must be on one GPU")
+
+
+def _rows(L, n, what="L"):
+    """L (or another per-row vector) is an fp32 tensor of n elements."""
+    if L.dtype != torch.float32 or L.numel() != n:
+        raise ValueError(f"{what} must be an fp32 tensor of {n} elements")
+
+
 def _same(ref, *ts):
     for t in ts:
         if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device or not t.is_contiguous():
@@ -149,6 +176,7 @@ def _same(ref, *ts):
 
 def fa_fwd(Q, K, V, O, L, scale, causal, stream=None):
     B, H, N, d = _shape4(Q)
+    _on_device(Q, K, V, O, L)
     _same(Q, K, V, O)
     if L.dtype != torch.float32 or L.numel() != B * H * N or not L.is_contiguous():
         raise ValueError("L must be a contiguous fp32 tensor of B*H*N elements")
@@ -170,6 +198,7 @@ def _kv_heads(Q, K, V, *kv_like):
 
 def fa_fwd_gqa(Q, K, V, O, L, scale, causal, stream=None):
     B, H, N, d = _shape4(Q)
+    _on_device(Q, K, V, O, L)
     Hkv = _kv_heads(Q, K, V)
     _same(Q, O)
     if L.dtype != torch.float32 or L.numel() != B * H * N or not L.is_contiguous():
@@ -180,8 +209,10 @@ def fa_fwd_gqa(Q, K, V, O, L, scale, causal, stream=None):
 
 def fa_bwd_gqa(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, stream=None):
     B, H, N, d = _shape4(Q)
+    _on_device(Q, K, V, O, dO, L, dQ, dK, dV, workspace)
     Hkv = _kv_heads(Q, K, V, dK, dV)
     _same(Q, O, dO, dQ)
+    _rows(L, B * H * N)
     _check(load_library().fa_bwd_gqa(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV),
                                      _p(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
                                      float(scale), int(bool(causal)), _dt(Q), _stream(stream)))
@@ -193,7 +224,9 @@ def fa_bwd_workspace_size(B, H, N, d) -> int:
 
 def fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, stream=None):
     B, H, N, d = _shape4(Q)
+    _on_device(Q, K, V, O, dO, L, dQ, dK, dV, workspace)
     _same(Q, K, V, O, dO, dQ, dK, dV)
+    _rows(L, B * H * N)
     _check(load_library().fa_bwd(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV), _p(workspace),
                                  workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
                                  int(bool(causal)), _dt(Q), _stream(stream)))
@@ -201,7 +234,9 @@ def fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, stream=None)
 
 def fa_bwd_preprocess(O, dO, L, workspace, stream=None):
     B, H, N, d = _shape4(O)
+    _on_device(O, dO, L, workspace)
     _same(O, dO)
+    _rows(L, B * H * N)
     _check(load_library().fa_bwd_preprocess(_p(O), _p(dO), _p(L), _p(workspace),
                                             workspace.numel() * workspace.element_size(), B, H, N, d, _dt(O),
                                             _stream(stream)))
@@ -209,6 +244,7 @@ def fa_bwd_preprocess(O, dO, L, workspace, stream=None):
 
 def fa_bwd_main(Q, K, V, dO, dK, dV, workspace, scale, causal, stream=None):
     B, H, N, d = _shape4(Q)
+    _on_device(Q, K, V, dO, dK, dV, workspace)
     _same(Q, K, V, dO, dK, dV)
     _check(load_library().fa_bwd_main(_p(Q), _p(K), _p(V), _p(dO), _p(dK), _p(dV), _p(workspace),
                                       workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
@@ -217,6 +253,7 @@ def fa_bwd_main(Q, K, V, dO, dK, dV, workspace, scale, causal, stream=None):
 
 def fa_bwd_dq_convert(workspace, dQ, scale, stream=None):
     B, H, N, d = _shape4(dQ)
+    _on_device(workspace, dQ)
     _check(load_library().fa_bwd_dq_convert(_p(workspace), workspace.numel() * workspace.element_size(), _p(dQ),
                                             B, H, N, d, float(scale), _dt(dQ), _stream(stream)))
 
@@ -224,7 +261,9 @@ def fa_bwd_dq_convert(workspace, dQ, scale, stream=None):
 def fa_bwd_noalloc(Q, K, V, O, dO, L, dQ, dK, dV, scale, causal, stream=None):
     """fa_bwd with the library's static device scratch instead of a workspace (no allocation)."""
     B, H, N, d = _shape4(Q)
+    _on_device(Q, K, V, O, dO, L, dQ, dK, dV)
     _same(Q, K, V, O, dO, dQ, dK, dV)
+    _rows(L, B * H * N)
     _check(load_library().fa_bwd_noalloc(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV), B, H, N,
                                          d, float(scale), int(bool(causal)), _dt(Q), _stream(stream)))
 
@@ -253,6 +292,7 @@ def fa_fwd_bwd_host(Q, K, V, dO, O, L, dQ, dK, dV, workspace, scale, causal, chu
         raise ValueError("L must be an fp32 tensor of B*H*N elements")
     if workspace.device.type != "cuda":
         raise ValueError("the workspace is device memory")
+    _on_device(workspace)
     _check(load_library().fa_fwd_bwd_host(_p(Q), _p(K), _p(V), _p(dO), _p(O), _p(L), _p(dQ), _p(dK), _p(dV),
                                           _p(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N,
                                           d, float(scale), int(bool(causal)), _dt(Q), int(chunk), _stream(stream)))
@@ -266,6 +306,7 @@ def fa_decode(Q, K, V, O, L, scale, splits=0, workspace=None, stream=None):
     """Decode: Q, O [B, H, Nq, d] against the cache K, V [B, Hkv, Nk, d]; L [B, H, Nq]."""
     B, H, Nq, d = _shape4(Q)
     Bk, Hkv, Nk, dk = _shape4(K)
+    _on_device(Q, K, V, O, L, workspace)
     if (Bk, dk) != (B, d) or V.shape != K.shape or V.dtype != Q.dtype or K.dtype != Q.dtype or not V.is_contiguous():
         raise ValueError("K, V must be [B, Hkv, Nk, d] of Q's dtype")
     _same(Q, O)
@@ -280,6 +321,7 @@ def fa_quantize_fp8(X, X8, scales, stream=None):
     """Block quantisation of X [B, H, N, d] to E4M3 codes X8 (uint8, same shape) and
     scales [B, H, ceil(N / 128)] fp32."""
     B, H, N, d = _shape4(X)
+    _on_device(X, X8, scales)
     if X8.dtype != torch.uint8 or tuple(X8.shape) != (B, H, N, d) or not X8.is_contiguous():
         raise ValueError("X8 must be a contiguous uint8 tensor of X's shape")
     nb = (N + 127) // 128
@@ -293,6 +335,7 @@ def fa_fwd_fp8(Q8, K8, V8, q_scales, k_scales, v_scales, O, L, scale, causal, st
     K8, V8 (and their scales) may have fewer heads than Q8 (grouped-query: fa_fwd_fp8_gqa)."""
     B, H, N, d = _shape4(Q8)
     Hkv = _shape4(K8)[1]
+    _on_device(Q8, K8, V8, q_scales, k_scales, v_scales, O, L)
     nb = (N + 127) // 128
     for t, heads in ((Q8, H), (K8, Hkv), (V8, Hkv)):
         if t.dtype != torch.uint8 or tuple(t.shape) != (B, heads, N, d) or not t.is_contiguous():
@@ -333,8 +376,10 @@ def _mask_args(block_mask, H):
 def fa_fwd_masked(Q, K, V, O, L, scale, causal, window=0, block_mask=None, stream=None):
     """Forward with a sliding window and/or a block mask over 128 x 128 score blocks."""
     B, H, N, d = _shape4(Q)
-    _, Hkv, _, _ = _shape4(K)
+    _on_device(Q, K, V, O, L, block_mask)
+    Hkv = _kv_heads(Q, K, V)
     _same(Q, O)
+    _rows(L, B * H * N)
     mp, mh = _mask_args(block_mask, H)
     _check(load_library().fa_fwd_masked(_p(Q), _p(K), _p(V), _p(O), _p(L), B, H, Hkv, N, d, float(scale),
                                         int(bool(causal)), int(window), mp, mh, _dt(Q), _stream(stream)))
@@ -343,8 +388,10 @@ def fa_fwd_masked(Q, K, V, O, L, scale, causal, window=0, block_mask=None, strea
 def fa_bwd_masked(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, window=0, block_mask=None, stream=None):
     """Backward of fa_fwd_masked (same mask)."""
     B, H, N, d = _shape4(Q)
-    _, Hkv, _, _ = _shape4(K)
+    _on_device(Q, K, V, O, dO, L, dQ, dK, dV, workspace, block_mask)
+    Hkv = _kv_heads(Q, K, V, dK, dV)
     _same(Q, O, dO, dQ)
+    _rows(L, B * H * N)
     mp, mh = _mask_args(block_mask, H)
     nbytes = workspace.numel() * workspace.element_size()
     _check(load_library().fa_bwd_masked(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(L), _p(dQ), _p(dK), _p(dV),
