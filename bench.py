@@ -90,7 +90,7 @@ def profiled_traffic(kernel_key, workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms; summary() keeps the timed window."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms; summary() keeps the timed window."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -106,7 +106,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, FileNotFoundError):
@@ -149,6 +149,39 @@ class ClockSampler:
         reasons = sorted({nm for p in window for nm, v in zip(names, p[3]) if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(p[1] for p in window), "sm_max_mhz": max(p[2] for p in window),
                 "reasons": reasons, "samples": len(window), "note": note}
+
+
+# Dense 16-bit tensor-core work per SM per clock: one 128 x N x 16 MMA every N / 2 cycles, i.e.
+# 4096 multiply-adds (the published dense bf16 rate, 2.25 PFLOP/s on 148 SMs at about 1.86 GHz).
+TENSOR_FLOP_PER_SM_CLOCK = 8192
+# A timed region shorter than this is a burst: the kernel is compared with the burst peak.
+BURST_REGION_S = 1.0
+
+
+def sm_clock_mhz(before, after):
+    """Per-SM mean clock (MHz) between two fa_sm_clock_sample readings (rows of SM id, cycle
+    counter, global timer in ns): for each SM seen in both, cycles elapsed over ns elapsed."""
+    first = {int(r[0]): (int(r[1]), int(r[2])) for r in before}
+    out = []
+    for r in after:
+        sm = int(r[0])
+        if sm in first and int(r[2]) > first[sm][1]:
+            out.append(1e3 * (int(r[1]) - first[sm][0]) / (int(r[2]) - first[sm][1]))
+    return out
+
+
+def peak_for_region(peaks, region_s):
+    """(peak TFLOP/s, which one): the burst cuBLAS figure for a region shorter than
+    BURST_REGION_S, the sustained (seconds-long, power-capped) figure otherwise."""
+    if region_s < BURST_REGION_S:
+        return float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), "bf16_tflops (burst)"
+    return float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])), \
+        "bf16_tflops_sustained (seconds-long region)"
+
+
+def tensor_peak_at_clock(sm_mhz, n_sm):
+    """Dense 16-bit tensor peak (TFLOP/s) of n_sm SMs at the given clock."""
+    return n_sm * TENSOR_FLOP_PER_SM_CLOCK * sm_mhz * 1e6 / 1e12
 
 
 # ---------------------------------------------------------------------------
@@ -365,13 +398,19 @@ def run_gpu(args, w: Workload):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    # every SM's cycle counter read just before and just after the timed region (outside its
+    # events): each SM's mean clock over exactly the timed steps
+    n_sm = torch.cuda.get_device_properties(device).multi_processor_count
+    smc = [torch.zeros(3 * n_sm, dtype=torch.int64, device=device) for _ in range(2)]
     with ClockSampler(local) as clocks:
         time.sleep(0.5)  # let the sampler start
         wall0 = time.time()
+        binding.fa_sm_clock_sample(smc[0], stream)
         t_start.record(stream)
         for s_ in range(args.steps):
             step(ev[s_])
         t_end.record(stream)
+        binding.fa_sm_clock_sample(smc[1], stream)
         torch.cuda.synchronize()
         wall1 = time.time()
     if dist:
@@ -389,6 +428,10 @@ def run_gpu(args, w: Workload):
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    region_s = total_ms * 1e-3
+    peak, peak_kind = peak_for_region(peaks, region_s)
+    mhz = sm_clock_mhz(smc[0].cpu().numpy().reshape(-1, 3), smc[1].cpu().numpy().reshape(-1, 3))
+    sm_mhz_dev = statistics.median(mhz) if mhz else None
 
     # ---------------- roofline of the dominant kernel
     kflops = {"fwd": attention_flops(w.B, w.H, w.N, w.d, w.causal, "fwd"),
@@ -396,53 +439,63 @@ def run_gpu(args, w: Workload):
     dom = max((nm for nm in per_kernel if nm in kflops), key=lambda nm: per_kernel[nm])
     achieved = kflops[dom] / (per_kernel[dom] * 1e-3) / 1e12
     traffic = profiled_traffic(dom, w.name)
-    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} {peak_kind}: the timed region lasted {region_s:.3f} s",
                 "share_of_step": per_kernel[dom] / ms_per_step}
+    if sm_mhz_dev:
+        at_clock = tensor_peak_at_clock(sm_mhz_dev, n_sm)
+        roofline.update({"frac_at_clock": achieved / at_clock, "peak_at_clock": at_clock,
+                         "peak_at_clock_source": f"{n_sm} SMs x {TENSOR_FLOP_PER_SM_CLOCK} FLOP/clock x "
+                                                 f"{sm_mhz_dev:.0f} MHz (median SM clock over the timed region, "
+                                                 f"from each SM's cycle counter)"})
 
     # ---------------- end to end: pinned host buffers -> device, the C-ABI calls, results -> host
-    h2d = sum(pinned[k_].numel() * pinned[k_].element_size() for k_ in pinned)
-    outs = [o, lse] + ([] if w.fwd_only else [dq, dk, dv])
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    d2h = sum(t.numel() * t.element_size() for t in outs)
-    ins = [(dev[k_], pinned[k_]) for k_ in pinned]
-    if not w.fwd_only:
-        # one C-ABI call over the host buffers: chunks of heads copied in, computed and copied
-        # out on the library's streams, overlapping the copies of one chunk with its neighbours'
-        # computation
-        ws_host = torch.empty(binding.fa_fwd_bwd_host_workspace_size(w.B, w.H, w.H, w.N, w.d, q.dtype,
-                                                                     args.e2e_chunk),
-                              dtype=torch.uint8, device=device)
+    def measure_e2e():
+        h2d = sum(pinned[k_].numel() * pinned[k_].element_size() for k_ in pinned)
+        outs = [o, lse] + ([] if w.fwd_only else [dq, dk, dv])
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+        ins = [(dev[k_], pinned[k_]) for k_ in pinned]
+        if not w.fwd_only:
+            # one C-ABI call over the host buffers: chunks of heads copied in, computed and copied
+            # out on the library's streams, overlapping the copies of one chunk with its neighbours'
+            # computation
+            ws_host = torch.empty(binding.fa_fwd_bwd_host_workspace_size(w.B, w.H, w.H, w.N, w.d, q.dtype,
+                                                                         args.e2e_chunk),
+                                  dtype=torch.uint8, device=device)
 
-        def e2e_step():
-            binding.fa_fwd_bwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["do"], *host_out, ws_host, scale,
-                                    causal, args.e2e_chunk, stream)
-    else:
-        def e2e_step():
-            for d_, h_ in ins:
-                d_.copy_(h_, non_blocking=True)
-            step()
-            for h_, d_ in zip(host_out, outs):
-                h_.copy_(d_, non_blocking=True)
+            def e2e_step():
+                binding.fa_fwd_bwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["do"], *host_out, ws_host, scale,
+                                        causal, args.e2e_chunk, stream)
+        else:
+            def e2e_step():
+                for d_, h_ in ins:
+                    d_.copy_(h_, non_blocking=True)
+                step()
+                for h_, d_ in zip(host_out, outs):
+                    h_.copy_(d_, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    e_s.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e_e.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e_s.elapsed_time(e_e) / args.steps
-    e2e_ms = max_over_ranks(e2e_ms, dist, device)
-    e2e = {"value": aggregate_tflops(flops_rank, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "call": "fa_fwd_bwd_host" if not w.fwd_only else "copies + fa_fwd",
-           "chunk_kv_heads": args.e2e_chunk if not w.fwd_only else None}
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        e_s.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e_e.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e_s.elapsed_time(e_e) / args.steps
+        e2e_ms = max_over_ranks(e2e_ms, dist, device)
+        e2e = {"value": aggregate_tflops(flops_rank, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "call": "fa_fwd_bwd_host" if not w.fwd_only else "copies + fa_fwd",
+               "chunk_kv_heads": args.e2e_chunk if not w.fwd_only else None}
+        return e2e
+
+    e2e = None if args.no_e2e else measure_e2e()
 
     # ---------------- per-pass figures, including the non-causal variant of the same shape
     targets = None
@@ -549,7 +602,8 @@ def run_gpu(args, w: Workload):
                 torch.cuda.synchronize()
                 ms = a_.elapsed_time(b_) / reps
                 tf = attention_flops(ow.B, ow.H, ow.N, ow.d, ow.causal, pname) / (ms * 1e-3) / 1e12
-                entry[pname] = {"ms": ms, "tflops": tf, "pct_of_sustained_peak": 100 * tf / peak_sus}
+                entry[pname] = {"ms": ms, "tflops": tf, "pct_of_burst_peak": 100 * tf / peak_burst,
+                                "pct_of_sustained_peak": 100 * tf / peak_sus}
             others[wname] = entry
             del od, oo, ol, odq, odk, odv, ows
         binding.fa_check_device_error()
@@ -567,9 +621,14 @@ def run_gpu(args, w: Workload):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": workload_config(w),
                 "pct_of_peak": {"sustained": 100 * value / world / peak_sus, "burst": 100 * value / world / peak_burst,
+                                "at_clock": (100 * value / world / tensor_peak_at_clock(sm_mhz_dev, n_sm)
+                                             if sm_mhz_dev else None),
                                 "source": peak_src},
                 "kernels_ms": per_kernel, "gpu_launches": len(names) * args.steps, "roofline": roofline,
-                "e2e": e2e, "clocks": clocks.summary(wall0, wall1), "cpu_baseline": cpu, "targets": targets,
+                "e2e": e2e, "clocks": dict(clocks.summary(wall0, wall1), sm_mhz_device=sm_mhz_dev,
+                                           sm_mhz_device_range=[min(mhz), max(mhz)] if mhz else None,
+                                           sm_seen=len(mhz)),
+                "cpu_baseline": cpu, "targets": targets,
                 "other_workloads": others, "decode": decode}
         print(json.dumps(line), flush=True)
     if dist:
@@ -586,6 +645,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-targets", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
     ap.add_argument("--e2e-chunk", type=int, default=0,
                     help="key/value heads per chunk of the end-to-end host-buffer call (0: automatic)")
     args = ap.parse_args()

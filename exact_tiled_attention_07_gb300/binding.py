@@ -24,6 +24,7 @@ __all__ = [
     "fa_selftest_bounded_wait", "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size",
     "attention_forward", "attention_backward", "attention_decode",
     "attention_forward_fp8", "quantize_fp8", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
+    "fa_sm_clock_sample",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_status_string",
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
     "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_fp8_gqa", "fa_fwd_masked", "fa_bwd_masked",
-    "fa_selftest_bounded_wait", "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size",
+    "fa_selftest_bounded_wait", "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size", "fa_sm_clock_sample",
 )
 
 _lib = None
@@ -90,6 +91,7 @@ def load_library():
         lib.fa_fwd_bwd_host_workspace_size.restype = sz
         lib.fa_fwd_bwd_host.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
+        lib.fa_sm_clock_sample.argtypes = [vp, i, vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
         lib.fa_uses_tensor_cores.argtypes = [i, i, i]
         lib.fa_status_string.argtypes = [i]
@@ -101,7 +103,7 @@ def load_library():
                      "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait", "fa_fwd_bwd_host",
                      "fa_bwd_noalloc", "fa_bwd_preprocess",
                      "fa_bwd_main", "fa_bwd_dq_convert",
-                     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores"):
+                     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_sm_clock_sample"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -402,6 +404,15 @@ def fa_bwd_masked(Q, K, V, O, dO, L, dQ, dK, dV, workspace, scale, causal, windo
 def fa_selftest_bounded_wait(timeout_ms=20, arrive=False, stream=None):
     """Launch the bounded-wait self-test (see include/fa.h); read the outcome with fa_check_device_error."""
     _check(load_library().fa_selftest_bounded_wait(int(timeout_ms), int(bool(arrive)), _stream(stream)))
+
+
+def fa_sm_clock_sample(out, stream=None):
+    """Enqueue one reading of every SM's cycle counter and the global timer into ``out``, a CUDA
+    uint64 (or int64) tensor of 3 x blocks elements, blocks <= the SM count (see include/fa.h)."""
+    _on_device(out)
+    if out.element_size() != 8 or out.numel() % 3 != 0:
+        raise ValueError("out must hold 3 x blocks 64-bit words")
+    _check(load_library().fa_sm_clock_sample(_p(out), out.numel() // 3, _stream(stream)))
 
 
 def fa_check_device_error(stream=None):

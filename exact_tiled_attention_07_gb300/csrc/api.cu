@@ -1,5 +1,7 @@
 // C ABI (include/fa.h): argument validation, workspace carving, kernel selection.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
@@ -31,13 +33,16 @@ fa_status fail(fa_status s, const char* fmt, ...) {
 struct DeviceSyms {
   unsigned long long* err = nullptr;
   unsigned long long* counter = nullptr;
+  unsigned long long ctx = 0;  // id of the context the addresses belong to
 };
 
 constexpr int kMaxDevices = 64;
 DeviceSyms g_syms[kMaxDevices];
 std::mutex g_syms_mu;
 
-// Device addresses of the file-scope device symbols for the current device.
+// Device addresses of the file-scope device symbols for the current device, looked up again
+// whenever the current context is not the one they were taken in (a device reset destroys the
+// primary context, and the next one may place the library's module elsewhere).
 fa_status device_syms(DeviceSyms* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -45,7 +50,8 @@ fa_status device_syms(DeviceSyms* out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d out of range", dev);
   std::lock_guard<std::mutex> lk(g_syms_mu);
   DeviceSyms& s = g_syms[dev];
-  if (!s.err) {
+  const unsigned long long ctx = current_context_id();
+  if (!s.err || ctx == 0 || ctx != s.ctx) {
     void* p = nullptr;
     if ((e = cudaGetSymbolAddress(&p, g_err_word)) != cudaSuccess)
       return fail(FA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
@@ -54,14 +60,13 @@ fa_status device_syms(DeviceSyms* out) {
       return fail(FA_ERR_CUDA, "cudaGetSymbolAddress(tile counter): %s", cudaGetErrorString(e));
     s.counter = static_cast<unsigned long long*>(c);
     s.err = static_cast<unsigned long long*>(p);
+    s.ctx = current_context_id();  // the lookup made the device's context current if none was
   }
   *out = s;
   return FA_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int elem_bytes(fa_dtype dt) { return dt == FA_FP32 ? 4 : 2; }
 
 // Shared shape/pointer checks. Returns FA_OK and sets *empty when there is nothing to do.
 fa_status check_common(int B, int H, int N, int d, fa_dtype dt, bool* empty) {
@@ -121,6 +126,28 @@ fa_status carve(BwdArgs* a, void* ws, size_t ws_bytes, int B, int H, int N, int 
 }
 
 }  // namespace
+
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 int device_sm_count() {
   static int cached[kMaxDevices] = {};
@@ -526,6 +553,13 @@ fa_status fa_selftest_bounded_wait(int timeout_ms, int arrive, void* stream) {
   if (st != FA_OK) return st;
   return launched(launch_bounded_wait_selftest(syms.err, timeout_ms, arrive ? 1 : 0, static_cast<cudaStream_t>(stream)),
                   "fa_selftest_bounded_wait");
+}
+
+fa_status fa_sm_clock_sample(unsigned long long* out, int blocks, void* stream) {
+  if (!out || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "fa_sm_clock_sample: null or misaligned output");
+  if (blocks < 1 || blocks > device_sm_count())
+    return fail(FA_ERR_INVALID_ARG, "fa_sm_clock_sample: blocks=%d outside [1, %d]", blocks, device_sm_count());
+  return launched(launch_sm_clock_sample(out, blocks, static_cast<cudaStream_t>(stream)), "fa_sm_clock_sample");
 }
 
 fa_status fa_tile_counter(void* stream, unsigned long long* value, int reset) {

@@ -89,6 +89,9 @@ struct DecodeArgs {
 };
 // Streaming multiprocessors of a GB300, for sizing grids.
 constexpr int kSmCount = 152;
+// Unique id of the CUDA context current on the calling thread (ids are never reused), or 0 when
+// no context is current or the driver cannot say.
+unsigned long long current_context_id();
 // Streaming multiprocessors of the current device (cached per device; kSmCount if unknown).
 int device_sm_count();
 int decode_auto_splits(int b, int h, int hkv, int nq, int nk);
@@ -150,6 +153,10 @@ cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a);
 // One CTA waits (bounded by timeout_ms) on an mbarrier phase nothing completes, or that it
 // completes itself when arrive != 0.
 cudaError_t launch_bounded_wait_selftest(unsigned long long* err, int timeout_ms, int arrive, cudaStream_t stream);
+
+// Block b of `blocks` (one per SM when blocks <= the SM count) writes {SM id, SM cycle counter,
+// global timer in ns} to out[3 b], out[3 b + 1], out[3 b + 2].
+cudaError_t launch_sm_clock_sample(unsigned long long* out, int blocks, cudaStream_t stream);
 
 // Records the calling thread's last error message (read by fa_last_error_message) and
 // returns `status`.

@@ -27,12 +27,17 @@ namespace {
 __device__ __align__(256) unsigned char g_bwd_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
+struct ScratchAddr {
+  void* ptr = nullptr;
+  unsigned long long ctx = 0;  // id of the context the address belongs to
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
 
 // Device address of g_bwd_scratch on the current device.  In host code the array's name
-// is only a host-side stand-in; the address comes from cudaGetSymbolAddress, looked up
-// once per device with that device current.
+// is only a host-side stand-in; the address comes from cudaGetSymbolAddress, looked up with
+// the device current on the first call in each context (once per device, unless the device's
+// context is destroyed and recreated, e.g. by cudaDeviceReset, when it is looked up again).
 fa_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -40,15 +45,18 @@ fa_status scratch_address(void** out) {
   if (dev < 0 || dev >= kMaxDevices)
     return (fa_status)set_last_error(FA_ERR_UNSUPPORTED, "device index %d out of range", dev);
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& a = g_scratch_addr[dev];
+  const unsigned long long ctx = current_context_id();
+  if (!a.ptr || ctx == 0 || ctx != a.ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_bwd_scratch);
     if (e != cudaSuccess || !p)
       return (fa_status)set_last_error(FA_ERR_CUDA, "cudaGetSymbolAddress(backward scratch): %s",
                                        cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
+    a.ptr = p;
+    a.ctx = current_context_id();  // the lookup made the device's context current if none was
   }
-  *out = g_scratch_addr[dev];
+  *out = a.ptr;
   return FA_OK;
 }
 

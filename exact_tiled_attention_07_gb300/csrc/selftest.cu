@@ -28,7 +28,35 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long* err, uint64_t l
   mbar_wait_for(&bar, 0, ctx, kSelftestSite, limit_ns);
 }
 
+// One reading per SM of its cycle counter (%clock64, SM clock cycles, free-running across
+// kernels) and of the global nanosecond timer.  Each block asks for more shared memory than two
+// blocks can share, so a grid of one block per SM puts one block on every idle SM.  Two
+// readings taken around a stretch of work give each SM's mean clock over it.
+constexpr int kClockSampleSmem = 160 * 1024;
+
+__global__ void sm_clock_sample_kernel(unsigned long long* out) {
+  extern __shared__ uint8_t pad[];
+  if (threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    pad[0] = (uint8_t)smid;  // keeps the shared allocation
+    const unsigned long long c = clock64();
+    const unsigned long long t = globaltimer();
+    out[3 * blockIdx.x] = smid;
+    out[3 * blockIdx.x + 1] = c;
+    out[3 * blockIdx.x + 2] = t;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_sm_clock_sample(unsigned long long* out, int blocks, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(sm_clock_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kClockSampleSmem);
+  if (e != cudaSuccess) return e;
+  sm_clock_sample_kernel<<<blocks, 32, kClockSampleSmem, stream>>>(out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bounded_wait_selftest(unsigned long long* err, int timeout_ms, int arrive, cudaStream_t stream) {
   bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(err, (uint64_t)timeout_ms * 1000000ull, arrive);

@@ -154,7 +154,8 @@ FA_API fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes
  *             larger problems return FA_ERR_INVALID_ARG and launch nothing.
  *   Set-up    The first call on a device looks up the array's device address
  *             (cudaGetSymbolAddress) with that device current; make that first call
- *             before any stream capture.
+ *             before any stream capture. (If the device's context is destroyed and
+ *             recreated, e.g. by cudaDeviceReset, the next call looks it up again.)
  *   Sharing   Every call uses the same array and leaves its contents behind; each call
  *             re-initialises what it reads. Calls whose kernels overlap on the GPU
  *             (different streams or host threads) race on the array: serialise them.
@@ -303,6 +304,17 @@ FA_API fa_status fa_selftest_bounded_wait(int timeout_ms, int arrive, void* stre
  * reset != 0 clears the counter afterwards.
  */
 FA_API fa_status fa_tile_counter(void* stream, unsigned long long* value, int reset);
+
+/*
+ * Measurement helper (no counterpart on the pages): launches `blocks` thread blocks on `stream`
+ * (1 <= blocks <= the device's SM count; each takes enough shared memory to have an SM to
+ * itself) and block b writes three 64-bit words to the DEVICE array out[3 * blocks]:
+ * out[3 b] = the id of the SM it ran on, out[3 b + 1] = that SM's cycle counter (%clock64),
+ * out[3 b + 2] = the global timer in nanoseconds (%globaltimer). Two samples taken on a stream
+ * before and after a stretch of work give, for each SM seen in both, its mean clock over that
+ * stretch: (cycles difference) / (nanoseconds difference) GHz.
+ */
+FA_API fa_status fa_sm_clock_sample(unsigned long long* out, int blocks, void* stream);
 
 /* Whether the given pass ("fwd" = 0, "bwd" = 1) runs on tensor cores for dtype and d. */
 FA_API int fa_uses_tensor_cores(int pass, fa_dtype dtype, int d);

@@ -42,6 +42,16 @@ def test_binding_covers_every_symbol():
         assert callable(getattr(binding, name))
 
 
+def test_noalloc_scratch_size_matches_the_header():
+    # the binding's copy of FA_BWD_NOALLOC_SCRATCH_BYTES, which its size checks and tests use
+    from exact_tiled_attention_07_gb300 import binding
+
+    txt = open(os.path.join(ROOT, "include", "fa.h")).read()
+    m = re.search(r"#define\s+FA_BWD_NOALLOC_SCRATCH_BYTES\s+\((\d+)ull\s*<<\s*(\d+)\)", txt)
+    assert m, "FA_BWD_NOALLOC_SCRATCH_BYTES not found in include/fa.h"
+    assert binding.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
 def test_status_strings(lib):
     lib.fa_status_string.restype = ctypes.c_char_p
     assert lib.fa_status_string(0) == b"ok"

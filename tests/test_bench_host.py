@@ -64,3 +64,24 @@ def test_timed_workloads_have_inputs_larger_than_l2(name):
 
 def test_small_workload_is_reported_as_fitting_in_l2():
     assert "fit in L2" in bench.l2_note(WORKLOADS["tiny_fp32"])
+
+
+def test_sm_clock_from_two_counter_readings():
+    # SM 3: 2,070,000 cycles in 1 ms -> 2070 MHz; SM 5: 1,500,000 cycles in 1 ms -> 1500 MHz;
+    # SM 9 appears only in the second reading and is ignored
+    before = [(3, 10_000, 5_000_000), (5, 20_000, 5_000_100)]
+    after = [(5, 1_520_000, 6_000_100), (3, 2_080_000, 6_000_000), (9, 1, 6_000_000)]
+    got = sorted(bench.sm_clock_mhz(before, after))
+    assert got == pytest.approx([1500.0, 2070.0])
+    assert bench.sm_clock_mhz(before, []) == []
+
+
+def test_peak_follows_the_length_of_the_timed_region():
+    peaks = {"bf16_tflops": 1881.8, "bf16_tflops_sustained": 1707.9}
+    assert bench.peak_for_region(peaks, 0.033) == (1881.8, "bf16_tflops (burst)")
+    assert bench.peak_for_region(peaks, 5.0)[0] == 1707.9
+
+
+def test_tensor_peak_at_clock():
+    # 152 SMs x 8192 FLOP per clock at 2070 MHz
+    assert bench.tensor_peak_at_clock(2070.0, 152) == pytest.approx(152 * 8192 * 2.07e9 / 1e12)
