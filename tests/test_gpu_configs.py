@@ -14,7 +14,8 @@ import pytest
 
 import oracle
 from exact_tiled_attention_07_gb300.inputs import WORKLOADS, make_inputs, to_float64
-from helpers import TOL_GRAD_RELRMS, TOL_L_MAXABS, TOL_O_MAXABS, TOL_O_RELRMS, max_abs, rel_rms, to_device, to_f64
+from helpers import (TOL_GRAD_RELRMS, TOL_L_MAXABS, TOL_O_MAXABS, TOL_O_RELRMS, key_side_reference, max_abs,
+                     oracle_pool_map, rel_rms, to_device, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -153,16 +154,33 @@ def test_long_sequence_causal_bf16(fa):
     x, host = _run_full(fa, w)
     _check_properties(w, x, host)
     _check_sampled_rows(w, x, host, _sample(w, 256, 41), with_bwd=True)
-    # key-side gradients: 32 sampled keys of one head (needs every row's L and D of that head)
-    b, h = 0, 3
-    keys = np.concatenate([np.random.default_rng(42).choice(w.N, 30, replace=False), [0, w.N - 1]])
-    q, k, v, do = (_head64(w, x, nm, b, h)[None, None] for nm in ("q", "k", "v", "do"))
-    stats = oracle.attn_stats64(q, k, v, do, w.scale, w.causal, 0, 0)
-    dk_ref, dv_ref = oracle.attn_bwd64_key_rows(q, k, v, do, w.scale, w.causal, 0, 0, keys, stats=stats)
-    kt = torch.as_tensor(keys, dtype=torch.long)
-    assert rel_rms(to_f64(host["dk"][b, h][kt]), dk_ref) <= TOL_GRAD_RELRMS
-    assert rel_rms(to_f64(host["dv"][b, h][kt]), dv_ref) <= TOL_GRAD_RELRMS
-    assert max_abs(to_f64(host["lse"][b, h]), stats[0]) <= TOL_L_MAXABS  # every row's L of that head
+    # key-side gradients: 32 keys in each of the 8 heads (256 in all), random ones plus keys at
+    # tile edges (0, 127, 128, 129, N - 129, N - 128, N - 1); each head's exact values need
+    # every row's L and D of that head, so the heads run in a pool of worker processes
+    rng = np.random.default_rng(42)
+    edges = np.array([0, 127, 128, 129, w.N - 129, w.N - 128, w.N - 1])
+    jobs, keys_of = [], {}
+    for h in range(w.H):
+        rnd = rng.choice(np.setdiff1d(np.arange(w.N), edges), 32 - edges.size, replace=False)
+        keys = np.sort(np.concatenate([rnd, edges]))
+        keys_of[h] = keys
+        q, k, v, do = (_head64(w, x, nm, 0, h)[None, None] for nm in ("q", "k", "v", "do"))
+        jobs.append((q, k, v, do, w.scale, w.causal, keys))
+    refs = oracle_pool_map(key_side_reference, jobs)
+    got_k, got_v, ref_k, ref_v = [], [], [], []
+    for h, (dk_ref, dv_ref, l_ref) in enumerate(refs):
+        kt = torch.as_tensor(keys_of[h], dtype=torch.long)
+        got_k.append(to_f64(host["dk"][0, h][kt]))
+        got_v.append(to_f64(host["dv"][0, h][kt]))
+        ref_k.append(dk_ref)
+        ref_v.append(dv_ref)
+        assert max_abs(to_f64(host["lse"][0, h]), l_ref) <= TOL_L_MAXABS, h  # every row's L of the head
+    assert sum(len(k_) for k_ in keys_of.values()) >= 256
+    assert rel_rms(np.concatenate(got_k), np.concatenate(ref_k)) <= TOL_GRAD_RELRMS
+    assert rel_rms(np.concatenate(got_v), np.concatenate(ref_v)) <= TOL_GRAD_RELRMS
+    for h in range(w.H):  # and head by head
+        assert rel_rms(got_k[h], ref_k[h]) <= TOL_GRAD_RELRMS, h
+        assert rel_rms(got_v[h], ref_v[h]) <= TOL_GRAD_RELRMS, h
 
 
 def test_head_dim_256_forward_bf16(fa):
