@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                   const __grid_constant__ CUtensorMap tm_dv, const float* __restrict__ lse2,
                   const float* __restrict__ delta, int n, int npad, int bh_count, int ktiles, float scale,
                   int causal, int group, unsigned long long* err, int window,
-                  const uint8_t* __restrict__ block_mask, int mask_heads, int heads, unsigned* __restrict__ sched) {
+                  const uint8_t* __restrict__ block_mask, int mask_heads, int heads, unsigned* __restrict__ sched,
+                  int hgroup) {
   using C = BwdCfg<D>;
   constexpr int BM = C::BM;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   // L2); causal: heaviest (first) key tiles first within groups of heads
   auto tile_of = [&](int item, int* kvh, int* kt) {
     if (causal) {
-      grouped_work_item(item, bh_count, ktiles, kvh, kt);
+      grouped_work_item(item, bh_count, ktiles, hgroup, kvh, kt);
     } else {
       *kvh = item / ktiles;
       *kt = item - *kvh * ktiles;
@@ -426,20 +427,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       };
       // K-major operand rows of 128 bytes in 64-column blocks: offset of K-slice kk (16 wide)
       auto kmaj = [](int kk, int rows) { return (uint32_t)((kk * 16 / 64) * (rows * 128) + (kk * 16 % 64) * 2); };
-      // dP^T = V dO_i^T (A: 128 keys x d, B: BM queries x d, both K-major in smem)
-      auto issue_dp = [&](uint32_t b) {
-        uint64_t ad[D / 16], bd[D / 16];
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          ad[kk] = make_sdesc_sw128(vs + kmaj(kk, BN), 16, 1024);
-          bd[kk] = make_sdesc_sw128(b + kmaj(kk, BM), 16, 1024);
-        }
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + C::COL_DP, ad[kk], bd[kk], idesc_s, kk > 0);
-        }
-        __syncwarp();
-      };
       // S^T = K Q_i^T with K_j from TMEM (A) and Q_i K-major in smem (B)
       auto issue_s = [&](uint32_t b) {
         uint64_t bd[D / 16];
@@ -473,8 +460,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const uint32_t g1 = gs + 1;
           const int s1 = g1 % C::QSTAGES;
           const uint32_t qs = qs_of(s), dos = dos_of(s);
-          // dP^T_i (its columns, holding dS^T_{i-1}, were last read by dK_{i-1}: same lane, in order)
-          issue_dp(dos);
+          // dP^T_i = V dO_i^T (A: 128 keys x d, B: BM queries x d, both K-major in smem), issued
+          // before the wait for P^T_i so that the tensor core works while the softmax side
+          // finishes it.  Its columns (holding dS^T_{i-1}) were last read by dK_{i-1}: same
+          // issuing thread, in order.
+          {
+            uint64_t ad[D / 16], bd[D / 16];
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              ad[kk] = make_sdesc_sw128(vs + kmaj(kk, BN), 16, 1024);
+              bd[kk] = make_sdesc_sw128(dos + kmaj(kk, BM), 16, 1024);
+            }
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + C::COL_DP, ad[kk], bd[kk], idesc_s, kk > 0);
+            }
+            __syncwarp();
+          }
           commit(bar + B_DP_FULL);
           // dV += P^T dO_i (P^T from TMEM, K = queries; dO_i as MN-major B)
           {
@@ -495,53 +497,64 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             }
             __syncwarp();
           }
-          // S^T_{i+1}: overwrites P^T_i only after dV_i has read it (same issuing lane, in order)
+          // S^T_{i+1}: overwrites P^T_i only after dV_i has read it (same issuing thread, in order)
           if (i + 1 < w.nsteps) {
             if (!(ok = wait(bar + B_QD_FULL + s1, (g1 / C::QSTAGES) & 1, 121))) break;
             tc_fence_after();
             issue_s(qs_of(s1));
             commit(bar + B_S_FULL);
           }
-          // dK += dS^T Q_i (dS^T 16-bit in TMEM over the dP^T columns, Q_i MN-major)
+          // dK += dS^T Q_i (dS^T 16-bit in TMEM over the dP^T columns, Q_i MN-major B) and the dQ
+          // partial (K and dS^T from smem; the previous partial, of this item or the last, drained
+          // from TMEM first).  The dQ k-steps, whose A operand comes from shared memory, are
+          // interleaved with the dK k-steps, whose A is in TMEM and which write another
+          // accumulator: a shared-memory-A MMA then overlaps the other's arithmetic instead of
+          // waiting for its operand reads, and the pair runs at about the tensor core's rate.
+          // The first kDkHead dK k-steps go out before the wait for the drain.
           {
-            uint64_t bd[BM / 16];
+            uint64_t dk_b[BM / 16], kd[BN / 16], sd[BN / 16];
 #pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk) bd[kk] = make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024);
-            if (!(ok = wait(bar + B_DS_READY, gs & 1, 124))) break;
-            tc_fence_after();
-            if (leader) {
-#pragma unroll
-              for (int kk = 0; kk < BM / 16; ++kk)
-                umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + packed_col(kk, C::CH_COLS), bd[kk], idesc_kv,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-            }
-            __syncwarp();
-          }
-          commit(bar + B_QD_EMPTY + s);
-          // dQ partial (the previous one, of this item or the last, drained from TMEM first)
-          {
-            uint64_t kd[BN / 16], sd[BN / 16];
+            for (int kk = 0; kk < BM / 16; ++kk) dk_b[kk] = make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
               kd[kk] = make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024);   // K as MN-major (d contiguous)
               sd[kk] = make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024);  // dS^T as MN-major (queries contiguous)
             }
+            constexpr int kDkHead = BM / 64;  // 1 at d = 128, 2 at d = 64
+            if (!(ok = wait(bar + B_DS_READY, gs & 1, 124))) break;
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < kDkHead; ++kk)
+                umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + packed_col(kk, C::CH_COLS), dk_b[kk], idesc_kv,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            __syncwarp();
             if (gs > 0) {
               if (!(ok = wait(bar + B_DQ_FREE, (gs - 1) & 1, 122))) break;
               tc_fence_after();
             }
             if (leader) {
+              constexpr int NA = BN / 16, NB = BM / 16 - kDkHead;  // dQ and remaining dK k-steps
+              int a = 0, b = 0;
 #pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                if constexpr (C::DQT)
-                  umma_ss(tbase + C::COL_DQ, kd[kk], sd[kk], idesc_q, kk > 0);
-                else
-                  umma_ss(tbase + C::COL_DQ, sd[kk], kd[kk], idesc_q, kk > 0);
+              for (int t = 0; t < NA + NB; ++t) {
+                if (b >= NB || (a < NA && a * NB <= b * NA)) {
+                  const int kk = a++;
+                  if constexpr (C::DQT)
+                    umma_ss(tbase + C::COL_DQ, kd[kk], sd[kk], idesc_q, kk > 0);
+                  else
+                    umma_ss(tbase + C::COL_DQ, sd[kk], kd[kk], idesc_q, kk > 0);
+                } else {
+                  const int kk = kDkHead + b++;
+                  umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + packed_col(kk, C::CH_COLS), dk_b[kk], idesc_kv, 1u);
+                  if (b == NB) umma_commit(bar + B_QD_EMPTY + s);  // Q_i, dO_i no longer read
+                }
               }
+              umma_commit(bar + B_DQ_FULL);
             }
             __syncwarp();
           }
-          commit(bar + B_DQ_FULL);
         }
         // an item without steps still takes its turn on acc_empty, so the phases stay in step
         if (ok && !acc_free) ok = wait(bar + B_ACC_EMPTY, (r - 1) & 1, 127);
@@ -1039,9 +1052,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
   const int64_t items = (int64_t)bh_kv * ktiles;
   const int64_t grid = MASKED ? items : std::min<int64_t>(items, device_sm_count());
   if (!MASKED && !a.sched) return cudaErrorInvalidValue;
+  // causal order: groups of key/value heads whose query-side streams (Q, dO, the fp32 dQ
+  // accumulator, L and D of each of their `group` query heads) stay in L2
+  const int hgroup = head_group_for_l2((int64_t)a.group * ((int64_t)npad * D * 8 + (int64_t)npad * 8));
   kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a.lse2, a.delta, a.n, npad,
                                                        bh_kv, ktiles, a.scale, a.causal, a.group, a.err, a.window,
-                                                       a.block_mask, a.mask_heads, a.heads, a.sched);
+                                                       a.block_mask, a.mask_heads, a.heads, a.sched, hgroup);
   return cudaGetLastError();
 }
 

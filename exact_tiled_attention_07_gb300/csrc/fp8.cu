@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ q_scales,
                    const float* __restrict__ k_scales, const float* __restrict__ v_scales, void* __restrict__ out,
                    float* __restrict__ lse, int n, int bh_count, int tiles_per_head, float scale_log2, int causal,
-                   int group, unsigned long long* err, unsigned long long* counter, unsigned* __restrict__ sched) {
+                   int group, unsigned long long* err, unsigned long long* counter, unsigned* __restrict__ sched,
+                   int hgroup) {
   using C = Fp8Cfg;
   constexpr int D = C::D;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     int tile;
     if (causal) {
       int rank;
-      grouped_work_item(item, bh_count, tiles_per_head, &w.head, &rank);
+      grouped_work_item(item, bh_count, tiles_per_head, hgroup, &w.head, &rank);
       tile = tiles_per_head - 1 - rank;
     } else {
       w.head = item / tiles_per_head;
@@ -778,11 +779,13 @@ cudaError_t launch_fwd_fp8_t(const Fp8FwdArgs& a) {
   QueueSlot qs;
   if (grid < items) qs = queue_slot_take(a.stream);
   auto kern = qs.slot >= 0 ? fwd_fp8_kernel<OUT_BF16, true> : fwd_fp8_kernel<OUT_BF16, false>;
+  // causal order: groups of query heads whose 8-bit K, V stay in L2
+  const int hgroup = head_group_for_l2((int64_t)2 * a.n * C::D / a.group);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e == cudaSuccess) {
     kern<<<(unsigned)grid, C::THREADS, C::SMEM, a.stream>>>(tq, tk, tv, a.q_scales, a.k_scales, a.v_scales, a.o,
                                                             a.lse, a.n, a.bh, tiles, a.scale * 1.4426950408889634f,
-                                                            a.causal, a.group, a.err, a.counter, qs.counters);
+                                                            a.causal, a.group, a.err, a.counter, qs.counters, hgroup);
     e = cudaGetLastError();
   }
   return queue_slot_done(qs, e, a.stream);

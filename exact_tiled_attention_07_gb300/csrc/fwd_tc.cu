@@ -76,19 +76,29 @@ struct FwdCfg {
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
   // TMEM columns
   static constexpr int S_COL0 = 0, S_COL1 = 128;
+  // d = 64: P gets columns of its own (S, O and P of both query tiles fill the 512), so the
+  // next S = Q K^T may overwrite S as soon as the softmax has read it, before P V has run
+  static constexpr bool SEP_P = (D == 64);
+  static constexpr int P_COL0 = 384, P_COL1 = 448;
   static constexpr int O_COL0 = 256;
   static constexpr int O_COL1 = (NQ == 2) ? 256 + D : 256;
   // shared memory
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = NQ * Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + STAGES * ENTRY_BYTES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 3 + 4;
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 3 + 4 + 4 + 4;
   // after the barriers: TMEM base, abort flag, the two work-item slots
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 32;
   // masked variant: the CTA's key-tile list after the barriers (4 ints, then uint16 tile
   // indices and uint8 visibility flags, nb rounded up to 16 entries each)
   static constexpr int OFF_LIST = SMEM;
   static constexpr int list_bytes(int nb) { return 16 + 3 * ((nb + 15) & ~15); }
+  // unmasked variant: after the barriers, one epilogue staging box per softmax warpgroup
+  // ([128 rows][64 columns] 16-bit, 128-byte swizzle, the layout of the O tensor map's box),
+  // through which O leaves by TMA stores 64 columns at a time
+  static constexpr int OFF_STG = (SMEM + 1023) & ~1023;
+  static constexpr int STG_BOX = BM * 128;
+  static constexpr int SMEM_STG = OFF_STG + NQ * STG_BOX;
 };
 
 struct FwdSmemBars {
@@ -104,6 +114,10 @@ struct FwdSmemBars {
   uint64_t* q_empty;  // [1] every S = Q K^T of the last item is done (Q may be overwritten)
   uint64_t* item_full;   // [2] the producer published a work item in this slot (queue mode)
   uint64_t* item_empty;  // [2] every consumer warp has read it
+  uint64_t* stg_free;    // [2] the last TMA store from softmax warpgroup q's staging box has read it
+  uint64_t* stg_full;    // [2] every thread of warpgroup q has written its row into the box
+  uint64_t* s_free;      // [2] (separate P) the softmax has read S_q: the next S_q may be computed
+  uint64_t* pv_q;        // [2] (separate P) P_q V of the last tile is done: P_q and O_q are free
 };
 
 // Masked variant (block mask and/or window, "Lecture 8" §5.7 block-sparse attention): one warp
@@ -115,10 +129,10 @@ struct FwdSmemBars {
 template <int D, bool BF16, bool MASKED, bool QUEUE>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, float* __restrict__ lse, int n,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, void* __restrict__ out, float* __restrict__ lse, int n,
                   int bh_count, int tiles_per_head, float scale_log2, int causal, int group, unsigned long long* err,
                   unsigned long long* counter, int window, const uint8_t* __restrict__ block_mask, int mask_heads,
-                  int heads, int snake, unsigned* __restrict__ sched) {
+                  int heads, int snake, unsigned* __restrict__ sched, int hgroup) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -138,6 +152,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   B.q_empty = B.o_empty + 2;
   B.item_full = B.q_empty + 1;
   B.item_empty = B.item_full + 2;
+  B.stg_free = B.item_empty + 2;
+  B.stg_full = B.stg_free + 2;
+  B.s_free = B.stg_full + 2;
+  B.pv_q = B.s_free + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
@@ -158,7 +176,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     int tile;
     if (causal) {
       int rank;
-      grouped_work_item(item, bh_count, tiles_per_head, &w.head, &rank);
+      grouped_work_item(item, bh_count, tiles_per_head, hgroup, &w.head, &rank);
       tile = tiles_per_head - 1 - rank;
     } else {
       w.head = item / tiles_per_head;
@@ -257,6 +275,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(B.item_full + t, 1);
       mbar_init(B.item_empty + t, C::SOFTMAX_WARPS + 1);  // the softmax warps and the MMA warp
+      mbar_init(B.stg_free + t, 1);
+      mbar_init(B.stg_full + t, 128);
+      mbar_init(B.s_free + t, 128);
+      mbar_init(B.pv_q + t, 1);
     }
     fence_barrier_init();
   }
@@ -502,32 +524,77 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             commit(B.kv_empty + slot_of(0));
           }
           if (nmax <= 1) commit(B.q_empty);  // every S of the item is issued
-          for (int j = 0; ok && j < nmax; ++j) {
-            const int vidx = 2 * j + 1, kidx = 2 * j + 2;
-            if (!(ok = wait_full(vidx))) break;
-            if (j < nq[0]) {
-              if (!(ok = wait(B.p_full + 0, (tq[0] + j) & 1, 22))) break;
-              if (j == 0 && !(ok = o_free(0))) break;
-              tc_fence_after();
-              issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
+          if constexpr (C::SEP_P) {
+            // S_q(j+1) goes out as soon as the softmax has read S_q(j) (s_free), P_q(j) V_j once
+            // it has written P_q(j) (p_full); each P V tells the softmax (pv_q) that P_q and O_q
+            // are free again.  In the order the events come: tile 0's S, tile 0's P V, tile 1's
+            // S, tile 1's P V (query tile 1 runs half a period behind tile 0).
+            for (int j = 0; ok && j < nmax; ++j) {
+              const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+              const bool more = j + 1 < nmax;
+              if (more && !(ok = wait_full(kidx))) break;
+              if (j + 1 < nq[0]) {
+                if (!(ok = wait(B.s_free + 0, (tq[0] + j) & 1, 28))) break;
+                tc_fence_after();
+                issue_qk(0, kidx, C::S_COL0);
+                commit(B.s_full + 0);
+              }
+              if (!(ok = wait_full(vidx))) break;
+              if (j < nq[0]) {
+                if (!(ok = wait(B.p_full + 0, (tq[0] + j) & 1, 22))) break;
+                if (j == 0 && !(ok = o_free(0))) break;
+                tc_fence_after();
+                issue_pv(C::O_COL0, C::P_COL0, vidx, j > 0);
+                commit(B.pv_q + 0);
+                if (j == nq[0] - 1) commit(B.o_full + 0);
+              }
+              if (j + 1 < nq[1]) {
+                if (!(ok = wait(B.s_free + 1, (tq[1] + j) & 1, 29))) break;
+                tc_fence_after();
+                issue_qk(1, kidx, C::S_COL1);
+                commit(B.s_full + 1);
+              }
+              if (more) commit(B.kv_empty + slot_of(kidx));  // both S_{j+1} issued
+              if (j == nmax - 2) commit(B.q_empty);         // the item's last S are issued
+              if (j < nq[1]) {
+                if (!(ok = wait(B.p_full + 1, (tq[1] + j) & 1, 23))) break;
+                if (j == 0 && !(ok = o_free(1))) break;
+                tc_fence_after();
+                issue_pv(C::O_COL1, C::P_COL1, vidx, j > 0);
+                commit(B.pv_q + 1);
+                if (j == nq[1] - 1) commit(B.o_full + 1);
+              }
+              commit(B.kv_empty + slot_of(vidx));
             }
-            if (j + 1 < nmax) {
-              if (!(ok = wait_full(kidx))) break;
-              tc_fence_after();
+          } else {
+            for (int j = 0; ok && j < nmax; ++j) {
+              const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+              if (!(ok = wait_full(vidx))) break;
+              if (j < nq[0]) {
+                if (!(ok = wait(B.p_full + 0, (tq[0] + j) & 1, 22))) break;
+                if (j == 0 && !(ok = o_free(0))) break;
+                tc_fence_after();
+                issue_pv(C::O_COL0, C::S_COL0, vidx, j > 0);
+                // O_0 is final: its epilogue need not wait for query tile 1's last P
+                if (j == nq[0] - 1) commit(B.o_full + 0);
+              }
+              if (j + 1 < nmax) {
+                if (!(ok = wait_full(kidx))) break;
+                tc_fence_after();
+              }
+              if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); commit(B.s_full + 0); }
+              if (j < nq[1]) {
+                if (!(ok = wait(B.p_full + 1, (tq[1] + j) & 1, 23))) break;
+                if (j == 0 && !(ok = o_free(1))) break;
+                tc_fence_after();
+                issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
+              }
+              commit(B.kv_empty + slot_of(vidx));
+              if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); commit(B.s_full + 1); }
+              if (j + 1 < nmax) commit(B.kv_empty + slot_of(kidx));
+              if (j == nmax - 2) commit(B.q_empty);  // the item's last S are issued
+              if (j == nq[1] - 1) commit(B.o_full + 1);
             }
-            if (j + 1 < nq[0]) { issue_qk(0, kidx, C::S_COL0); commit(B.s_full + 0); }
-            if (j < nq[1]) {
-              if (!(ok = wait(B.p_full + 1, (tq[1] + j) & 1, 23))) break;
-              if (j == 0 && !(ok = o_free(1))) break;
-              tc_fence_after();
-              issue_pv(C::O_COL1, C::S_COL1, vidx, j > 0);
-            }
-            commit(B.kv_empty + slot_of(vidx));
-            if (j + 1 < nq[1]) { issue_qk(1, kidx, C::S_COL1); commit(B.s_full + 1); }
-            if (j + 1 < nmax) commit(B.kv_empty + slot_of(kidx));
-            if (j == nmax - 2) commit(B.q_empty);  // the item's last S are issued
-            if (j == nq[0] - 1) commit(B.o_full + 0);
-            if (j == nq[1] - 1) commit(B.o_full + 1);
           }
         } else {
           // NQ == 1: S double-buffered in columns 0 / 128 (by the global tile count), O at 256
@@ -584,6 +651,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t o_col = q ? C::O_COL1 : C::O_COL0;
     int tq = 0;  // key tiles this query tile processed (all items): S / P phases
     int oq = 0;  // items with a result: O phases
+    uint32_t stg_uses = 0;  // TMA stores from this warpgroup's staging box (all items)
     bool ok = start_ok;
     for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
       const Item w = item_at(item);
@@ -621,6 +689,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+        if constexpr (C::SEP_P) {  // S_q is in registers: the next S_q may be computed over it
+          tc_fence_before();
+          mbar_arrive(B.s_free + q);
+        }
         // visible columns [lo, hi) of this row: keys before N, (causal) not after the row,
         // (window) within the window; none when the tile is listed only for the other query tile
         const int jt = tile_at(j);
@@ -638,7 +710,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           for (int c = 0; c < BN; ++c)
             if (c < lo || c >= hi) s[c] = -INFINITY;
         }
-        const float mx = row_max(s);
+        const float mx = row_max3(s);
         const float m_blk = mx * scale_log2;
         float alpha = 1.f;
         bool rescale = false;
@@ -651,24 +723,35 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           rescale = true;
         }
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
-        float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
-#pragma unroll
-        for (int h = 0; h < BN / 64; ++h) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2(fmaf(s[h * 64 + 2 * i], scale_log2, neg_m));
-            const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], scale_log2, neg_m));
-            part[i & 3] += p0 + p1;
-            pk[i] = pack2<BF16>(p0, p1);
+        if constexpr (C::SEP_P) {
+          // P_q and O_q are free once the previous tile's P V is done
+          if (t > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(B.pv_q + q, (t - 1) & 1, ctx, 36 + q));
+            if (!ok) break;
+            tc_fence_after();
           }
-          tmem_st32(tmem_addr(tbase, lane_base, s_col + h * 32), pk);
         }
-        const float sum = (part[0] + part[1]) + (part[2] + part[3]);
+        const uint32_t p_col = C::SEP_P ? (q ? C::P_COL1 : C::P_COL0) : s_col;
+        // two partial sums of pairs (paired fp32 adds): no single long add chain
+        float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int h = 0; h < BN / 32; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = ffma2(make_float2(s[h * 32 + 2 * i], s[h * 32 + 2 * i + 1]), scale_log2, neg_m);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            part[i & 1] = fadd2(part[i & 1], pp);
+            pk[i] = pack2<BF16>(pp.x, pp.y);
+          }
+          tmem_st16(tmem_addr(tbase, lane_base, p_col + h * 16), pk);
+        }
+        const float sum = (part[0].x + part[1].x) + (part[0].y + part[1].y);
         l = l * alpha + sum;
         if (__any_sync(0xffffffffu, rescale)) {
-          // O row *= alpha; O is stable: the PV of block j-1 completed before S_j
-          // (NQ = 2: same issuing thread, in order) or pv_done says so (NQ = 1).
+          // O row *= alpha; O is stable: the PV of block j-1 completed before S_j (NQ = 2 without
+          // separate P: same issuing thread, in order), or pv_done (NQ = 1) / pv_q (separate P,
+          // waited above) says so.
           if constexpr (C::NQ == 1) {
             ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done, (t - 1) & 1, ctx, 34));
             if (!ok) break;
@@ -697,7 +780,61 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // epilogue: O / l -> global (16-bit), L = (m + log2 l) ln 2
       if (ok && nb > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(B.o_full + q, oq & 1, ctx, 40 + q));
-        if (ok) {
+        if (ok && !MASKED) {
+          // 64 columns at a time: TMEM -> registers (x 1/l) -> this warpgroup's staging box ->
+          // one TMA store (rows past N are not written).  The box is taken once the previous
+          // store from it has read it; O is released (o_empty) as soon as its last columns are in
+          // registers, so the next item's first P V need not wait for the stores.
+          tc_fence_after();
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          uint8_t* box = smem + C::OFF_STG + q * C::STG_BOX;
+          const bool leader = (rit == 0);
+#pragma unroll 1
+          for (int pc = 0; pc < D / 64 && ok; ++pc) {
+            if (leader) {
+              bulk_wait_group_read<0>();
+              mbar_arrive(B.stg_free + q);
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(B.stg_free + q, stg_uses & 1, ctx, 44 + q));
+            if (!ok) break;
+            uint8_t* rp = box + rit * 128;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+              uint32_t r[32];
+              tmem_ld32(tmem_addr(tbase, lane_base, o_col + pc * 64 + h * 32), r);
+              tmem_wait_ld();
+              reg_fence(r);
+              if (pc == D / 64 - 1 && h == 1) {  // O is in registers: the next item may overwrite it
+                tc_fence_before();
+                mbar_arrive(B.o_empty + q);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t* v = &r[u * 8];
+                const uint4 pk = make_uint4(pack2<BF16>(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                                            pack2<BF16>(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                                            pack2<BF16>(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                                            pack2<BF16>(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+                const uint32_t ch = (uint32_t)(h * 4 + u);
+                *reinterpret_cast<uint4*>(rp + ((ch ^ (uint32_t)(rit & 7)) << 4)) = pk;
+              }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(B.stg_full + q);
+            if (leader) {
+              ok = mbar_wait(B.stg_full + q, stg_uses & 1, ctx, 46 + q);
+              if (ok) {
+                tma_store_3d(&tm_o, box, pc * 64, w.qrow0 + q * BM, head);
+                bulk_commit_group();
+              }
+            }
+            ++stg_uses;
+          }
+          ++oq;
+          if (row < n) lse[(int64_t)head * n + row] = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          if (counter && rit == 0) atomicAdd(counter, (unsigned long long)nb);
+        } else if (ok) {
+          // masked launches (one item per CTA): rows straight from registers to global memory
           tc_fence_after();
           const float inv = l > 0.f ? 1.f / l : 0.f;
           uint8_t* orow = reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2;
@@ -733,6 +870,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       tq += nb;
     }
+    if (!MASKED && rit == 0) bulk_wait_group<0>();  // this warpgroup's TMA stores have completed
   }
 
   tc_fence_before();
@@ -754,7 +892,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
 // Largest per-CTA work (key tiles) of a persistent causal grid of g CTAs over the items, in grid
 // order or snake order: the same item order and key-tile counts as the kernel.
-int64_t max_cta_tiles(int bh, int tiles_per_head, int n, int nq_tiles, int g, bool snake) {
+int64_t max_cta_tiles(int bh, int tiles_per_head, int n, int nq_tiles, int g, bool snake, int hgroup) {
   std::vector<int64_t> load(g, 0);
   const int64_t total = (int64_t)bh * tiles_per_head;
   const int nblocks = (n + BN - 1) / BN;
@@ -763,7 +901,7 @@ int64_t max_cta_tiles(int bh, int tiles_per_head, int n, int nq_tiles, int g, bo
       const int64_t item = r * g + ((snake && (r & 1)) ? (g - 1 - c) : c);
       if (item >= total) continue;
       int head, rank;
-      grouped_work_item((int)item, bh, tiles_per_head, &head, &rank);
+      grouped_work_item((int)item, bh, tiles_per_head, hgroup, &head, &rank);
       const int tile = tiles_per_head - 1 - rank;
       for (int q = 0; q < nq_tiles; ++q) {
         const int first = tile * nq_tiles * BM + q * BM;
@@ -776,13 +914,13 @@ int64_t max_cta_tiles(int bh, int tiles_per_head, int n, int nq_tiles, int g, bo
 template <int D, bool BF16, bool MASKED>
 cudaError_t launch_fwd_d(const FwdArgs& a) {
   using C = FwdCfg<D>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int bh_kv = a.bh / a.group;
   if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) ||
-      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN))
+      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN) || !make_tmap_16bit_3d(&to, a.o, BF16, D, a.n, a.bh, BM))
     return cudaErrorInvalidValue;
   const int nblocks = (a.n + BN - 1) / BN;
-  const int smem = C::SMEM + (MASKED ? C::list_bytes(nblocks) : 0);
+  const int smem = MASKED ? C::SMEM + C::list_bytes(nblocks) : C::SMEM_STG;
   if (smem > 232448) return cudaErrorInvalidValue;  // key-tile list too long for shared memory
   const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
   const float scale_log2 = a.scale * 1.4426950408889634f;
@@ -790,9 +928,11 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
   // lives in shared memory)
   const int64_t items = (int64_t)a.bh * tiles;
   const int64_t grid = MASKED ? items : std::min<int64_t>(items, device_sm_count());
+  // causal order: groups of query heads whose K, V (shared by `group` query heads) stay in L2
+  const int hgroup = head_group_for_l2((int64_t)2 * a.n * D * 2 / a.group);
   const int snake = (!MASKED && a.causal && grid < items &&
-                     max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, true) <
-                         max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, false))
+                     max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, true, hgroup) <
+                         max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, false, hgroup))
                         ? 1
                         : 0;
   // with more items than CTAs: the queue when a slot is free (CTAs that finish early take more
@@ -805,9 +945,9 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess) {
-    kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
+    kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, to, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
                                                          a.causal, a.group, a.err, a.counter, a.window, a.block_mask,
-                                                         a.mask_heads, a.heads, snake, qs.counters);
+                                                         a.mask_heads, a.heads, snake, qs.counters, hgroup);
     e = cudaGetLastError();
   }
   return queue_slot_done(qs, e, a.stream);

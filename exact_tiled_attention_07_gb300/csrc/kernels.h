@@ -87,6 +87,15 @@ struct DecodeArgs {
   unsigned long long* err = nullptr;      // device error word (tensor-core path)
   unsigned long long* counter = nullptr;  // device count of processed (row tile, key tile) pairs
 };
+// Heads per group of the causal work-item order (grouped_work_item): as many heads as keep
+// `bytes_per_head` (what a head's items stream: K and V in the forward; Q, dO, the dQ
+// accumulator, L and D in the backward) within an L2 budget of kL2HeadBudget bytes, at
+// least 1 and at most kMaxHeadGroup.
+constexpr int64_t kL2HeadBudget = 80ll << 20;
+inline int head_group_for_l2(int64_t bytes_per_head) {
+  const int64_t g = bytes_per_head > 0 ? kL2HeadBudget / bytes_per_head : 16;
+  return (int)(g < 1 ? 1 : (g > 16 ? 16 : g));  // 16: kMaxHeadGroup
+}
 // Streaming multiprocessors of a GB300, for sizing grids.
 constexpr int kSmCount = 152;
 // Unique id of the CUDA context current on the calling thread (ids are never reused), or 0 when

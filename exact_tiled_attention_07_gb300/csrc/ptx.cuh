@@ -60,11 +60,6 @@ __device__ __forceinline__ bool elect_one_sync() {
   return pred != 0;
 }
 
-// Work-item order for grids of (head, tile) CTAs whose work depends on the tile index.
-// Heads are taken in groups of kHeadGroup; inside a group, tiles go from the heaviest to the
-// lightest, all heads of the group per tile.  The block scheduler then runs a
-// longest-first list schedule per group while the CTAs running together touch at most a
-// group's heads, whose K/V (or Q/dO) stay in L2.  `heavy_rank` 0 is the heaviest tile.
 // %ctaid.x / %nctaid.x through volatile reads: the compiler cannot hoist them out of a loop and
 // keep them in registers, which matters in kernels at the register cap.
 __device__ __forceinline__ uint32_t cta_id_x() {
@@ -78,20 +73,25 @@ __device__ __forceinline__ uint32_t grid_dim_x() {
   return v;
 }
 
-constexpr int kHeadGroup = 16;
-__host__ __device__ __forceinline__ void grouped_work_item(int bid, int heads, int tiles, int* head,
+// Work-item order for grids of (head, tile) items whose work depends on the tile index.
+// Heads are taken in groups of `group` (chosen on the host so that what a group's items stream
+// stays in L2, see head_group_for_l2); inside a group, tiles go from the heaviest to the
+// lightest, all heads of the group per tile.  Items drawn in order then run a longest-first
+// list schedule per group while the CTAs running together touch at most a group's heads,
+// whose K/V (or Q/dO) stay in L2.  `heavy_rank` 0 is the heaviest tile.
+constexpr int kMaxHeadGroup = 16;
+__host__ __device__ __forceinline__ void grouped_work_item(int bid, int heads, int tiles, int group, int* head,
                                                            int* heavy_rank) {
-  const int per_group = kHeadGroup * tiles;
+  const int per_group = group * tiles;
   const int g = bid / per_group;
   const int r = bid - g * per_group;
-  const int rest = heads - g * kHeadGroup;
-  const int gsize = kHeadGroup < rest ? kHeadGroup : rest;
+  const int rest = heads - g * group;
+  const int gsize = group < rest ? group : rest;
   *heavy_rank = r / gsize;
-  *head = g * kHeadGroup + (r - *heavy_rank * gsize);
+  *head = g * group + (r - *heavy_rank * gsize);
 }
 
 // ---------------------------------------------------------------------------
-// mbarrier// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -374,6 +374,58 @@ __device__ __forceinline__ float row_max(const float (&s)[N]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], s[c + i]);
   return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// Largest of N values (N a multiple of 8) with three-input max instructions: four independent
+// chains taking two new values per step, then a tree.
+template <int N>
+__device__ __forceinline__ float row_max3(const float (&s)[N]) {
+  static_assert(N % 8 == 0, "row_max3 takes a multiple of 8 values");
+  float m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = s[i];
+#pragma unroll
+  for (int c = 4; c < N - 4; c += 8)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      asm("max.f32 %0, %0, %1, %2;" : "+f"(m[i]) : "f"(s[c + 2 * i]), "f"(s[c + 2 * i + 1]));
+  // the last four values
+  float r0, r1;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r0) : "f"(m[0]), "f"(m[1]), "f"(s[N - 4]));
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r1) : "f"(m[2]), "f"(m[3]), "f"(s[N - 3]));
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(r0), "f"(r1), "f"(s[N - 2]));
+  return fmaxf(r, s[N - 1]);
+}
+
+// Paired fp32 arithmetic (two lanes per instruction, each rounded as the scalar operation):
+// (a.x b + c, a.y b + c) and the same with a per-lane addend, and a + b.
+__device__ __forceinline__ float2 ffma2(float2 a, float b, float c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
 // 2^x on the SFU (PTX ex2.approx, flush-to-zero).
