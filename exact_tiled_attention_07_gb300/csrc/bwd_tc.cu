@@ -4,6 +4,7 @@
 // and GPU memory" §09): nothing N x N was stored, so every (key tile j, query tile i) pair
 // recomputes its scores from Q, K and the saved row statistic L:
 //     S^T = K_j Q_i^T,   P^T = exp2(S^T tau log2e - L_i log2e)       (= e^(S - m)/l)
+// (the workspace holds -L_i log2e, so the exponent is one fused multiply-add)
 //     dV_j += P^T dO_i,   dP^T = V_j dO_i^T,   dS^T = P^T o (dP^T - D_i)
 //     dK_j += dS^T Q_i,   dQ_i += dS K_j      (tau applied to dK here and to dQ on conversion)
 // with D_i = sum_k dO_ik O_ik precomputed by the preprocess kernel (the §5.4 identity).
@@ -79,9 +80,13 @@ struct BwdCfg {
   static constexpr int list_bytes(int entries) { return 16 + 2 * ((entries + 7) & ~7); }
   static constexpr int SUB = 128 / BM;  // steps per 128-row query block
   // d = 64 (128 queries per step): both warpgroups compute P^T, dS^T (half the queries each)
-  // and drain half of each dQ partial; d = 128 (tensor-bound): warpgroup 0 computes P^T, dS^T
-  // and warpgroup 1 drains whole dQ partials as soon as they complete
-  static constexpr bool SPLIT = !DQT;
+  // and drain half of each dQ partial (half its d columns).  d = 128: warpgroup 0 computes P^T,
+  // dS^T and warpgroup 1 drains whole dQ partials as soon as they complete.  The split also
+  // builds at d = 128 (kSplit128: each warpgroup drains half the query columns of dQ^T and
+  // stores one of dV, dK), but measured 12 % slower there: each warpgroup's drain then sits
+  // between its dS^T half and its next P^T half, on the path to the next step's P^T.
+  static constexpr bool kSplit128 = false;
+  static constexpr bool SPLIT = !DQT || kSplit128;
   static constexpr int COMPUTE_THREADS = SPLIT ? 256 : 128;
   static constexpr int DRAIN_THREADS = SPLIT ? 256 : 128;
   static constexpr int CH_COLS = SPLIT ? 32 : 16;  // TMEM columns between packed 32-query chunks
@@ -609,6 +614,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mask_above = key + window - q0;
           }
         }
+        // the whole warp sees every query of the step: no masking of P
+        const bool all_visible = __all_sync(0xffffffffu, key_ok && mask_below <= 0 && mask_above >= BM);
         // P^T row (this key against the BM queries), kept as packed 16-bit pairs: the same
         // rounded values feed dV += P^T dO and dS = P o (dP - D)
         uint32_t pk[BM / 2];
@@ -625,14 +632,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             reg_fence(r);
 #pragma unroll
             for (int t = 0; t < 32; t += 4) {
+              // x = S tau log2 e - L log2 e, two queries per paired FMA (l2v holds -L log2 e)
               const float4 l4 = *reinterpret_cast<const float4*>(l2v + c * 32 + t);
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-              float e[4];
+              const float2 x01 = ffma2(make_float2(__uint_as_float(r[t]), __uint_as_float(r[t + 1])), scale_log2,
+                                       make_float2(l4.x, l4.y));
+              const float2 x23 = ffma2(make_float2(__uint_as_float(r[t + 2]), __uint_as_float(r[t + 3])), scale_log2,
+                                       make_float2(l4.z, l4.w));
+              float e[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
+              if (!all_visible) {
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int qc = c * 32 + t + u;
-                const float x = ex2(fmaf(__uint_as_float(r[t + u]), scale_log2, -lv[u]));
-                e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? x : 0.f;
+                for (int u = 0; u < 4; ++u) {
+                  const int qc = c * 32 + t + u;
+                  e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? e[u] : 0.f;
+                }
               }
               pk[(c * 32 + t) / 2] = pack2<BF16>(e[0], e[1]);
               pk[(c * 32 + t) / 2 + 1] = pack2<BF16>(e[2], e[3]);
@@ -667,13 +679,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             uint32_t dsk[16];
 #pragma unroll
             for (int t = 0; t < 16; t += 2) {
+              // dS = P o (dP - D), two queries per paired subtract and multiply
               const float4 d4 = *reinterpret_cast<const float4*>(dvec + c * 32 + 2 * t);
-              const float2 p01 = unpack2<BF16>(pk[c * 16 + t]);
-              const float2 p23 = unpack2<BF16>(pk[c * 16 + t + 1]);
-              dsk[t] = pack2<BF16>(p01.x * (__uint_as_float(r[2 * t]) - d4.x),
-                                   p01.y * (__uint_as_float(r[2 * t + 1]) - d4.y));
-              dsk[t + 1] = pack2<BF16>(p23.x * (__uint_as_float(r[2 * t + 2]) - d4.z),
-                                       p23.y * (__uint_as_float(r[2 * t + 3]) - d4.w));
+              const float2 ds01 = fmul2(unpack2<BF16>(pk[c * 16 + t]),
+                                        fsub2(make_float2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1])),
+                                              make_float2(d4.x, d4.y)));
+              const float2 ds23 = fmul2(unpack2<BF16>(pk[c * 16 + t + 1]),
+                                        fsub2(make_float2(__uint_as_float(r[2 * t + 2]), __uint_as_float(r[2 * t + 3])),
+                                              make_float2(d4.z, d4.w)));
+              dsk[t] = pack2<BF16>(ds01.x, ds01.y);
+              dsk[t + 1] = pack2<BF16>(ds23.x, ds23.y);
             }
             // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
             uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
@@ -846,18 +861,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(bar + B_DQ_FREE);
         if (!stage_begin()) return false;
-        // [128 queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns; TMEM lane =
-        // query row (rit), columns = this thread's d (one box per 32)
+        if constexpr (C::DQT) {
+          // [64 queries][128 d] fp32, row-major: TMEM lane = d (rit), columns = this warpgroup's
+          // 32 queries
+          float* st = reinterpret_cast<float*>(stg) + rit;
 #pragma unroll
-        for (int j = 0; j < DCOLS / 4; ++j) {
-          uint8_t* bx = stg + (dcol0 / 32 + j / 8) * (BM * 128) + rit * 128;
-          *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ sw) << 4)) =
-              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          for (int j = 0; j < DCOLS; ++j) st[(dcol0 + j) * D] = __uint_as_float(v[j]);
+        } else {
+          // [128 queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns; TMEM lane =
+          // query row (rit), columns = this thread's d (one box per 32)
+#pragma unroll
+          for (int j = 0; j < DCOLS / 4; ++j) {
+            uint8_t* bx = stg + (dcol0 / 32 + j / 8) * (BM * 128) + rit * 128;
+            *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ sw) << 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
         }
         good = stage_end();
         if (leader && good) {
-          tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
-          tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, qh);
+          if constexpr (C::DQT) {
+            tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
+          } else {
+            tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
+            tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, qh);
+          }
           bulk_commit_group();
         }
         ++stg_uses;
@@ -897,6 +924,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               mask_above = key + window - q0;
             }
           }
+          // the whole warp sees every query of the step: no masking of P
+          const bool all_visible = __all_sync(0xffffffffu, key_ok && mask_below <= 0 && mask_above >= BM);
           // P^T of this key against this half's queries, kept as packed 16-bit pairs: the same
           // rounded values feed dV += P^T dO and dS = P o (dP - D)
           uint32_t pk[NCH * 16];
@@ -912,14 +941,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               reg_fence(r);
 #pragma unroll
               for (int t = 0; t < 32; t += 4) {
+                // x = S tau log2 e - L log2 e, two queries per paired FMA (l2v holds -L log2 e)
                 const float4 l4 = *reinterpret_cast<const float4*>(l2v + c * 32 + t);
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                float e[4];
+                const float2 x01 = ffma2(make_float2(__uint_as_float(r[t]), __uint_as_float(r[t + 1])), scale_log2,
+                                         make_float2(l4.x, l4.y));
+                const float2 x23 = ffma2(make_float2(__uint_as_float(r[t + 2]), __uint_as_float(r[t + 3])),
+                                         scale_log2, make_float2(l4.z, l4.w));
+                float e[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
+                if (!all_visible) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const int qc = c * 32 + t + u;
-                  const float x = ex2(fmaf(__uint_as_float(r[t + u]), scale_log2, -lv[u]));
-                  e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? x : 0.f;
+                  for (int u = 0; u < 4; ++u) {
+                    const int qc = c * 32 + t + u;
+                    e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? e[u] : 0.f;
+                  }
                 }
                 pk[cl * 16 + t / 2] = pack2<BF16>(e[0], e[1]);
                 pk[cl * 16 + t / 2 + 1] = pack2<BF16>(e[2], e[3]);
@@ -953,13 +987,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               uint32_t dsk[16];
 #pragma unroll
               for (int t = 0; t < 16; t += 2) {
+                // dS = P o (dP - D), two queries per paired subtract and multiply
                 const float4 d4 = *reinterpret_cast<const float4*>(dvec + c * 32 + 2 * t);
-                const float2 p01 = unpack2<BF16>(pk[cl * 16 + t]);
-                const float2 p23 = unpack2<BF16>(pk[cl * 16 + t + 1]);
-                dsk[t] = pack2<BF16>(p01.x * (__uint_as_float(r[2 * t]) - d4.x),
-                                     p01.y * (__uint_as_float(r[2 * t + 1]) - d4.y));
-                dsk[t + 1] = pack2<BF16>(p23.x * (__uint_as_float(r[2 * t + 2]) - d4.z),
-                                         p23.y * (__uint_as_float(r[2 * t + 3]) - d4.w));
+                const float2 ds01 = fmul2(unpack2<BF16>(pk[cl * 16 + t]),
+                                          fsub2(make_float2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1])),
+                                                make_float2(d4.x, d4.y)));
+                const float2 ds23 =
+                    fmul2(unpack2<BF16>(pk[cl * 16 + t + 1]),
+                          fsub2(make_float2(__uint_as_float(r[2 * t + 2]), __uint_as_float(r[2 * t + 3])),
+                                make_float2(d4.z, d4.w)));
+                dsk[t] = pack2<BF16>(ds01.x, ds01.y);
+                dsk[t + 1] = pack2<BF16>(ds23.x, ds23.y);
               }
               // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
               uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
@@ -989,24 +1027,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         // without steps (masked) stores zeros.
         ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, r & 1, ctx, 132));
         if (!ok) break;
-        uint32_t pa[2][16] = {};
+        uint32_t pa[D / 32][16] = {};
         if (w.nsteps > 0) {
           tc_fence_after();
-          load_acc32(lane_base, (wg ? C::COL_DK : C::COL_DV), wg ? scale : 1.f, pa[0]);
-          load_acc32(lane_base, (wg ? C::COL_DK : C::COL_DV) + 32, wg ? scale : 1.f, pa[1]);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c)
+            load_acc32(lane_base, (wg ? C::COL_DK : C::COL_DV) + c * 32, wg ? scale : 1.f, pa[c]);
         }
         tc_fence_before();
         mbar_arrive(bar + B_ACC_EMPTY);  // the accumulators may be overwritten
-        if (!(ok = stage_begin())) break;
-        stage_row32(stg + wg * (BN * 128), rit, 0, pa[0]);
-        stage_row32(stg + wg * (BN * 128), rit, 1, pa[1]);
-        ok = stage_end();
-        if (leader && ok) {
-          tma_store_3d(&tm_dv, stg, 0, w.k0, w.kvh);
-          tma_store_3d(&tm_dk, stg + BN * 128, 0, w.k0, w.kvh);
-          bulk_commit_group();
+        // one [128 rows][64 columns] box of dV (warpgroup 0) and of dK (warpgroup 1) per round
+#pragma unroll
+        for (int b = 0; b < D / 64 && ok; ++b) {
+          if (!(ok = stage_begin())) break;
+          stage_row32(stg + wg * (BN * 128), rit, 0, pa[2 * b]);
+          stage_row32(stg + wg * (BN * 128), rit, 1, pa[2 * b + 1]);
+          ok = stage_end();
+          if (leader && ok) {
+            tma_store_3d(&tm_dv, stg, b * 64, w.k0, w.kvh);
+            tma_store_3d(&tm_dk, stg + BN * 128, b * 64, w.k0, w.kvh);
+            bulk_commit_group();
+          }
+          ++stg_uses;
         }
-        ++stg_uses;
+        if (!ok) break;
       }
       if (leader) bulk_wait_group<0>();  // every reduction and store issued here has completed
     }

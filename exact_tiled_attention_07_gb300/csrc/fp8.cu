@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           for (int c = 0; c < BN; ++c)
             if (c >= limit) s[c] = -INFINITY;
         }
-        const float mx = row_max(s);
+        const float mx = row_max3(s);
         const float m_blk = mx * st;
         float alpha = 1.f;
         bool rescale = false;
@@ -679,18 +679,18 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         // P sv / sv_max = exp2(S st - m + log2(sv / sv_max)): the V factor rides in the exponent,
         // and the row sum of P is that of the scaled values divided by the factor once per tile
         const float neg_m = ((m == -INFINITY) ? 0.f : -m) + lpv;
-        float part[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: no single long add chain
+        // two partial sums of pairs (paired fp32 FMA and adds): no single long add chain
+        float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(s[4 * i], st, neg_m));
-          const float p1 = ex2(fmaf(s[4 * i + 1], st, neg_m));
-          const float p2 = ex2(fmaf(s[4 * i + 2], st, neg_m));
-          const float p3 = ex2(fmaf(s[4 * i + 3], st, neg_m));
-          part[i & 3] += (p0 + p1) + (p2 + p3);
-          pk[i] = pack4_e4m3(p0, p1, p2, p3);
+          const float2 x01 = ffma2(make_float2(s[4 * i], s[4 * i + 1]), st, neg_m);
+          const float2 x23 = ffma2(make_float2(s[4 * i + 2], s[4 * i + 3]), st, neg_m);
+          const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y)), p23 = make_float2(ex2(x23.x), ex2(x23.y));
+          part[i & 1] = fadd2(part[i & 1], fadd2(p01, p23));
+          pk[i] = pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
         }
-        const float sum = ((part[0] + part[1]) + (part[2] + part[3])) / pv;
+        const float sum = ((part[0].x + part[1].x) + (part[0].y + part[1].y)) / pv;
         tmem_st32(tmem_addr(tbase, lane_base, s_col), pk);
         l = l * alpha + sum;
         if (__any_sync(0xffffffffu, rescale)) {

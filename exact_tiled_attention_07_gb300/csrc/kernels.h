@@ -38,7 +38,7 @@ struct FwdArgs {
 
 // Backward workspace, carved from one caller buffer of fa_bwd_workspace_size bytes:
 //   delta  [bh][npad]     fp32  D_i = sum_k dO_ik O_ik (0 on padding rows)
-//   lse2   [bh][npad]     fp32  L_i * log2(e) (+inf on padding rows)
+//   lse2   [bh][npad]     fp32  -L_i * log2(e) (-inf on padding rows and rows with L = -inf)
 //   dq_acc [bh][npad][d]  fp32  accumulated dS K (before the factor tau)
 struct BwdArgs {
   const void* q;

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt(const T* __restrict__ 
     load_rows(dos, d + 1, dO + hoff, q0, kTile, n, d);
     if (threadIdx.x < kTile) {
       const int qi = q0 + threadIdx.x;
-      ls[threadIdx.x] = qi < n ? lse2[(int64_t)bh * npad + qi] : INFINITY;
+      ls[threadIdx.x] = qi < n ? lse2[(int64_t)bh * npad + qi] : -INFINITY;
       ds_[threadIdx.x] = qi < n ? delta[(int64_t)bh * npad + qi] : 0.f;
     }
     __syncthreads();
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv_simt(const T* __restrict__ 
           s = fmaf(qs[lane * (d + 1) + c], kb[jl * d + c], s);
           dp = fmaf(dos[lane * (d + 1) + c], vb[jl * d + c], dp);
         }
-        p = exp2f(s * scale_log2 - ls[lane]);
+        p = exp2f(fmaf(s, scale_log2, ls[lane]));
         dsv = p * (dp - ds_[lane]);
       }
       for (int r = 0; r < kTile; ++r) {
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt(const T* __restrict__ Q,
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const int row = r0 + warp * 4 + t;
-    lrow[t] = row < n ? lse2[(int64_t)bh * npad + row] : INFINITY;
+    lrow[t] = row < n ? lse2[(int64_t)bh * npad + row] : -INFINITY;
     drow[t] = row < n ? delta[(int64_t)bh * npad + row] : 0.f;
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) acc[t][i] = 0.f;
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq_simt(const T* __restrict__ Q,
           s = fmaf(qs[rl * d + c], ks[lane * (d + 1) + c], s);
           dp = fmaf(dos[rl * d + c], vs[lane * (d + 1) + c], dp);
         }
-        const float p = exp2f(s * scale_log2 - lrow[t]);
+        const float p = exp2f(fmaf(s, scale_log2, lrow[t]));
         dsv = p * (dp - drow[t]);
       }
       for (int j = 0; j < kTile; ++j) {
@@ -321,9 +321,9 @@ __global__ void __launch_bounds__(256) bwd_pre(const T* __restrict__ O, const T*
   }
   if (lane == 0) {
     delta[gw] = row < n ? acc : 0.f;
-    // +inf (P = 0) on padding rows and on rows that saw no key (L = -inf)
+    // -L log2 e; -inf (P = 0) on padding rows and on rows that saw no key (L = -inf)
     const float lv = row < n ? lse[bh * n + row] : -INFINITY;
-    lse2[gw] = lv > -INFINITY ? lv * 1.4426950408889634f : INFINITY;
+    lse2[gw] = lv > -INFINITY ? -lv * 1.4426950408889634f : -INFINITY;
   }
   float* q = dq_acc + gw * d;
   for (int c = lane; c < d; c += 32) q[c] = 0.f;
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(256) bwd_pre_vec(const T* __restrict__ O, cons
   if (sub == 0) {
     delta[grow] = row < n ? acc : 0.f;
     const float lv = row < n ? lse[bh * n + row] : -INFINITY;
-    lse2[grow] = lv > -INFINITY ? lv * 1.4426950408889634f : INFINITY;
+    lse2[grow] = lv > -INFINITY ? -lv * 1.4426950408889634f : -INFINITY;
   }
   float4* q = reinterpret_cast<float4*>(dq_acc + grow * d + sub * 8);
   q[0] = make_float4(0.f, 0.f, 0.f, 0.f);
