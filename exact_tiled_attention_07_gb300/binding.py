@@ -12,6 +12,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
+import warnings
 
 import torch
 
@@ -39,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "fa_last_error_message", "fa_bwd_noalloc", "fa_fwd_gqa", "fa_bwd_gqa", "fa_decode", "fa_decode_workspace_size",
     "fa_quantize_fp8", "fa_fwd_fp8", "fa_fwd_fp8_gqa", "fa_fwd_masked", "fa_bwd_masked",
     "fa_selftest_bounded_wait", "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size", "fa_sm_clock_sample",
+    "fa_debug_build", "fa_selftest_debug_check",
 )
 
 _lib = None
@@ -55,15 +57,19 @@ def library_path() -> str:
     return os.path.join(HERE, LIB_FILE)
 
 
-def load_library():
-    """Load ``libfa_gb300.so`` (built by ``exact_tiled_attention_07_gb300.build``); raises if absent."""
+def load_library(path=None):
+    """Load ``libfa_gb300.so`` (built by ``exact_tiled_attention_07_gb300.build``); raises if absent.
+
+    With ``path``, load that build of the library instead (for instance the FA_DEBUG build,
+    ``build.build(debug=True)``) and make it the one every entry point here calls.
+    """
     global _lib
-    if _lib is not None:
+    if path is None and _lib is not None:
         return _lib
     with _lock:
-        if _lib is not None:
+        if path is None and _lib is not None:
             return _lib
-        path = library_path()
+        path = path or library_path()
         if not os.path.exists(path):
             raise RuntimeError(f"the CUDA library {path} is not built; run __graft_entry__.build() first")
         lib = ctypes.CDLL(path)
@@ -92,6 +98,9 @@ def load_library():
         lib.fa_fwd_bwd_host.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, i, i, vp]
         lib.fa_check_device_error.argtypes = [vp]
         lib.fa_sm_clock_sample.argtypes = [vp, i, vp]
+        lib.fa_debug_build.argtypes = []
+        lib.fa_debug_build.restype = ctypes.c_int
+        lib.fa_selftest_debug_check.argtypes = [i, i, vp]
         lib.fa_tile_counter.argtypes = [vp, ctypes.POINTER(ctypes.c_ulonglong), i]
         lib.fa_uses_tensor_cores.argtypes = [i, i, i]
         lib.fa_status_string.argtypes = [i]
@@ -103,7 +112,8 @@ def load_library():
                      "fa_fwd_masked", "fa_bwd_masked", "fa_selftest_bounded_wait", "fa_fwd_bwd_host",
                      "fa_bwd_noalloc", "fa_bwd_preprocess",
                      "fa_bwd_main", "fa_bwd_dq_convert",
-                     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_sm_clock_sample"):
+                     "fa_check_device_error", "fa_tile_counter", "fa_uses_tensor_cores", "fa_sm_clock_sample",
+                     "fa_selftest_debug_check"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -415,6 +425,16 @@ def fa_sm_clock_sample(out, stream=None):
     _check(load_library().fa_sm_clock_sample(_p(out), out.numel() // 3, _stream(stream)))
 
 
+def fa_debug_build() -> bool:
+    """Whether the loaded library was built with FA_DEBUG (device-side index checks)."""
+    return bool(load_library().fa_debug_build())
+
+
+def fa_selftest_debug_check(index, limit, stream=None):
+    """Launch one device index check of index against [0, limit) (debug builds; see include/fa.h)."""
+    _check(load_library().fa_selftest_debug_check(int(index), int(limit), _stream(stream)))
+
+
 def fa_check_device_error(stream=None):
     _check(load_library().fa_check_device_error(_stream(stream)))
 
@@ -443,10 +463,18 @@ def fa_last_error_message() -> str:
 # ---------------------------------------------------------------------------
 
 
+def _warn_cuda_core(pass_, t, d):
+    """A 16-bit pass with no tensor-core kernel runs on the CUDA-core kernels: say so."""
+    if t.dtype != torch.float32 and not fa_uses_tensor_cores(pass_, t.dtype, d):
+        warnings.warn(f"{t.dtype} {'forward' if pass_ == 'fwd' else 'backward'} at d={d} runs on the CUDA-core "
+                      f"kernels (fp32 arithmetic): no tensor-core kernel for this head dimension", stacklevel=3)
+
+
 def attention_forward(q, k, v, causal=False, scale=None, stream=None, window=0, block_mask=None):
     """O, L = fa_fwd(q, k, v) (fa_fwd_gqa when k, v have fewer heads than q; fa_fwd_masked with a
     window or a block mask); outputs on q's device."""
     B, H, N, d = _shape4(q)
+    _warn_cuda_core("fwd", q, d)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
@@ -464,6 +492,7 @@ def attention_backward(q, k, v, o, do, lse, causal=False, scale=None, workspace=
     """dQ, dK, dV = fa_bwd(...) (fa_bwd_masked with a window or a block mask); outputs (and
     workspace, unless given) allocated with torch."""
     B, H, N, d = _shape4(q)
+    _warn_cuda_core("bwd", q, d)
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:

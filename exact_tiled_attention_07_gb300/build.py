@@ -19,6 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
+DEBUG_BUILD_DIR = os.path.join(HERE, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(HERE, "libfa_gb300_debug.so")
 
 SOURCES = ["api.cu", "simt.cu", "fwd_tc.cu", "bwd_tc.cu", "noalloc.cu", "decode.cu", "decode_tc.cu", "fp8.cu", "selftest.cu",
            "pipeline.cu"]
@@ -34,11 +36,12 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build the library")
 
 
-def _compile(nvcc: str, src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc, *ARCH, *CFLAGS, "-I", INCLUDE, "-I", CSRC, "-Xptxas", "-v", "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(nvcc: str, src: str, verbose: bool, build_dir: str = BUILD_DIR, extra=()) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc, *ARCH, *CFLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-Xptxas", "-v", "-c", os.path.join(CSRC, src),
+           "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
-    log = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".ptxas.log")
+    log = os.path.join(build_dir, os.path.splitext(src)[0] + ".ptxas.log")
     with open(log, "w") as f:
         f.write(r.stdout + r.stderr)
     if r.returncode != 0:
@@ -48,29 +51,36 @@ def _compile(nvcc: str, src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile every CUDA source for sm_103a and link the shared library; returns its path."""
+def build(verbose: bool = False, force: bool = False, debug: bool = False) -> str:
+    """Compile every CUDA source for sm_103a and link the shared library; returns its path.
+
+    debug=True builds ``libfa_gb300_debug.so`` instead, with FA_DEBUG defined: the kernels then
+    check their work-item, tile and row indices and record a device error on a failed check.
+    """
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    extra = ["-DFA_DEBUG=1"] if debug else []
+    os.makedirs(build_dir, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "fa.h"))
-    if not force and os.path.exists(LIB_PATH):
+    if not force and os.path.exists(lib_path):
         newest = max(os.path.getmtime(p) for p in srcs + headers)
-        if os.path.getmtime(LIB_PATH) >= newest:
-            return LIB_PATH
+        if os.path.getmtime(lib_path) >= newest:
+            return lib_path
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(nvcc, s, verbose), SOURCES))
-    tmp = LIB_PATH + ".tmp"
+        objs = list(ex.map(lambda s: _compile(nvcc, s, verbose, build_dir, extra), SOURCES))
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     if verbose:
-        print(f"[build] linked {LIB_PATH}")
-    return LIB_PATH
+        print(f"[build] linked {lib_path}")
+    return lib_path
 
 
 if __name__ == "__main__":

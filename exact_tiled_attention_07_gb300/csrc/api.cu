@@ -105,6 +105,17 @@ fa_status launched(cudaError_t e, const char* what) {
   return FA_OK;
 }
 
+// A 16-bit call that had no tensor-core kernel and ran on the CUDA-core kernels: it succeeded,
+// and the calling thread's message says which path ran (nothing changes backend silently).
+fa_status note_cuda_core_path(fa_status st, const char* pass, fa_dtype dtype, int d) {
+  if (st == FA_OK && dtype != FA_FP32)
+    snprintf(t_msg, sizeof(t_msg),
+             "notice: the %s %s pass at d=%d ran on the CUDA-core kernels (fp32 arithmetic): no tensor-core "
+             "kernel for this head dimension",
+             dtype == FA_BF16 ? "bf16" : "fp16", pass, d);
+  return st;
+}
+
 // after the per-row vectors and the dQ accumulator: the backward's work-item queue counters
 constexpr size_t kSchedBytes = 256;
 
@@ -228,7 +239,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   a.mask_heads = mask.mask_heads;
   a.heads = H;
   if (fwd_tc_supported(a.dtype, d)) return launched(launch_fwd_tc(a), "forward (tensor-core kernel)");
-  return launched(launch_fwd_simt(a), "forward (CUDA-core kernel)");
+  return note_cuda_core_path(launched(launch_fwd_simt(a), "forward (CUDA-core kernel)"), "forward", dtype, d);
 }
 
 fa_status bwd_main_impl(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
@@ -266,7 +277,7 @@ fa_status bwd_main_impl(const void* Q, const void* K, const void* V, const void*
   a.mask_heads = mask.mask_heads;
   a.heads = H;
   if (bwd_tc_supported(a.dtype, d)) return launched(launch_bwd_tc(a), "backward (tensor-core kernel)");
-  return launched(launch_bwd_simt(a), "backward (CUDA-core kernels)");
+  return note_cuda_core_path(launched(launch_bwd_simt(a), "backward (CUDA-core kernels)"), "backward", dtype, d);
 }
 
 }  // namespace
@@ -347,7 +358,8 @@ fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O,
   if ((st = bwd_main_impl(Q, K, V, dO, dK, dV, workspace, workspace_bytes, B, H, Hkv, N, d, scale, causal, dtype,
                           stream, "fa_bwd")) != FA_OK)
     return st;
-  return fa_bwd_dq_convert(workspace, workspace_bytes, dQ, B, H, N, d, scale, dtype, stream);
+  st = fa_bwd_dq_convert(workspace, workspace_bytes, dQ, B, H, N, d, scale, dtype, stream);
+  return bwd_tc_supported((int)dtype, d) ? st : note_cuda_core_path(st, "backward", dtype, d);
 }
 
 fa_status fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Hkv, int N,
@@ -542,6 +554,8 @@ fa_status fa_check_device_error(void* stream) {
   const unsigned long long block = w & 0xFFFFFFFFFFull;
   if (code == DERR_TIMEOUT)
     return fail(FA_ERR_TIMEOUT, "a bounded wait expired (site %u, block %llu)", site, block);
+  if (code == DERR_BOUNDS)
+    return fail(FA_ERR_DEVICE, "device index check failed (site %u, block %llu)", site, block);
   return fail(FA_ERR_DEVICE, "device check %u failed (site %u, block %llu)", code, site, block);
 }
 
@@ -554,6 +568,17 @@ fa_status fa_selftest_bounded_wait(int timeout_ms, int arrive, void* stream) {
   return launched(launch_bounded_wait_selftest(syms.err, timeout_ms, arrive ? 1 : 0, static_cast<cudaStream_t>(stream)),
                   "fa_selftest_bounded_wait");
 }
+
+fa_status fa_selftest_debug_check(int index, int limit, void* stream) {
+  if (!FA_DEBUG_CHECKS) return fail(FA_ERR_UNSUPPORTED, "fa_selftest_debug_check: library built without FA_DEBUG");
+  DeviceSyms syms;
+  fa_status st = device_syms(&syms);
+  if (st != FA_OK) return st;
+  return launched(launch_debug_check_selftest(syms.err, index, limit, static_cast<cudaStream_t>(stream)),
+                  "fa_selftest_debug_check");
+}
+
+int fa_debug_build(void) { return FA_DEBUG_CHECKS; }
 
 fa_status fa_sm_clock_sample(unsigned long long* out, int blocks, void* stream) {
   if (!out || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "fa_sm_clock_sample: null or misaligned output");

@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         if (item < 0) break;
         const BwdItem w = item_at(item);
+        if (!(ok = debug_check(w.kvh >= 0 && w.kvh < bh_count && w.k0 >= 0 && w.k0 < n, ctx, 160))) break;
         // K_j, V_j once the tensor core no longer reads the previous item's
         if (r > 0 && !(ok = mbar_wait(bar + B_KV_EMPTY, (r - 1) & 1, ctx, 113))) break;
         mbar_arrive_expect_tx(bar + B_KV, 2 * C::KV_BYTES);
@@ -387,6 +388,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           int gm, q0;
           step_rows(w, i, ii, g, &gm, &q0);
           const int qh = w.kvh * group + gm;
+          // the L and D rows of the step lie inside the head's padded vectors
+          if (!(ok = debug_check(gm >= 0 && gm < group && q0 >= 0 && q0 + BM <= npad, ctx, 161))) break;
           uint64_t* fb = bar + B_QD_FULL + s;
           mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + 2 * BM * 4);
           for (int kb = 0; kb < C::KB; ++kb) {

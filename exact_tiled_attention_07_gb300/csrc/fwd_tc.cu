@@ -369,6 +369,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int r = 0, item = draw(0); ok && item >= 0; item = draw(++r)) {
         const Item w = item_at(item);
         const int nmax = max(w.nq[0], w.nq[1]);
+        if (!(ok = debug_check(w.head < bh_count && w.kvhead * group < bh_count && w.qrow0 < n && nmax <= nblocks,
+                               ctx, 60)))
+          break;
         // Q of this item once the previous item's S = Q K^T are done
         if (q_loads > 0 && !(ok = mbar_wait(B.q_empty, (q_loads - 1) & 1, ctx, 13))) break;
         mbar_arrive_expect_tx(B.q_full, C::NQ * C::Q_BYTES);
@@ -381,6 +384,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           bool is_v;
           int j;
           ring_tile(idx, nmax, &is_v, &j);
+          if (!(ok = debug_check(j >= 0 && j < nmax && tile_at(j) >= 0 && tile_at(j) < nblocks, ctx, 61))) break;
           const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
           for (int e = 0; e < C::RB; ++e) {
             const uint32_t g = ring_pos;

@@ -163,6 +163,9 @@ cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a);
 // completes itself when arrive != 0.
 cudaError_t launch_bounded_wait_selftest(unsigned long long* err, int timeout_ms, int arrive, cudaStream_t stream);
 
+// One device index check, as debug builds make them: index outside [0, limit) is recorded.
+cudaError_t launch_debug_check_selftest(unsigned long long* err, int index, int limit, cudaStream_t stream);
+
 // Block b of `blocks` (one per SM when blocks <= the SM count) writes {SM id, SM cycle counter,
 // global timer in ns} to out[3 b], out[3 b + 1], out[3 b + 2].
 cudaError_t launch_sm_clock_sample(unsigned long long* out, int blocks, cudaStream_t stream);

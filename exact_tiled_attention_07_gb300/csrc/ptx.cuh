@@ -19,7 +19,7 @@ namespace fa {
 // ---------------------------------------------------------------------------
 // device error word: [63:56] code, [55:40] site, [39:0] linear block index
 // ---------------------------------------------------------------------------
-enum DeviceErr : uint32_t { DERR_NONE = 0, DERR_TIMEOUT = 1, DERR_BAD_SMEM_ALIGN = 2, DERR_BAD_ARG = 3 };
+enum DeviceErr : uint32_t { DERR_NONE = 0, DERR_TIMEOUT = 1, DERR_BAD_SMEM_ALIGN = 2, DERR_BAD_ARG = 3, DERR_BOUNDS = 4 };
 
 // Where a CTA reports failures: the library's device error word and the CTA's
 // shared abort flag (raised by the first role that gives up).
@@ -34,6 +34,30 @@ __device__ __forceinline__ void report_error(unsigned long long* err, uint32_t c
   unsigned long long w = ((unsigned long long)code << 56) | ((unsigned long long)(site & 0xFFFF) << 40) |
                          (blk & 0xFFFFFFFFFFull);
   if (err) atomicCAS(err, 0ull, w);
+}
+
+// Device-side index checks of debug builds (compiled with FA_DEBUG): a failed check records
+// (DERR_BOUNDS, site) in the error word, raises the CTA's abort flag (every bounded wait then
+// gives up) and returns false, so the caller skips the access and winds down; nothing traps.
+// Release builds compile the checks away.
+#ifdef FA_DEBUG
+#define FA_DEBUG_CHECKS 1
+#else
+#define FA_DEBUG_CHECKS 0
+#endif
+template <typename Ctx>
+__device__ __forceinline__ bool debug_check(bool ok, const Ctx& ctx, uint32_t site) {
+  if constexpr (FA_DEBUG_CHECKS) {
+    if (!ok) {
+      report_error(ctx.err, DERR_BOUNDS, site);
+      *ctx.abort = 1;
+    }
+    return ok;
+  } else {
+    (void)ctx;
+    (void)site;
+    return true;
+  }
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -13,6 +13,16 @@ namespace fa {
 namespace {
 
 constexpr uint32_t kSelftestSite = 900;
+constexpr uint32_t kDebugCheckSite = 901;
+
+// One index check of the kind debug builds make inside the kernels (debug_check): out of
+// [0, limit) it is recorded as a failed device check at site 901.
+__global__ void debug_check_selftest_kernel(unsigned long long* err, int index, int limit) {
+  __shared__ int abort_flag;
+  abort_flag = 0;
+  const ErrCtx ctx{err, &abort_flag};
+  debug_check(index >= 0 && index < limit, ctx, kDebugCheckSite);
+}
 
 __global__ void bounded_wait_selftest_kernel(unsigned long long* err, uint64_t limit_ns, int arrive) {
   __shared__ __align__(8) uint64_t bar;
@@ -55,6 +65,11 @@ cudaError_t launch_sm_clock_sample(unsigned long long* out, int blocks, cudaStre
                                        kClockSampleSmem);
   if (e != cudaSuccess) return e;
   sm_clock_sample_kernel<<<blocks, 32, kClockSampleSmem, stream>>>(out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_check_selftest(unsigned long long* err, int index, int limit, cudaStream_t stream) {
+  debug_check_selftest_kernel<<<1, 1, 0, stream>>>(err, index, limit);
   return cudaGetLastError();
 }
 

@@ -33,7 +33,10 @@
  *   Paths     bf16/fp16 with d in {64, 128, 256} (forward) or {64, 128} (backward)
  *             run the tensor-core kernels (TMA, tcgen05 MMAs accumulating in tensor
  *             memory); fp32, and any other d in [1, 256], run CUDA-core kernels that
- *             compute in fp32.
+ *             compute in fp32. The choice is never silent: fa_uses_tensor_cores() tells it
+ *             in advance, and a bf16/fp16 call that runs on the CUDA-core kernels (another
+ *             d, or the d = 256 backward) returns FA_OK with a notice in
+ *             fa_last_error_message() naming the path that ran.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -298,6 +301,18 @@ FA_API fa_status fa_check_device_error(void* stream);
 FA_API fa_status fa_selftest_bounded_wait(int timeout_ms, int arrive, void* stream);
 
 /*
+ * Debug builds. The library built with FA_DEBUG (exact_tiled_attention_07_gb300/build.py,
+ * debug=True: libfa_gb300_debug.so) checks work-item, tile and row indices inside the kernels;
+ * a failed check records a device error (fa_check_device_error: FA_ERR_DEVICE, "device index
+ * check failed"), stops the kernel's roles through their bounded waits and never traps.
+ * fa_debug_build() is 1 in such a library, 0 otherwise. fa_selftest_debug_check launches one
+ * such check of index against [0, limit) (a debug build records a failure when it is outside);
+ * a release build returns FA_ERR_UNSUPPORTED.
+ */
+FA_API int fa_debug_build(void);
+FA_API fa_status fa_selftest_debug_check(int index, int limit, void* stream);
+
+/*
  * Diagnostic: number of (query tile, key tile) pairs the forward kernels processed on the
  * current device since the last reset (128 x 128 tiles on the tensor-core path, 32 x 32 on
  * the CUDA-core path); skipped causal tiles are not counted. Synchronises `stream`;
@@ -322,7 +337,8 @@ FA_API int fa_uses_tensor_cores(int pass, fa_dtype dtype, int d);
 /* Static text for a status code. */
 FA_API const char* fa_status_string(fa_status status);
 
-/* Description of the last failure on the calling thread ("" if none). */
+/* Description of the last failure on the calling thread ("" if none), or, after a successful
+ * 16-bit call that ran on the CUDA-core kernels, a notice saying so (starting "notice:"). */
 FA_API const char* fa_last_error_message(void);
 
 #ifdef __cplusplus

@@ -196,3 +196,15 @@ def test_host_pipeline_rejects_null_host_pointers_before_any_cuda_call(lib):
     assert f(*([None] * 10), 0, 1, 2, 2, 128, 64, 0.125, 1, 0, 0, None) != 0
     lib.fa_last_error_message.restype = ctypes.c_char_p
     assert b"null" in lib.fa_last_error_message()
+
+
+def test_release_and_debug_builds(lib):
+    # the release library compiles the device index checks away; the FA_DEBUG build keeps them
+    # (its kernels are exercised on the GPU by tests/test_gpu_debug_build.py)
+    from exact_tiled_attention_07_gb300 import build as b
+
+    lib.fa_debug_build.restype = ctypes.c_int
+    assert lib.fa_debug_build() == 0
+    dbg = ctypes.CDLL(b.build(debug=True))
+    dbg.fa_debug_build.restype = ctypes.c_int
+    assert dbg.fa_debug_build() == 1

@@ -107,11 +107,41 @@ def test_tensor_core_fwd_d256(fa, dtype, causal, n):
 
 @pytest.mark.parametrize("d", [32, 96, 256])
 def test_cuda_core_path_16bit(fa, d):
-    # head dims without a tensor-core kernel (and the d = 256 backward) use the CUDA-core kernels
+    # head dims without a tensor-core kernel (and the d = 256 backward) use the CUDA-core kernels;
+    # the binding warns about it before the call
     w = Workload("simt16", 1, 2, 150, d, "bf16", True, "normal", 3000 + d)
-    x64, got = _run(fa, w)
+    with pytest.warns(UserWarning, match="CUDA-core"):
+        x64, got = _run(fa, w)
     _check_fwd(w, x64, got)
     _check_bwd(w, x64, got)
+
+
+@pytest.mark.parametrize("d,pass_", [(96, "forward"), (256, "backward"), (32, "backward")])
+def test_cuda_core_path_is_reported_by_the_c_abi(fa, d, pass_):
+    # a 16-bit call that runs on the CUDA-core kernels succeeds and leaves a notice naming the
+    # path; a tensor-core call leaves none
+    w = Workload("notice", 1, 1, 130, d, "fp16", False, "normal", 3100 + d)
+    x = {k: to_device(v, w.dtype) for k, v in make_inputs(w).items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((1, 1, 130), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, w.scale, False)
+    if pass_ == "forward":
+        msg = fa.fa_last_error_message()
+        assert msg.startswith("notice:") and "forward" in msg and f"d={d}" in msg, msg
+        return
+    fwd_msg = fa.fa_last_error_message()
+    assert (fwd_msg == "") == fa.fa_uses_tensor_cores("fwd", torch.float16, d), fwd_msg
+    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_size(1, 1, 130, d), dtype=torch.uint8, device="cuda")
+    fa.fa_bwd(x["q"], x["k"], x["v"], o, x["do"], lse, dq, dk, dv, ws, w.scale, False)
+    msg = fa.fa_last_error_message()
+    assert msg.startswith("notice:") and "backward" in msg and f"d={d}" in msg, msg
+    fa.fa_check_device_error()
+    # a tensor-core call clears it
+    w2 = Workload("notice_tc", 1, 1, 130, 64, "fp16", False, "normal", 3200)
+    x2 = {k: to_device(v, w2.dtype) for k, v in make_inputs(w2, with_do=False).items()}
+    fa.fa_fwd(x2["q"], x2["k"], x2["v"], torch.empty_like(x2["q"]), lse, w2.scale, False)
+    assert fa.fa_last_error_message() == ""
 
 
 def test_large_score_offsets_stress_rescaling(fa):
