@@ -11,9 +11,13 @@
 // O += P8 V8 are kind::f8f6f4 MMAs (K = 32 per instruction).  The block scales enter as
 //   S_ij = tau * sq(i) * sk(j) * (Q8 K8^T)_ij        (one factor per pair of tiles),
 //   O_i  = sum_j P_ij sv(j) V8_j / l_i,
-// with sv(j) folded into P before it is rounded to E4M3: P8 = E4M3(P * sv(j) / sv_max), where
-// sv_max is the head's largest V scale, so P8 <= 2^8 (the lazy-rescale bound) stays inside
-// E4M3's range, and the epilogue multiplies O by sv_max / l.  l sums the unrounded P.
+// with sv(j) folded into P before it is rounded to E4M3: P8 = E4M3(exp2(S st + log2 sv(j) - m)),
+// where the online softmax's running maximum m is taken over S st + log2 sv(j): so P8 <= 2^8
+// (the lazy-rescale bound) stays inside E4M3's range and a row's largest V-weighted
+// probabilities stay near 1 whatever the spread of the V scales (a head-wide reference, the
+// head's largest V scale, let the probabilities of small-scale blocks sink into E4M3's subnormal
+// range).  l sums the unrounded probabilities exp2(S st - m) (each tile's sum divided by sv(j)),
+// and the epilogue divides O by l.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -297,16 +301,19 @@ constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
 constexpr float kRescaleThreshold = 8.0f;
 
-// d = 128: one 128-byte row per tile row, so every tile is a single TMA box
+// d = 128: one 128-byte row per tile row (128-byte swizzle); d = 64: one 64-byte row (64-byte
+// swizzle); either way every tile is a single TMA box
+template <int D_>
 struct Fp8Cfg {
-  static constexpr int D = 128;
+  static constexpr int D = D_;
+  static constexpr int SW = D;                // swizzle width in bytes = row length
   static constexpr int NQ = 2;
-  static constexpr int TILE_BYTES = 128 * D;  // 16 KB (Q, K or V tile)
-  static constexpr int STAGES = 12;
+  static constexpr int TILE_BYTES = 128 * D;  // 16 / 8 KB (Q, K or V tile)
+  static constexpr int STAGES = D == 128 ? 12 : 24;
   static constexpr int PRODUCER_WARP = 8;
   static constexpr int MMA_WARP = 9;
   static constexpr int THREADS = 320;
-  static constexpr int S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 384;
+  static constexpr int S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = NQ * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_RING + STAGES * TILE_BYTES;
@@ -320,15 +327,15 @@ struct Fp8Cfg {
 // from the queue when the launch has a slot (QUEUE) or in grid order; q_empty lets an item's Q
 // load once the last S of the previous item is issued, o_empty lets an item's first P V overwrite
 // O once the softmax has read it, and every phase runs on counters that continue across items.
-template <bool OUT_BF16, bool QUEUE>
-__global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
+template <int DH, bool OUT_BF16, bool QUEUE>
+__global__ void __launch_bounds__(Fp8Cfg<DH>::THREADS, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ q_scales,
                    const float* __restrict__ k_scales, const float* __restrict__ v_scales, void* __restrict__ out,
                    float* __restrict__ lse, int n, int bh_count, int tiles_per_head, float scale_log2, int causal,
                    int group, unsigned long long* err, unsigned long long* counter, unsigned* __restrict__ sched,
                    int hgroup) {
-  using C = Fp8Cfg;
+  using C = Fp8Cfg<DH>;
   constexpr int D = C::D;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -349,7 +356,6 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
-  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);                   // [2][8]
   const ErrCtx ctx{err, abort_flag};
 
   const int nblk = (n + BN - 1) / BN;  // 128-row blocks per head: key tiles and scale entries
@@ -505,15 +511,19 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         if (leader) umma_commit(b);
         __syncwarp();
       };
-      // S = Q8_q K8^T: 32 bytes (32 elements) of the 128-byte rows per instruction
+      // K-major 8-bit tile rows of D bytes in 8-row swizzle atoms of 8 D bytes
+      auto sdesc = [](uint32_t addr, uint32_t lbo, uint32_t sbo) {
+        return C::SW == 128 ? make_sdesc_sw128(addr, lbo, sbo) : make_sdesc_sw64(addr, lbo, sbo);
+      };
+      // S = Q8_q K8^T: 32 bytes (32 elements) of the D-byte rows per instruction
       auto issue_qk = [&](int q, int kidx, uint32_t s_col) {
         const uint32_t kt = ring + slot_of(kidx) * C::TILE_BYTES;
         const uint32_t qt = q_base + q * C::TILE_BYTES;
         uint64_t ad[D / 32], bd[D / 32];
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk) {
-          ad[kk] = make_sdesc_sw128(qt + kk * 32, 16, 1024);
-          bd[kk] = make_sdesc_sw128(kt + kk * 32, 16, 1024);
+          ad[kk] = sdesc(qt + kk * 32, 16, 8 * C::SW);
+          bd[kk] = sdesc(kt + kk * 32, 16, 8 * C::SW);
         }
         if (leader) {
 #pragma unroll
@@ -521,13 +531,13 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         }
         __syncwarp();
       };
-      // O += P8 V8: P8 (4 keys per TMEM column) in [p_col, p_col + 32); V8 MN-major, 32 keys
-      // (4 swizzle atoms of 8 rows) per instruction
+      // O += P8 V8: P8 (4 keys per TMEM column) in [p_col, p_col + 32); V8 MN-major (the d bytes
+      // of a key contiguous), 32 keys (4 swizzle atoms of 8 rows) per instruction
       auto issue_pv = [&](uint32_t o_col, uint32_t p_col, int vidx, bool acc) {
         const uint32_t vt = ring + slot_of(vidx) * C::TILE_BYTES;
         uint64_t bd[BN / 32];
 #pragma unroll
-        for (int kk = 0; kk < BN / 32; ++kk) bd[kk] = make_sdesc_sw128(vt + kk * 4096, BN * 128, 1024);
+        for (int kk = 0; kk < BN / 32; ++kk) bd[kk] = sdesc(vt + kk * 32 * C::SW, BN * C::SW, 8 * C::SW);
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BN / 32; ++kk)
@@ -604,27 +614,16 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     int tq = 0;  // key tiles this query tile processed (all items): S / P phases
     int oq = 0;  // items with a result: O phases
     bool ok = start_ok;
-    // The eight softmax warps meet at a named barrier per item (the head's largest V scale), so
-    // they decide together, through that barrier's reduction, whether to take another item: a
-    // warp whose bounded wait ran out cannot leave the others waiting there.
+    // The eight softmax warps meet at a named barrier per item and decide together, through that
+    // barrier's reduction, whether to take another item: a warp whose bounded wait ran out cannot
+    // leave the others waiting there.
     for (int r = 0;; ++r) {
       bool got = ok;
       const int item = next_item(r, got);
       const bool have = got && item >= 0;
       const Item w = item_of(have ? item : 0);
-      // the head's largest V scale (both warpgroups; partial maxima in red[r % 2])
-      const float* vs = v_scales + (int64_t)w.kvhead * nblk;
-      float svmax = 0.f;
-      if (have)
-        for (int i = threadIdx.x; i < nblk; i += 256) svmax = fmaxf(svmax, vs[i]);
-      for (int o = 16; o > 0; o >>= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, o));
-      float* rd = red + (r & 1) * 8;
-      if (lane == 0) rd[warp] = svmax;
       if (!named_bar_and(1, 256, have)) break;
-      svmax = rd[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i) svmax = fmaxf(svmax, rd[i]);
-      const float inv_svmax = 1.f / svmax;
+      const float* vs = v_scales + (int64_t)w.kvhead * nblk;
       const int head = w.head;
       const int row = w.qrow0 + q * BM + rit;
       const int nb = w.nq[q];
@@ -636,8 +635,8 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       float sk_next = nb > 0 ? ks[0] : 0.f, sv_next = nb > 0 ? vs[0] : 0.f;
       for (int j = 0; ok && j < nb; ++j) {
         const int t = tq + j;
-        const float st = sq_log2 * sk_next;     // tau log2(e) sq sk: S units -> log2 units
-        const float pv = sv_next * inv_svmax;  // sv / sv_max (<= 1), folded into P's exponent
+        const float st = sq_log2 * sk_next;  // tau log2(e) sq sk: S units -> log2 units
+        const float pv = sv_next;            // the key block's V scale, folded into P's exponent
         const float lpv = __log2f(pv);
         if (j + 1 < nb) {
           sk_next = ks[j + 1];
@@ -664,8 +663,10 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           for (int c = 0; c < BN; ++c)
             if (c >= limit) s[c] = -INFINITY;
         }
+        // the running maximum is over S st + log2 sv: a row's largest V-weighted probability stays
+        // near 1 in E4M3, whatever the spread of the V block scales
         const float mx = row_max3(s);
-        const float m_blk = mx * st;
+        const float m_blk = mx * st + lpv;
         float alpha = 1.f;
         bool rescale = false;
         if (m == -INFINITY) {
@@ -676,8 +677,8 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           m = m_blk;
           rescale = true;
         }
-        // P sv / sv_max = exp2(S st - m + log2(sv / sv_max)): the V factor rides in the exponent,
-        // and the row sum of P is that of the scaled values divided by the factor once per tile
+        // P sv = exp2(S st + log2 sv - m): the V factor rides in the exponent, and the row sum of P
+        // is that of the scaled values divided by the factor once per tile
         const float neg_m = ((m == -INFINITY) ? 0.f : -m) + lpv;
         // two partial sums of pairs (paired fp32 FMA and adds): no single long add chain
         float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -713,12 +714,13 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
         tc_fence_before();
         mbar_arrive(p_full + q);
       }
-      // epilogue: O sv_max / l -> global (16-bit), L = (m + log2 l) ln 2
+      // epilogue: O / l -> global (16-bit), L = (m + log2 l) ln 2 (l sums exp2(S st - m), so
+      // m + log2 l is the log2-sum-exp of S st whatever V factors m took in)
       if (ok && nb > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(o_full + q, oq & 1, ctx, 240 + q));
         if (ok) {
           tc_fence_after();
-          const float inv = l > 0.f ? svmax / l : 0.f;
+          const float inv = l > 0.f ? 1.f / l : 0.f;
           uint8_t* orow = reinterpret_cast<uint8_t*>(out) + (((int64_t)head * n + row) * D) * 2;
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -765,20 +767,21 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
   }
 }
 
-template <bool OUT_BF16>
+template <int DH, bool OUT_BF16>
 cudaError_t launch_fwd_fp8_t(const Fp8FwdArgs& a) {
-  using C = Fp8Cfg;
+  using C = Fp8Cfg<DH>;
   CUtensorMap tq, tk, tv;
   const int bh_kv = a.bh / a.group;
-  if (!make_tmap_8bit_3d(&tq, a.q8, C::D, a.n, a.bh, BM) || !make_tmap_8bit_3d(&tk, a.k8, C::D, a.n, bh_kv, BN) ||
-      !make_tmap_8bit_3d(&tv, a.v8, C::D, a.n, bh_kv, BN))
+  if (!make_tmap_8bit_3d(&tq, a.q8, C::D, a.n, a.bh, BM, C::SW) ||
+      !make_tmap_8bit_3d(&tk, a.k8, C::D, a.n, bh_kv, BN, C::SW) ||
+      !make_tmap_8bit_3d(&tv, a.v8, C::D, a.n, bh_kv, BN, C::SW))
     return cudaErrorInvalidValue;
   const int tiles = (a.n + C::NQ * BM - 1) / (C::NQ * BM);
   const int64_t items = (int64_t)a.bh * tiles;
   const int64_t grid = std::min<int64_t>(items, device_sm_count());
   QueueSlot qs;
   if (grid < items) qs = queue_slot_take(a.stream);
-  auto kern = qs.slot >= 0 ? fwd_fp8_kernel<OUT_BF16, true> : fwd_fp8_kernel<OUT_BF16, false>;
+  auto kern = qs.slot >= 0 ? fwd_fp8_kernel<DH, OUT_BF16, true> : fwd_fp8_kernel<DH, OUT_BF16, false>;
   // causal order: groups of query heads whose 8-bit K, V stay in L2
   const int hgroup = head_group_for_l2((int64_t)2 * a.n * C::D / a.group);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -801,11 +804,15 @@ cudaError_t launch_quantize_fp8(const QuantArgs& a) {
   }
 }
 
-bool fwd_fp8_supported(int d) { return d == 128; }
+bool fwd_fp8_supported(int d) { return d == 64 || d == 128; }
 
 cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a) {
-  if (a.d != 128) return cudaErrorNotSupported;
-  return a.out_dtype == DT_BF16 ? launch_fwd_fp8_t<true>(a) : launch_fwd_fp8_t<false>(a);
+  const bool bf = a.out_dtype == DT_BF16;
+  switch (a.d) {
+    case 64: return bf ? launch_fwd_fp8_t<64, true>(a) : launch_fwd_fp8_t<64, false>(a);
+    case 128: return bf ? launch_fwd_fp8_t<128, true>(a) : launch_fwd_fp8_t<128, false>(a);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace fa

@@ -39,18 +39,19 @@ inline bool make_tmap_16bit_3d(CUtensorMap* map, const void* base, bool bf16, ui
 }
 
 // 3-D map over a [heads][rows][cols] row-major array of bytes (FP8 codes), boxes of 128 columns
-// (128 bytes) x box_rows rows with the 128-byte swizzle; rows beyond `rows` read as zero.
+// (128 bytes) x box_rows rows with the 128-byte swizzle, or, for 64-byte rows (swizzle_bytes 64),
+// boxes of 64 columns with the 64-byte swizzle; rows beyond `rows` read as zero.
 inline bool make_tmap_8bit_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t heads,
-                              uint32_t box_rows) {
+                              uint32_t box_rows, uint32_t swizzle_bytes = 128) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {cols, rows, heads};
   cuuint64_t strides[2] = {cols, cols * rows};
-  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t box[3] = {swizzle_bytes, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

@@ -263,12 +263,13 @@ FA_API fa_status fa_quantize_fp8(const void* X, void* X8, float* scales, int B, 
  *   q/k/v_scales         in:  [B][H][ceil(N / 128)] fp32 block scales
  *   O                    out: [B][H][N][d] out_dtype (FA_BF16 or FA_FP16)
  *   L                    out: [B][H][N] fp32, natural-log log-sum-exp of the scaled scores
- *   d                    128
+ *   d                    64 or 128 (other head dims return FA_ERR_UNSUPPORTED)
  * Computes attention of the dequantised tensors (code x block scale): S = scale Q K^T (causal
  * mask when causal != 0), O = softmax(S) V, L = m + ln l. The probabilities are rounded to
- * E4M3 before the P V product (after multiplying by the key block's V scale over the head's
- * largest V scale), so O carries E4M3's relative rounding of P (at most 2^-4 per element);
- * L does not. Pointers 16-byte aligned; the same errors as fa_fwd.
+ * E4M3 before the P V product, after multiplying by the key block's V scale; the online
+ * softmax's running maximum includes that factor, so a row's largest weighted probabilities
+ * stay near 1 whatever the spread of the V scales. O carries E4M3's relative rounding of P (at
+ * most 2^-4 per element above E4M3's subnormal range); L does not. Pointers 16-byte aligned; the same errors as fa_fwd.
  */
 FA_API fa_status fa_fwd_fp8(const void* Q8, const void* K8, const void* V8, const float* q_scales,
                             const float* k_scales, const float* v_scales, void* O, float* L, int B, int H, int N,

@@ -100,8 +100,8 @@ def test_quantize_quotients_at_and_beside_e4m3_midpoints(fa):
     np.testing.assert_array_equal(x8.cpu().numpy(), _codes_to_bytes(codes).numpy())
 
 
-def _fp8_case(b, h, n, seed, spread=True):
-    q, k, v = (_draw((b, h, n, 128), seed + i, spread) for i in range(3))
+def _fp8_case(b, h, n, seed, spread=True, d=128):
+    q, k, v = (_draw((b, h, n, d), seed + i, spread) for i in range(3))
     qc, qs = F8.quantize_blocks(q)
     kc, ks = F8.quantize_blocks(k)
     vc, vs = F8.quantize_blocks(v)
@@ -130,12 +130,13 @@ def _check_o(go, o_ref, vmax):
     assert max_abs(go, o_ref) <= TOL_FP8_O_MAXABS_OF_VMAX * vmax + 1e-3
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n", [128, 129, 300, 1000])
 @pytest.mark.parametrize("out", ["bf16", "fp16"])
-def test_fp8_forward_matches_attention_on_dequantised_inputs(fa, causal, n, out):
-    host, dev = _fp8_case(2, 2, n, 50 + n + causal)
-    scale = 128 ** -0.5
+def test_fp8_forward_matches_attention_on_dequantised_inputs(fa, d, causal, n, out):
+    host, dev = _fp8_case(2, 2, n, 50 + n + causal + d, d=d)
+    scale = d ** -0.5
     odt = torch.bfloat16 if out == "bf16" else torch.float16
     o, lse = fa.attention_forward_fp8(*dev[:3], *dev[3:], scale=scale, causal=causal, out_dtype=odt)
     fa.fa_check_device_error()
@@ -160,13 +161,14 @@ def _exact_values(shape, seed):
     return codes * np.float32(2.0 ** -8)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_forward_exact_sums_meet_the_plain_l_tolerance(fa, causal):
+def test_fp8_forward_exact_sums_meet_the_plain_l_tolerance(fa, causal, d):
     """Inputs whose products and sums are exact in 13 significant bits: S has no rounding beyond
     the tensor core's accumulation, so L must meet the plain 1e-3 (no score-size term); O keeps
     the tolerance of the E4M3 rounding of P."""
     b, h, n = 2, 2, 300
-    q, k, v = (_exact_values((b, h, n, 128), 500 + i) for i in range(3))
+    q, k, v = (_exact_values((b, h, n, d), 500 + i + d) for i in range(3))
     host, dev = [], []
     for t in (q, k, v):
         c, sc = F8.quantize_blocks(t)
@@ -177,7 +179,7 @@ def test_fp8_forward_exact_sums_meet_the_plain_l_tolerance(fa, causal):
     for (c8, s8), c, sc in zip(x8, host[0::2], host[1::2]):
         np.testing.assert_array_equal(c8.cpu().numpy(), _codes_to_bytes(c).numpy())
         np.testing.assert_array_equal(s8.cpu().numpy(), sc)
-    scale = 128 ** -0.5
+    scale = d ** -0.5
     o, lse = fa.attention_forward_fp8(*(c8 for c8, _ in x8), *(s8 for _, s8 in x8), scale=scale, causal=causal)
     fa.fa_check_device_error()
     o_ref, l_ref = F8.attn_fwd64_fp8(*host, scale, causal)
@@ -217,10 +219,11 @@ def test_fp8_forward_full_size_sampled_rows(fa):
 
 
 def test_fp8_argument_checks(fa):
-    z = torch.zeros((1, 1, 128, 64), dtype=torch.uint8, device="cuda")
-    s = torch.ones(1, dtype=torch.float32, device="cuda")
-    with pytest.raises(fa.FAError, match="d = 128"):
-        fa.attention_forward_fp8(z, z, z, s, s, s)
+    for d in (32, 256):
+        z = torch.zeros((1, 1, 128, d), dtype=torch.uint8, device="cuda")
+        s = torch.ones(1, dtype=torch.float32, device="cuda")
+        with pytest.raises(fa.FAError, match="d in"):
+            fa.attention_forward_fp8(z, z, z, s, s, s)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -243,3 +246,21 @@ def test_fp8_forward_grouped_query_heads(fa, causal, h, hkv):
     kx = np.repeat(deq[1], h // hkv, axis=1)
     rows = list(np.ndindex(2, h, n))
     _check_l(to_f64(lse).reshape(-1), l_ref.reshape(-1), _abs_dot_rows(deq[0], kx, scale, causal, rows))
+
+
+def test_fp8_forward_d64_gpt2_medium_shape_sampled_rows(fa):
+    # the GPT-2-medium attention shape (B 64, H 16, N 1024, d 64), sampled rows against the oracle
+    b, h, n, d = 64, 16, 1024, 64
+    host, dev = _fp8_case(b, h, n, 321, spread=False, d=d)
+    o, lse = fa.attention_forward_fp8(*dev[:3], *dev[3:], causal=False)
+    fa.fa_check_device_error()
+    rng = np.random.default_rng(6)
+    samples = np.stack([rng.integers(0, b, 48), rng.integers(0, h, 48), rng.integers(0, n, 48)], axis=1)
+    samples = np.concatenate([samples, [[0, 0, 0], [b - 1, h - 1, n - 1], [3, 4, 128], [5, 9, 127]]])
+    deq = [F8.dequantize_blocks(host[2 * i], host[2 * i + 1]) for i in range(3)]
+    o_ref, l_ref = oracle.attn_fwd64_rows(*deq, d ** -0.5, False, samples)
+    go, gl = to_f64(o), to_f64(lse)
+    got_o = np.stack([go[bb, hh, ii] for bb, hh, ii in samples])
+    got_l = np.array([gl[bb, hh, ii] for bb, hh, ii in samples])
+    _check_o(got_o, o_ref, np.abs(deq[2]).max())
+    _check_l(got_l, l_ref, _abs_dot_rows(deq[0], deq[1], d ** -0.5, False, samples))
