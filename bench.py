@@ -606,7 +606,7 @@ def run_gpu(args, w: Workload):
                 tf = attention_flops(ow.B, ow.H, ow.N, ow.d, ow.causal, pname) / (ms * 1e-3) / 1e12
                 entry[pname] = {"ms": ms, "tflops": tf, "pct_of_burst_peak": 100 * tf / peak_burst,
                                 "pct_of_sustained_peak": 100 * tf / peak_sus}
-            if ow.d in (64, 128) and ow.dtype != "fp32":
+            if ow.d in (64, 128, 256) and ow.dtype != "fp32":
                 # FP8 forward on block-quantised copies of the same inputs (quantised once, untimed)
                 (q8, qs), (k8, ks), (v8, vs) = (binding.quantize_fp8(od[n_]) for n_ in ("q", "k", "v"))
 

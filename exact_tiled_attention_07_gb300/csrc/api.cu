@@ -501,7 +501,7 @@ fa_status fa_fwd_fp8_gqa(const void* Q8, const void* K8, const void* V8, const f
   fa_status st = check_common(B, H, N, d, out_dtype, &empty);
   if (st != FA_OK || empty) return st;
   if ((st = check_heads(H, Hkv)) != FA_OK) return st;
-  if (!fwd_fp8_supported(d)) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8 supports d in {64, 128}, got %d", d);
+  if (!fwd_fp8_supported(d)) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8 supports d in {64, 128, 256}, got %d", d);
   if ((st = check_ptrs({Q8, K8, V8, q_scales, k_scales, v_scales, O, L}, "fa_fwd_fp8")) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   DeviceSyms syms;

@@ -57,31 +57,44 @@ constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+// F8: the FP8 variant (E4M3 codes of Q, K, V with one scale per 128-row block, kind::f8f6f4
+// MMAs).  Everything is laid out by bytes: a tile row is D * EB bytes, held in 128-byte column
+// blocks with the 128-byte swizzle (64-byte rows, FP8 at d = 64, with the 64-byte swizzle), and
+// an MMA k-step reads 32 bytes of a row (16 16-bit or 32 8-bit elements).
+template <int D, bool F8 = false>
 struct FwdCfg {
+  static constexpr int EB = F8 ? 1 : 2;               // bytes per element of Q, K, V
+  static constexpr int ROW = D * EB;                  // bytes per tile row
+  static constexpr int SW = ROW < 128 ? ROW : 128;    // swizzle width (bytes)
+  static constexpr int KB = ROW / SW;                 // column blocks per row
+  static constexpr int BLK_COLS = SW / EB;            // elements per column block
   static constexpr int NQ = (D == 256) ? 1 : 2;
-  static constexpr int KB = D / 64;                 // 64-column (128-byte) blocks per row
-  static constexpr int Q_BYTES = BM * D * 2;
-  static constexpr int TILE_BYTES = BN * D * 2;
-  // ring entries: a whole K or V tile at d = 64, 128; at d = 256 one 64-column block of a tile
-  // (16 KB), so that the blocks of K are released one by one as their MMAs finish.  The d = 256
-  // ring holds two tiles (8 entries; 10 entries, with the tiles that wrap round the end split into
-  // N = 128 halves, ran 4-7 % slower)
+  static constexpr int Q_BYTES = BM * ROW;
+  static constexpr int TILE_BYTES = BN * ROW;
+  // ring entries: a whole K or V tile at d = 64, 128; at d = 256 one 128-byte column block of a
+  // tile (16 KB), so that the blocks of K are released one by one as their MMAs finish.  The
+  // 16-bit d = 256 ring holds two tiles (8 entries; 10 entries, with the tiles that wrap round
+  // the end split into N = 128 halves, ran 4-7 % slower)
   static constexpr int RB = (D == 256) ? KB : 1;  // ring entries per tile
   static constexpr int ENTRY_BYTES = TILE_BYTES / RB;
-  static constexpr int STAGES = (D == 64) ? 8 : (D == 128 ? 4 : 8);
+  static constexpr int STAGES = F8 ? (D == 64 ? 16 : 8) : ((D == 64) ? 8 : (D == 128 ? 4 : 8));
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
   static constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
   static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  // an MMA k-step: 32 bytes of a row; P V: the keys of one k-step of packed P (8 TMEM columns)
+  static constexpr int QK_STEPS = ROW / 32;
+  static constexpr int PV_KEYS = 32 / EB;
+  static constexpr int P_COLS = BN / (4 / EB);  // TMEM columns of a packed P row (64 or 32)
   // TMEM columns
   static constexpr int S_COL0 = 0, S_COL1 = 128;
-  // d = 64: P gets columns of its own (S, O and P of both query tiles fill the 512), so the
-  // next S = Q K^T may overwrite S as soon as the softmax has read it, before P V has run
-  static constexpr bool SEP_P = (D == 64);
-  static constexpr int P_COL0 = 384, P_COL1 = 448;
   static constexpr int O_COL0 = 256;
   static constexpr int O_COL1 = (NQ == 2) ? 256 + D : 256;
+  // d = 64: P gets columns of its own (S, O and P of both query tiles fit in the 512), so the
+  // next S = Q K^T may overwrite S as soon as the softmax has read it, before P V has run
+  static constexpr bool SEP_P = (D == 64);
+  static constexpr int P_COL0 = 256 + 2 * D, P_COL1 = 256 + 2 * D + P_COLS;
+  static_assert(!SEP_P || P_COL1 + P_COLS <= 512, "TMEM columns");
   // shared memory
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = NQ * Q_BYTES;
@@ -126,14 +139,30 @@ struct FwdSmemBars {
 // score in it) with a flag per query tile; the producer, the MMA warp and the softmax walk
 // that list.  A query tile processes every listed tile up to its own last visible one, the
 // ones it cannot see fully masked, so both tiles keep the same ping-pong schedule.
-template <int D, bool BF16, bool MASKED, bool QUEUE>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+// FP8 variant (F8): Q, K, V are E4M3 codes with one fp32 scale per 128-row block of each head
+// ("Lecture 8" §8.1, "FlashAttention and GPU memory" §11); the scales enter the softmax as
+//   S_ij = tau sq(i) sk(j) (Q8 K8^T)_ij      (one score factor per pair of tiles),
+//   O_i  = sum_j P_ij sv(j) V8_j / l_i,
+// with sv(j) folded into P before it is rounded to E4M3: P8 = E4M3(exp2(S st + log2 sv(j) - m)),
+// where the running maximum m is taken over S st + log2 sv(j) itself, so P8 <= 2^8 (the
+// lazy-rescale bound) and a row's largest weighted probabilities stay near 1, whatever the
+// spread of the V scales.  l sums exp2(S st - m) (each tile's sum of P8's unrounded values
+// divided by sv(j)), so O = (sum P8 V8) / l and L = (m + log2 l) ln 2 as in the 16-bit kernel.
+struct F8Scales {
+  const float* q = nullptr;  // [bh][nb]
+  const float* k = nullptr;  // [bh / group][nb]
+  const float* v = nullptr;  // [bh / group][nb]
+};
+
+template <int D, bool BF16, bool MASKED, bool QUEUE, bool F8 = false>
+__global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, void* __restrict__ out, float* __restrict__ lse, int n,
                   int bh_count, int tiles_per_head, float scale_log2, int causal, int group, unsigned long long* err,
                   unsigned long long* counter, int window, const uint8_t* __restrict__ block_mask, int mask_heads,
-                  int heads, int snake, unsigned* __restrict__ sched, int hgroup) {
-  using C = FwdCfg<D>;
+                  int heads, int snake, unsigned* __restrict__ sched, int hgroup, F8Scales f8s) {
+  using C = FwdCfg<D, F8>;
+  static_assert(!(F8 && MASKED), "the FP8 variant has no masks");
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -377,7 +406,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(B.q_full, C::NQ * C::Q_BYTES);
         for (int q = 0; q < C::NQ; ++q)
           for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(smem + C::OFF_Q + q * C::Q_BYTES + kb * (BM * 128), &tm_q, B.q_full, kb * 64,
+            tma_load_3d(smem + C::OFF_Q + q * C::Q_BYTES + kb * (BM * C::SW), &tm_q, B.q_full, kb * C::BLK_COLS,
                         w.qrow0 + q * BM, w.head);
         ++q_loads;
         for (int idx = 0; ok && idx < 2 * nmax; ++idx) {
@@ -392,9 +421,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (use > 0 && !(ok = mbar_wait(B.kv_empty + slot, (use - 1) & 1, ctx, 10))) break;
             mbar_arrive_expect_tx(B.kv_full + slot, C::ENTRY_BYTES);
             uint8_t* dst = smem + C::OFF_RING + slot * C::ENTRY_BYTES;
-            constexpr int kbs = C::KB / C::RB;  // 64-column blocks per entry
+            constexpr int kbs = C::KB / C::RB;  // column blocks per entry
             for (int kb = 0; kb < kbs; ++kb)
-              tma_load_3d(dst + kb * (BN * 128), tm, B.kv_full + slot, (e * kbs + kb) * 64, tile_at(j) * BN,
+              tma_load_3d(dst + kb * (BN * C::SW), tm, B.kv_full + slot, (e * kbs + kb) * C::BLK_COLS, tile_at(j) * BN,
                           w.kvhead);
             ++ring_pos;
           }
@@ -415,8 +444,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // issues every MMA and commit (a commit tracks the MMAs of its own lane).
     if (start_ok) {
       const bool leader = elect_one_sync();
-      const uint32_t idesc_qk = make_idesc_f16(BM, BN, BF16, false, false);
-      const uint32_t idesc_pv = make_idesc_f16(BM, D, BF16, false, true);
+      // (FP8: E4M3 is format code 0 in the A and B fields of kind::f8f6f4, the layout of kind::f16)
+      const uint32_t idesc_qk = make_idesc_f16(BM, BN, BF16 && !F8, false, false);
+      const uint32_t idesc_pv = make_idesc_f16(BM, D, BF16 && !F8, false, true);
       const uint32_t q_base = smem_u32(smem + C::OFF_Q);
       const uint32_t ring = smem_u32(smem + C::OFF_RING);
       uint32_t ring_pos = 0;    // ring entry of the item's first tile (all items so far)
@@ -440,22 +470,35 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (leader) umma_commit(b);
         __syncwarp();
       };
+      // shared-memory descriptors of the tile layout (128- or 64-byte swizzle) and the MMA kind
+      auto sdesc = [](uint32_t addr, uint32_t lbo, uint32_t sbo) {
+        if constexpr (C::SW == 128) return make_sdesc_sw128(addr, lbo, sbo);
+        else return make_sdesc_sw64(addr, lbo, sbo);
+      };
+      auto mma_ss = [](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (F8) umma_ss_f8(d, a, b, id, acc);
+        else umma_ss(d, a, b, id, acc);
+      };
+      auto mma_ts = [](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (F8) umma_ts_f8(d, a, b, id, acc);
+        else umma_ts(d, a, b, id, acc);
+      };
       // S = Q_q K^T into TMEM columns s_col.  With block entries (d = 256) each 64-column block
       // of K is released as soon as its four MMAs are done.
       auto issue_qk = [&](int q, int kidx, uint32_t s_col) {
         const uint32_t qt = q_base + q * C::Q_BYTES;
         if constexpr (C::RB == 1) {
           const uint32_t kt = ring + slot_of(kidx) * C::ENTRY_BYTES;
-          uint64_t ad[D / 16], bd[D / 16];
+          uint64_t ad[C::QK_STEPS], bd[C::QK_STEPS];
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int k0 = kk * 16;
-            ad[kk] = make_sdesc_sw128(qt + (k0 / 64) * (BM * 128) + (k0 % 64) * 2, 16, 1024);
-            bd[kk] = make_sdesc_sw128(kt + (k0 / 64) * (BN * 128) + (k0 % 64) * 2, 16, 1024);
+          for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+            const int b0 = kk * 32;  // byte offset of the k-step in the row
+            ad[kk] = sdesc(qt + (b0 / C::SW) * (BM * C::SW) + (b0 % C::SW), 16, 8 * C::SW);
+            bd[kk] = sdesc(kt + (b0 / C::SW) * (BN * C::SW) + (b0 % C::SW), 16, 8 * C::SW);
           }
           if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + s_col, ad[kk], bd[kk], idesc_qk, kk > 0);
+            for (int kk = 0; kk < C::QK_STEPS; ++kk) mma_ss(tbase + s_col, ad[kk], bd[kk], idesc_qk, kk > 0);
           }
           __syncwarp();
         } else {
@@ -471,7 +514,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             if (leader) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) umma_ss(tbase + s_col, ad[i], bd[i], idesc_qk, (e > 0 || i > 0) ? 1u : 0u);
+              for (int i = 0; i < 4; ++i) mma_ss(tbase + s_col, ad[i], bd[i], idesc_qk, (e > 0 || i > 0) ? 1u : 0u);
               umma_commit(B.kv_empty + slot);
             }
             __syncwarp();
@@ -485,25 +528,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       auto issue_pv = [&](uint32_t o_col, uint32_t p_col, int vidx, bool acc) {
         if constexpr (C::RB == 1) {
           const uint32_t vt = ring + slot_of(vidx) * C::ENTRY_BYTES;
-          uint64_t bd[BN / 16];
+          uint64_t bd[BN / C::PV_KEYS];
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) bd[kk] = make_sdesc_sw128(vt + kk * 2048, BN * 128, 1024);
+          for (int kk = 0; kk < BN / C::PV_KEYS; ++kk) bd[kk] = sdesc(vt + kk * C::PV_KEYS * C::SW, BN * C::SW, 8 * C::SW);
           if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              umma_ts(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BN / C::PV_KEYS; ++kk)
+              mma_ts(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
           }
           __syncwarp();
         } else {
           static_assert(C::STAGES % C::RB == 0, "a tile's blocks never wrap round the ring");
           const uint32_t vt = ring + slot_of(vidx, 0) * C::ENTRY_BYTES;
-          uint64_t bd[BN / 16];
+          uint64_t bd[BN / C::PV_KEYS];
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) bd[kk] = make_sdesc_sw128(vt + kk * 2048, C::ENTRY_BYTES, 1024);
+          for (int kk = 0; kk < BN / C::PV_KEYS; ++kk) bd[kk] = sdesc(vt + kk * C::PV_KEYS * C::SW, C::ENTRY_BYTES, 8 * C::SW);
           if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              umma_ts(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BN / C::PV_KEYS; ++kk)
+              mma_ts(tbase + o_col, tbase + p_col + kk * 8, bd[kk], idesc_pv, (acc || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int e = 0; e < C::RB; ++e) umma_commit(B.kv_empty + slot_of(vidx, e));
           }
@@ -664,8 +707,31 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       const int nb = w.nq[q];
       float m = -INFINITY;  // reference maximum, log2 units (scores * tau * log2 e)
       float l = 0.f;
+      // FP8: the query block's scale, and the key and value scales of the next key tile
+      const int nblk_s = (n + BN - 1) / BN;
+      float sq_log2 = scale_log2, sk_next = 1.f, sv_next = 1.f;
+      if constexpr (F8) {
+        const int qblk = min((w.qrow0 + q * BM) / BM, nblk_s - 1);
+        sq_log2 = scale_log2 * f8s.q[(int64_t)head * nblk_s + qblk];
+        if (nb > 0) {
+          sk_next = f8s.k[(int64_t)w.kvhead * nblk_s];
+          sv_next = f8s.v[(int64_t)w.kvhead * nblk_s];
+        }
+      }
       for (int j = 0; ok && j < nb; ++j) {
         const int t = tq + j;
+        // score scale (log2 units per unit of S) and, FP8, log2 of the key tile's V scale,
+        // which rides in P's exponent
+        float st = scale_log2, pv = 1.f, lpv = 0.f;
+        if constexpr (F8) {
+          st = sq_log2 * sk_next;
+          pv = sv_next;
+          lpv = __log2f(pv);
+          if (j + 1 < nb) {
+            sk_next = f8s.k[(int64_t)w.kvhead * nblk_s + j + 1];
+            sv_next = f8s.v[(int64_t)w.kvhead * nblk_s + j + 1];
+          }
+        }
         uint32_t s_col;
         uint64_t* sbar;
         uint32_t sparity;
@@ -715,7 +781,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             if (c < lo || c >= hi) s[c] = -INFINITY;
         }
         const float mx = row_max3(s);
-        const float m_blk = mx * scale_log2;
+        const float m_blk = F8 ? mx * st + lpv : mx * st;
         float alpha = 1.f;
         bool rescale = false;
         if (m == -INFINITY) {
@@ -726,7 +792,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           m = m_blk;
           rescale = true;
         }
-        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        const float neg_m = F8 ? ((m == -INFINITY) ? 0.f : -m) + lpv : ((m == -INFINITY) ? 0.f : -m);
         if constexpr (C::SEP_P) {
           // P_q and O_q are free once the previous tile's P V is done
           if (t > 0) {
@@ -738,19 +804,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const uint32_t p_col = C::SEP_P ? (q ? C::P_COL1 : C::P_COL0) : s_col;
         // two partial sums of pairs (paired fp32 adds): no single long add chain
         float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        if constexpr (!F8) {
 #pragma unroll
-        for (int h = 0; h < BN / 32; ++h) {
-          uint32_t pk[16];
+          for (int h = 0; h < BN / 32; ++h) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x = ffma2(make_float2(s[h * 32 + 2 * i], s[h * 32 + 2 * i + 1]), scale_log2, neg_m);
-            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-            part[i & 1] = fadd2(part[i & 1], pp);
-            pk[i] = pack2<BF16>(pp.x, pp.y);
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = ffma2(make_float2(s[h * 32 + 2 * i], s[h * 32 + 2 * i + 1]), st, neg_m);
+              const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+              part[i & 1] = fadd2(part[i & 1], pp);
+              pk[i] = pack2<BF16>(pp.x, pp.y);
+            }
+            tmem_st16(tmem_addr(tbase, lane_base, p_col + h * 16), pk);
           }
-          tmem_st16(tmem_addr(tbase, lane_base, p_col + h * 16), pk);
+        } else {
+          // E4M3, four to a TMEM column
+#pragma unroll
+          for (int h = 0; h < BN / 64; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float* sv4 = &s[h * 64 + 4 * i];
+              const float2 x01 = ffma2(make_float2(sv4[0], sv4[1]), st, neg_m);
+              const float2 x23 = ffma2(make_float2(sv4[2], sv4[3]), st, neg_m);
+              const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y)), p23 = make_float2(ex2(x23.x), ex2(x23.y));
+              part[i & 1] = fadd2(part[i & 1], fadd2(p01, p23));
+              pk[i] = pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
+            }
+            tmem_st16(tmem_addr(tbase, lane_base, p_col + h * 16), pk);
+          }
         }
-        const float sum = (part[0].x + part[1].x) + (part[0].y + part[1].y);
+        // (FP8: the values carry sv; dividing their sum by it gives the sum of exp2(S st - m))
+        const float sum = F8 ? ((part[0].x + part[1].x) + (part[0].y + part[1].y)) / pv
+                             : (part[0].x + part[1].x) + (part[0].y + part[1].y);
         l = l * alpha + sum;
         if (__any_sync(0xffffffffu, rescale)) {
           // O row *= alpha; O is stable: the PV of block j-1 completed before S_j (NQ = 2 without
@@ -915,14 +1001,21 @@ int64_t max_cta_tiles(int bh, int tiles_per_head, int n, int nq_tiles, int g, bo
   return *std::max_element(load.begin(), load.end());
 }
 
-template <int D, bool BF16, bool MASKED>
-cudaError_t launch_fwd_d(const FwdArgs& a) {
-  using C = FwdCfg<D>;
+// Launch of the persistent forward (16-bit, or FP8 when f8 carries the block scales; then
+// Q, K, V of `a` are E4M3 codes and BF16 is O's type).
+template <int D, bool BF16, bool MASKED, bool F8 = false>
+cudaError_t launch_fwd_d(const FwdArgs& a, F8Scales f8 = F8Scales()) {
+  using C = FwdCfg<D, F8>;
   CUtensorMap tq, tk, tv, to;
   const int bh_kv = a.bh / a.group;
-  if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) ||
-      !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN) || !make_tmap_16bit_3d(&to, a.o, BF16, D, a.n, a.bh, BM))
-    return cudaErrorInvalidValue;
+  bool maps;
+  if constexpr (F8)
+    maps = make_tmap_8bit_3d(&tq, a.q, D, a.n, a.bh, BM, C::SW) && make_tmap_8bit_3d(&tk, a.k, D, a.n, bh_kv, BN, C::SW) &&
+           make_tmap_8bit_3d(&tv, a.v, D, a.n, bh_kv, BN, C::SW);
+  else
+    maps = make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, BM) && make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) &&
+           make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN);
+  if (!maps || !make_tmap_16bit_3d(&to, a.o, BF16, D, a.n, a.bh, BM)) return cudaErrorInvalidValue;
   const int nblocks = (a.n + BN - 1) / BN;
   const int smem = MASKED ? C::SMEM + C::list_bytes(nblocks) : C::SMEM_STG;
   if (smem > 232448) return cudaErrorInvalidValue;  // key-tile list too long for shared memory
@@ -933,7 +1026,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
   const int64_t items = (int64_t)a.bh * tiles;
   const int64_t grid = MASKED ? items : std::min<int64_t>(items, device_sm_count());
   // causal order: groups of query heads whose K, V (shared by `group` query heads) stay in L2
-  const int hgroup = head_group_for_l2((int64_t)2 * a.n * D * 2 / a.group);
+  const int hgroup = head_group_for_l2((int64_t)2 * a.n * C::ROW / a.group);
   const int snake = (!MASKED && a.causal && grid < items &&
                      max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, true, hgroup) <
                          max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, false, hgroup))
@@ -943,15 +1036,15 @@ cudaError_t launch_fwd_d(const FwdArgs& a) {
   // items, whatever the cause), else the static order
   QueueSlot qs;
   if (!MASKED && grid < items) qs = queue_slot_take(a.stream);
-  auto kern = fwd_tc_kernel<D, BF16, MASKED, false>;
+  auto kern = fwd_tc_kernel<D, BF16, MASKED, false, F8>;
   if constexpr (!MASKED) {
-    if (qs.slot >= 0) kern = fwd_tc_kernel<D, BF16, false, true>;
+    if (qs.slot >= 0) kern = fwd_tc_kernel<D, BF16, false, true, F8>;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess) {
     kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, to, a.o, a.lse, a.n, a.bh, tiles, scale_log2,
                                                          a.causal, a.group, a.err, a.counter, a.window, a.block_mask,
-                                                         a.mask_heads, a.heads, snake, qs.counters, hgroup);
+                                                         a.mask_heads, a.heads, snake, qs.counters, hgroup, f8);
     e = cudaGetLastError();
   }
   return queue_slot_done(qs, e, a.stream);
@@ -1077,6 +1170,25 @@ bool fwd_masked_fits(int n, int d) {
   if (nb > 65535) return false;
   const int base = d == 64 ? FwdCfg<64>::SMEM : (d == 128 ? FwdCfg<128>::SMEM : FwdCfg<256>::SMEM);
   return base + FwdCfg<64>::list_bytes(nb) <= 232448;
+}
+
+bool fwd_fp8_supported(int d) { return d == 64 || d == 128 || d == 256; }
+
+cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a) {
+  FwdArgs f{a.q8, a.k8, a.v8, a.o, a.lse, a.bh, a.n, a.d, a.scale, a.causal, a.out_dtype, a.err, a.counter, a.stream};
+  f.group = a.group;
+  f.heads = a.bh;
+  F8Scales sc;
+  sc.q = a.q_scales;
+  sc.k = a.k_scales;
+  sc.v = a.v_scales;
+  const bool bf = a.out_dtype == DT_BF16;
+  switch (a.d) {
+    case 64: return bf ? launch_fwd_d<64, true, false, true>(f, sc) : launch_fwd_d<64, false, false, true>(f, sc);
+    case 128: return bf ? launch_fwd_d<128, true, false, true>(f, sc) : launch_fwd_d<128, false, false, true>(f, sc);
+    case 256: return bf ? launch_fwd_d<256, true, false, true>(f, sc) : launch_fwd_d<256, false, false, true>(f, sc);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 bool fwd_tc_supported(int dtype, int d) {

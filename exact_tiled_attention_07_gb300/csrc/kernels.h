@@ -91,7 +91,10 @@ struct DecodeArgs {
 // `bytes_per_head` (what a head's items stream: K and V in the forward; Q, dO, the dQ
 // accumulator, L and D in the backward) within an L2 budget of kL2HeadBudget bytes, at
 // least 1 and at most kMaxHeadGroup.
-constexpr int64_t kL2HeadBudget = 80ll << 20;
+#ifndef FA_L2_HEAD_BUDGET_MB
+#define FA_L2_HEAD_BUDGET_MB 80
+#endif
+constexpr int64_t kL2HeadBudget = (int64_t)FA_L2_HEAD_BUDGET_MB << 20;
 inline int head_group_for_l2(int64_t bytes_per_head) {
   const int64_t g = bytes_per_head > 0 ? kL2HeadBudget / bytes_per_head : 16;
   return (int)(g < 1 ? 1 : (g > 16 ? 16 : g));  // 16: kMaxHeadGroup
@@ -157,7 +160,7 @@ struct Fp8FwdArgs {
   int group = 1;
 };
 bool fwd_fp8_supported(int d);
-cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a);
+cudaError_t launch_fwd_fp8(const Fp8FwdArgs& a);  // fwd_tc.cu: the 16-bit forward with 8-bit operands
 
 // One CTA waits (bounded by timeout_ms) on an mbarrier phase nothing completes, or that it
 // completes itself when arrive != 0.

@@ -263,7 +263,7 @@ FA_API fa_status fa_quantize_fp8(const void* X, void* X8, float* scales, int B, 
  *   q/k/v_scales         in:  [B][H][ceil(N / 128)] fp32 block scales
  *   O                    out: [B][H][N][d] out_dtype (FA_BF16 or FA_FP16)
  *   L                    out: [B][H][N] fp32, natural-log log-sum-exp of the scaled scores
- *   d                    64 or 128 (other head dims return FA_ERR_UNSUPPORTED)
+ *   d                    64, 128 or 256 (other head dims return FA_ERR_UNSUPPORTED)
  * Computes attention of the dequantised tensors (code x block scale): S = scale Q K^T (causal
  * mask when causal != 0), O = softmax(S) V, L = m + ln l. The probabilities are rounded to
  * E4M3 before the P V product, after multiplying by the key block's V scale; the online

@@ -3,7 +3,7 @@
 The debug library (``build.build(debug=True)``) is loaded in place of the release one for this
 module and the release one is put back afterwards.  Small problems of every tensor-core path
 (forward and backward at d = 64 and 128, grouped-query heads, a sliding window, the d = 256
-forward, FP8) must run through it with no device error and match the fp64 oracle, so the checks
+forward, FP8 at d = 64, 128 and 256) must run through it with no device error and match the fp64 oracle, so the checks
 raise no false alarm; the self-test launches one check with an index out of range, which must
 come back as a device error while the context stays usable.
 """
@@ -93,14 +93,15 @@ def test_debug_build_grouped_query_window_and_d256(fa):
     _check_fwd(w, x, o, lse, *oracle.attn_fwd64(x64["q"], x64["k"], x64["v"], w.scale, False))
 
 
-def test_debug_build_fp8_forward(fa):
-    rng = np.random.default_rng(7400)
-    q, k, v = (rng.standard_normal((1, 2, 300, 128)).astype(np.float32) for _ in range(3))
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True), (256, False)])
+def test_debug_build_fp8_forward(fa, d, causal):
+    rng = np.random.default_rng(7400 + d)
+    q, k, v = (rng.standard_normal((1, 2, 300, d)).astype(np.float32) for _ in range(3))
     host = [a for t in (q, k, v) for a in F8.quantize_blocks(t)]
     x8 = [fa.quantize_fp8(torch.from_numpy(t).cuda()) for t in (q, k, v)]
-    o, lse = fa.attention_forward_fp8(*(c for c, _ in x8), *(s for _, s in x8), causal=True)
+    o, lse = fa.attention_forward_fp8(*(c for c, _ in x8), *(s for _, s in x8), causal=causal)
     fa.fa_check_device_error()
-    o_ref, l_ref = F8.attn_fwd64_fp8(*host, 128 ** -0.5, True)
+    o_ref, l_ref = F8.attn_fwd64_fp8(*host, d ** -0.5, causal)
     assert rel_rms(to_f64(o), o_ref) <= 0.05
 
 

@@ -130,7 +130,7 @@ def _check_o(go, o_ref, vmax):
     assert max_abs(go, o_ref) <= TOL_FP8_O_MAXABS_OF_VMAX * vmax + 1e-3
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n", [128, 129, 300, 1000])
 @pytest.mark.parametrize("out", ["bf16", "fp16"])
@@ -161,7 +161,7 @@ def _exact_values(shape, seed):
     return codes * np.float32(2.0 ** -8)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_forward_exact_sums_meet_the_plain_l_tolerance(fa, causal, d):
     """Inputs whose products and sums are exact in 13 significant bits: S has no rounding beyond
@@ -219,7 +219,7 @@ def test_fp8_forward_full_size_sampled_rows(fa):
 
 
 def test_fp8_argument_checks(fa):
-    for d in (32, 256):
+    for d in (32, 96):
         z = torch.zeros((1, 1, 128, d), dtype=torch.uint8, device="cuda")
         s = torch.ones(1, dtype=torch.float32, device="cuda")
         with pytest.raises(fa.FAError, match="d in"):
@@ -264,3 +264,32 @@ def test_fp8_forward_d64_gpt2_medium_shape_sampled_rows(fa):
     got_l = np.array([gl[bb, hh, ii] for bb, hh, ii in samples])
     _check_o(got_o, o_ref, np.abs(deq[2]).max())
     _check_l(got_l, l_ref, _abs_dot_rows(deq[0], deq[1], d ** -0.5, False, samples))
+
+
+def test_fp8_forward_d256_head_dim_256_shape_sampled_rows(fa):
+    """The large-head-dimension shape (B 4, H 16, N 16384, d 256, non-causal), sampled rows.  The
+    device quantises the whole problem (its codes are checked bit for bit against the oracle's
+    quantiser above); the oracle quantises, from the same fp32 values, only the heads it samples."""
+    b, h, n, d = 4, 16, 16384, 256
+    x = [_draw((b, h, n, d), 654 + i, spread=False) for i in range(3)]
+    x8 = [fa.quantize_fp8(torch.from_numpy(t).cuda()) for t in x]
+    o, lse = fa.attention_forward_fp8(*(c for c, _ in x8), *(s for _, s in x8), causal=False)
+    fa.fa_check_device_error()
+    del x8
+    rng = np.random.default_rng(7)
+    samples = np.stack([rng.integers(0, b, 40), rng.integers(0, h, 40), rng.integers(0, n, 40)], axis=1)
+    samples = np.concatenate([samples, [[0, 0, 0], [b - 1, h - 1, n - 1], [2, 3, 128], [1, 7, 127]]])
+    go, gl = to_f64(o), to_f64(lse)
+    got_o = np.stack([go[bb, hh, ii] for bb, hh, ii in samples])
+    got_l = np.array([gl[bb, hh, ii] for bb, hh, ii in samples])
+    o_ref, l_ref = np.zeros_like(got_o), np.zeros_like(got_l)
+    absdot, vmax = np.zeros_like(got_l), 0.0
+    for bb, hh in sorted({(int(p), int(q)) for p, q, _ in samples}):
+        idx = np.nonzero((samples[:, 0] == bb) & (samples[:, 1] == hh))[0]
+        rows = np.stack([np.zeros_like(idx), np.zeros_like(idx), samples[idx, 2]], axis=1)
+        deq = [F8.dequantize_blocks(*F8.quantize_blocks(t[bb, hh][None, None])) for t in x]
+        o_ref[idx], l_ref[idx] = oracle.attn_fwd64_rows(*deq, d ** -0.5, False, rows)
+        absdot[idx] = _abs_dot_rows(deq[0], deq[1], d ** -0.5, False, rows)
+        vmax = max(vmax, float(np.abs(deq[2]).max()))
+    _check_o(got_o, o_ref, vmax)
+    _check_l(got_l, l_ref, absdot)
