@@ -19,14 +19,16 @@
 // the shared-memory read of A that an all-smem MMA pays; dS^T also goes to shared memory
 // as an operand of the dQ GEMM.
 //
-// Two warpgroups share the elementwise work: both own the tile's 128 key rows (a warp reads
-// the TMEM lanes of its quarter, so warps w and w + 4 see the same rows) and each takes half of
-// every step's queries for P^T and dS^T.  dQ partials are summed over key tiles in an fp32
-// accumulator in global memory: after its dS^T half, each warpgroup drains its half of the
-// previous step's dQ partial from TMEM into a shared-memory staging tile, and one thread adds
-// the tile to global memory with a TMA bulk reduction (whole 128-byte lines, no per-element
-// atomics).  Two shapes of the dQ GEMM keep every TMEM region separate, so no
-// GEMM waits for another region to be drained:
+// Roles: two compute warpgroups for the elementwise work (P^T, dS^T), one drain warpgroup, a
+// TMA producer warp and an MMA warp.  Both compute warpgroups own the tile's 128 key rows (a
+// warp reads the TMEM lanes of its quarter, so warps w and w + 4 see the same rows) and each
+// takes half of every step's queries.  dQ
+// partials are summed over key tiles in an fp32 accumulator in global memory: the drain
+// warpgroup moves each step's dQ partial from TMEM into a shared-memory staging tile as soon as
+// it completes, and one thread adds the tile to global memory with a TMA bulk reduction (whole
+// 128-byte lines, no per-element atomics); at the end of an item it also stores dK, dV.  Two
+// shapes of the dQ GEMM keep every TMEM region separate, so no GEMM waits for another region to
+// be drained:
 //   d = 64:  128 queries per step, dQ = dS K   (M = 128 queries, N = 64)
 //   d = 128:  64 queries per step, dQ^T = K^T dS^T (M = 128 = d, N = 64 queries)
 //
@@ -59,9 +61,14 @@ struct BwdCfg {
   static constexpr int QT_BYTES = BM * D * 2;
   static constexpr int DS_BYTES = BN * BM * 2;
   static constexpr int STG_BYTES = BM * D * 4;
-  static constexpr int THREADS = 320;            // WG0, WG1 (P/dS, dQ drain), TMA warp, MMA warp
-  static constexpr int PRODUCER_WARP = 8;
-  static constexpr int MMA_WARP = 9;
+  // WG0 and WG1 compute (half the queries of a step each), WG2 drains; then the TMA producer
+  // warp and the MMA warp.
+  static constexpr int COMPUTE_WGS = 2;
+  static constexpr int DRAIN_WARP0 = 4 * COMPUTE_WGS;  // first warp of the drain warpgroup
+  static constexpr int PRODUCER_WARP = DRAIN_WARP0 + 4;
+  static constexpr int MMA_WARP = PRODUCER_WARP + 1;
+  static constexpr int THREADS = 32 * (MMA_WARP + 1);
+  static constexpr uint32_t ITEM_READERS = 1 + 4 * COMPUTE_WGS + 4;  // MMA, compute and drain warps
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
   static constexpr int QSTAGES = 3;                          // query-tile ring depth
@@ -71,7 +78,7 @@ struct BwdCfg {
   static constexpr int OFF_STG = OFF_DS + DS_BYTES;              // dQ staging tile
   static constexpr int OFF_VEC = OFF_STG + STG_BYTES;            // [QSTAGES] x (L2[BM], D[BM]) fp32
   static constexpr int OFF_BAR = OFF_VEC + QSTAGES * 2 * BM * 4;
-  static constexpr int NBAR = 24;
+  static constexpr int NBAR = 22;
   // after the barriers: TMEM base, abort flag, the two work-item slots
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 32;
   // masked variant: the CTA's step list after the barriers (an int count, then uint16 entries
@@ -79,18 +86,13 @@ struct BwdCfg {
   static constexpr int OFF_LIST = SMEM;
   static constexpr int list_bytes(int entries) { return 16 + 2 * ((entries + 7) & ~7); }
   static constexpr int SUB = 128 / BM;  // steps per 128-row query block
-  // d = 64 (128 queries per step): both warpgroups compute P^T, dS^T (half the queries each)
-  // and drain half of each dQ partial (half its d columns).  d = 128: warpgroup 0 computes P^T,
-  // dS^T and warpgroup 1 drains whole dQ partials as soon as they complete.  The split also
-  // builds at d = 128 (kSplit128: each warpgroup drains half the query columns of dQ^T and
-  // stores one of dV, dK), but measured 12 % slower there: each warpgroup's drain then sits
-  // between its dS^T half and its next P^T half, on the path to the next step's P^T.
-  static constexpr bool kSplit128 = false;
-  static constexpr bool SPLIT = !DQT || kSplit128;
-  static constexpr int COMPUTE_THREADS = SPLIT ? 256 : 128;
-  static constexpr int DRAIN_THREADS = SPLIT ? 256 : 128;
-  static constexpr int CH_COLS = SPLIT ? 32 : 16;  // TMEM columns between packed 32-query chunks
-  static constexpr int EPI_THREADS = SPLIT ? 256 : 128;  // threads that read dK, dV out of TMEM
+  static constexpr int COMPUTE_THREADS = 128 * COMPUTE_WGS;
+  static constexpr int DRAIN_THREADS = 128;
+  // TMEM columns between packed 32-query chunks of P^T / dS^T: each chunk keeps its packed
+  // values inside its own 32 fp32 columns, so neither compute warpgroup writes over scores the
+  // other has yet to read
+  static constexpr int CH_COLS = 32;
+  static constexpr int EPI_THREADS = 128;  // threads that read dK, dV out of TMEM (the drain warpgroup)
   // the staging tile also carries an item's dV and dK as 16-bit [128 rows][64 columns] boxes with
   // the 128-byte swizzle (d = 128: dV, then dK, two boxes each; d = 64: dV and dK side by side)
   static_assert(STG_BYTES >= 2 * BN * 128 && OFF_STG % 1024 == 0, "staging tile");
@@ -118,19 +120,14 @@ enum BwdBar {
   B_ACC_FULL = 13,
   B_DRAIN = 14,
   B_KT_READY = 15,  // K_j copied into TMEM
-  B_STG_FREE = 16,  // dQ staging tile free (the previous reduction has read it)
-  B_STG_FULL = 17,  // both warpgroups wrote their half of the staging tile
-  B_KV_EMPTY = 18,  // the tensor core no longer reads this item's K_j, V_j (persistent)
-  B_ACC_EMPTY = 19, // this item's dK, dV have left TMEM (persistent)
-  B_ITEM_FULL = 20,   // [2] the producer published the next work item in its slot
-  B_ITEM_EMPTY = 22,  // [2] every consumer warp has read it
+  B_KV_EMPTY = 16,  // the tensor core no longer reads this item's K_j, V_j (persistent)
+  B_ACC_EMPTY = 17, // this item's dK, dV have left TMEM (persistent)
+  B_ITEM_FULL = 18,   // [2] the producer published the next work item in its slot
+  B_ITEM_EMPTY = 20,  // [2] every consumer warp has read it
 };
-constexpr uint32_t kItemReaders = 9;  // the MMA warp and the eight compute warps
 
-// TMEM column of the packed 16-bit A operand (P^T or dS^T) for MMA k-step kk (16 queries),
-// chunk c of 32 queries starting at c * ch_cols: contiguous (16) when one warpgroup reads every
-// score before writing any, or at the start of the chunk's own 32 fp32 columns (32) when two
-// warpgroups share the queries, so neither writes over scores the other has yet to read
+// TMEM column of the packed 16-bit A operand (P^T or dS^T) for MMA k-step kk (16 queries):
+// chunk c of 32 queries starts at c * ch_cols, the start of the chunk's own 32 fp32 columns
 __host__ __device__ constexpr uint32_t packed_col(int kk, int ch_cols) {
   return (uint32_t)((kk >> 1) * ch_cols + (kk & 1) * 8);
 }
@@ -248,8 +245,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar + B_DS_READY, C::COMPUTE_THREADS);
     mbar_init(bar + B_DQ_FULL, 1);
     mbar_init(bar + B_DQ_FREE, C::DRAIN_THREADS);
-    mbar_init(bar + B_STG_FREE, 1);
-    mbar_init(bar + B_STG_FULL, C::DRAIN_THREADS);
     mbar_init(bar + B_ACC_FULL, 1);
     mbar_init(bar + B_DRAIN, 1);
     mbar_init(bar + B_KT_READY, 128);
@@ -257,7 +252,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar + B_ACC_EMPTY, C::EPI_THREADS);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar + B_ITEM_FULL + t, 1);
-      mbar_init(bar + B_ITEM_EMPTY + t, kItemReaders);
+      mbar_init(bar + B_ITEM_EMPTY + t, C::ITEM_READERS);
     }
     fence_barrier_init();
   }
@@ -579,148 +574,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_wait(bar + B_DRAIN, 0, nctx, 125);
     }
     __syncwarp();
-  } else if (!C::SPLIT && warp < 4) {
-    // ---------------------------------------------------------------- WG0: K_j -> TMEM, P^T, dS^T
-    const uint32_t lane_base = warp * 32;
-    const int rit = warp * 32 + lane;  // key row within the tile
-    uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
-    const uint32_t sw = (uint32_t)(rit & 7);
-    bool ok = start_ok;
-    uint32_t gs = 0;  // steps processed (all items)
-    for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
-      const BwdItem w = item_at(item);
-      const int key = w.k0 + rit;
-      const bool key_ok = key < n;
-      // K_j -> TMEM: the previous item's last S^T (which read it) completed before its last step
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + B_KV, r & 1, ctx, 134));
-      if (!ok) break;
-      k_to_tmem(rit, lane_base);
-      tc_fence_before();
-      mbar_arrive(bar + B_KT_READY);
-      for (int i = 0, ii = 0, g = 0; ok && i < w.nsteps; ++i, ++gs, step_next(ii, g, w.nsteps_head)) {
-        const int s = gs % C::QSTAGES;
-        int gm, q0;
-        step_rows(w, i, ii, g, &gm, &q0);
-        const float* l2v = reinterpret_cast<const float*>(smem + C::OFF_VEC) + s * 2 * BM;
-        const float* dvec = l2v + BM;
-        // L_i, D_i arrive with the query tile (TMA); S^T_i from the tensor core
-        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_QD_FULL + s, (gs / C::QSTAGES) & 1, ctx, 133));
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar + B_S_FULL, gs & 1, ctx, 130));
-        if (!ok) break;
-        tc_fence_after();
-        // visible queries q0 + qc: qc in [mask_below, mask_above) (causal: not before this key;
-        // window: |query - key| < window, an upper bound on the query with or without causal)
-        int mask_below = causal ? key - q0 : INT32_MIN, mask_above = INT32_MAX;
-        if constexpr (MASKED) {
-          if (window > 0) {
-            mask_below = max(mask_below, key - window + 1 - q0);
-            mask_above = key + window - q0;
-          }
-        }
-        // the whole warp sees every query of the step: no masking of P
-        const bool all_visible = __all_sync(0xffffffffu, key_ok && mask_below <= 0 && mask_above >= BM);
-        // P^T row (this key against the BM queries), kept as packed 16-bit pairs: the same
-        // rounded values feed dV += P^T dO and dS = P o (dP - D)
-        uint32_t pk[BM / 2];
-#pragma unroll
-        for (int g = 0; g < BM / 64; ++g) {  // 64 columns per batch of TMEM loads
-          uint32_t sr[2][32];
-          tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + g * 64), sr[0]);
-          tmem_ld32(tmem_addr(tbase, lane_base, C::COL_S + g * 64 + 32), sr[1]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int c = g * 2 + cc;
-            uint32_t(&r)[32] = sr[cc];
-            reg_fence(r);
-#pragma unroll
-            for (int t = 0; t < 32; t += 4) {
-              // x = S tau log2 e - L log2 e, two queries per paired FMA (l2v holds -L log2 e)
-              const float4 l4 = *reinterpret_cast<const float4*>(l2v + c * 32 + t);
-              const float2 x01 = ffma2(make_float2(__uint_as_float(r[t]), __uint_as_float(r[t + 1])), scale_log2,
-                                       make_float2(l4.x, l4.y));
-              const float2 x23 = ffma2(make_float2(__uint_as_float(r[t + 2]), __uint_as_float(r[t + 3])), scale_log2,
-                                       make_float2(l4.z, l4.w));
-              float e[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
-              if (!all_visible) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const int qc = c * 32 + t + u;
-                  e[u] = (key_ok && qc >= mask_below && qc < mask_above) ? e[u] : 0.f;
-                }
-              }
-              pk[(c * 32 + t) / 2] = pack2<BF16>(e[0], e[1]);
-              pk[(c * 32 + t) / 2 + 1] = pack2<BF16>(e[2], e[3]);
-            }
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < BM / 64; ++h) {
-          uint32_t wv[32];
-#pragma unroll
-          for (int t = 0; t < 32; ++t) wv[t] = pk[h * 32 + t];
-          tmem_st32(tmem_addr(tbase, lane_base, C::COL_S + h * 32), wv);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar + B_P_READY);
-        // dS^T = P^T o (dP^T - D); dp_full(i) also means the MMAs of step i-1 that read dS^T are done
-        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DP_FULL, gs & 1, ctx, 131));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int g = 0; g < BM / 64; ++g) {  // 64 columns per batch of TMEM loads
-          uint32_t dr[2][32];
-          tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + g * 64), dr[0]);
-          tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DP + g * 64 + 32), dr[1]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int c = g * 2 + cc;
-            uint32_t(&r)[32] = dr[cc];
-            reg_fence(r);
-            uint32_t dsk[16];
-#pragma unroll
-            for (int t = 0; t < 16; t += 2) {
-              // dS = P o (dP - D), two queries per paired subtract and multiply
-              const float4 d4 = *reinterpret_cast<const float4*>(dvec + c * 32 + 2 * t);
-              const float2 ds01 = fmul2(unpack2<BF16>(pk[c * 16 + t]),
-                                        fsub2(make_float2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1])),
-                                              make_float2(d4.x, d4.y)));
-              const float2 ds23 = fmul2(unpack2<BF16>(pk[c * 16 + t + 1]),
-                                        fsub2(make_float2(__uint_as_float(r[2 * t + 2]), __uint_as_float(r[2 * t + 3])),
-                                              make_float2(d4.z, d4.w)));
-              dsk[t] = pack2<BF16>(ds01.x, ds01.y);
-              dsk[t + 1] = pack2<BF16>(ds23.x, ds23.y);
-            }
-            // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
-            uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
-              *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
-                  make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
-            }
-            // and packed into TMEM over dP^T columns already read (A operand of dK += dS^T Q)
-            tmem_st16(tmem_addr(tbase, lane_base, C::COL_DP + c * 16), dsk);
-          }
-        }
-        fence_proxy_async_smem();
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar + B_DS_READY);
-      }
-    }
-
-  } else if (!C::SPLIT && warp < 8) {
-    // ---------------------------------------------------------------- WG1: dQ drain, epilogue
-    // TMEM lane = d index; the dQ partial goes to a staging tile in the layout of the dQ
-    // accumulator's tensor map and one thread adds it to global memory (TMA reduce).  After an
-    // item's last partial, its dV and dK (x tau) go through the same staging tile to global
-    // memory (TMA stores), while warpgroup 0 starts the next item.
+  } else if (warp >= C::DRAIN_WARP0) {
+    // ---------------------------------------------------------------- drain warpgroup: dQ, epilogue
+    // Each dQ partial goes from TMEM to a staging tile in the layout of the dQ accumulator's
+    // tensor map and one thread adds it to global memory (TMA reduce).  After an item's last
+    // partial, its dV and dK (x tau) go through the same staging tile to global memory (TMA
+    // stores), while the compute warpgroups start the next item.
     const uint32_t lane_base = (warp & 3) * 32;
-    const int rr = (warp & 3) * 32 + lane;  // d index of a dQ partial; key row of dK, dV
-    const bool leader = (warp == 4 && lane == 0);
+    // TMEM lane: d index (d = 128) or query row (d = 64) of a dQ partial; key row of dK, dV
+    const int rr = (warp & 3) * 32 + lane;
+    const bool leader = (warp == C::DRAIN_WARP0 && lane == 0);
     uint8_t* stg = smem + C::OFF_STG;
     bool ok = start_ok;
     uint32_t gs = 0;  // dQ partials drained (all items)
@@ -750,14 +613,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mbar_arrive(bar + B_DQ_FREE);
         if (leader) bulk_wait_group_read<0>();  // the previous bulk copy has finished reading the tile
         named_bar_sync(1, 128);
-        // [BM queries][D] fp32, row-major: column rr (this thread's d) of each query row
-        float* st = reinterpret_cast<float*>(stg) + rr;
+        if constexpr (C::DQT) {
+          // [BM queries][D] fp32, row-major: column rr (this thread's d) of each query row
+          float* st = reinterpret_cast<float*>(stg) + rr;
 #pragma unroll
-        for (int q = 0; q < BM; ++q) st[q * D] = __uint_as_float(v[q]);
+          for (int q = 0; q < BM; ++q) st[q * D] = __uint_as_float(v[q]);
+        } else {
+          // [BM queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns: row rr (this
+          // thread's query), 16-byte chunks
+          const uint32_t sw = (uint32_t)(rr & 7);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            uint8_t* bx = stg + (j >> 3) * (BM * 128) + rr * 128;
+            *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ sw) << 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (leader && ok) {
           tma_reduce_add_3d(&tm_dq, stg, 0, q0, w.kvh * group + gm);
+          if constexpr (!C::DQT) tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, w.kvh * group + gm);
           bulk_commit_group();
         }
       }
@@ -811,88 +687,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     if (leader) bulk_wait_group<0>();  // every reduction and store issued here has completed
 
-  } else if (warp < 8) {
-    if constexpr (C::SPLIT) {
-      // ---------------------------------------------------------------- WG0, WG1: P^T, dS^T, dQ drain
-      // (d = 64, 128 queries per step) Both warpgroups own the same 128 key rows (TMEM lane
-      // quarter warp % 4) and each takes half of every step's 32-query chunks for P^T and dS^T;
-      // after its dS^T half of step i each drains its half of the dQ partial of step i - 1 (that
-      // MMA completed before dP^T_i, which the dS^T half has just read).  WG0 also copies K_j
-      // into TMEM at the start of an item; at its end WG0 stores dV and WG1 dK.
-      constexpr bool SPLIT = C::SPLIT;
+  } else {
+    {
+      // ---------------------------------------------------------------- WG0, WG1: P^T, dS^T
+      // Both warpgroups own the same 128 key rows (TMEM lane quarter warp % 4) and each takes
+      // half of every step's 32-query chunks for P^T and dS^T.  WG0 also copies K_j into TMEM
+      // at the start of an item.
       const int wg = warp >> 2;
       const uint32_t lane_base = (warp & 3) * 32;
       const int rit = (warp & 3) * 32 + lane;  // key row within the tile (and TMEM lane)
       uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
       const uint32_t sw = (uint32_t)(rit & 7);
-      constexpr int NCH = SPLIT ? BM / 64 : BM / 32;  // 32-query chunks a computing warpgroup takes
-      const int c0 = SPLIT ? wg * NCH : 0;
-      constexpr int DCOLS = SPLIT ? 32 : 64;  // TMEM columns of a dQ partial one thread drains
-      const int dcol0 = SPLIT ? wg * 32 : 0;
-      const bool leader = (warp == 0 && lane == 0);  // issues the dQ reductions and the stores
-      uint8_t* stg = smem + C::OFF_STG;
+      constexpr int NCH = BM / 64;  // 32-query chunks a compute warpgroup takes
+      const int c0 = wg * NCH;
       bool ok = start_ok;
-      uint32_t stg_uses = 0;  // staging-tile handshakes (dQ partials and epilogues, all items)
-      // take the staging tile: free once the previous bulk copy has read it (bounded waits on
-      // mbarriers, not named barriers, so a warp that gave up cannot leave the others waiting)
-      auto stage_begin = [&]() {
-        if (leader) {
-          bulk_wait_group_read<0>();
-          mbar_arrive(bar + B_STG_FREE);
-        }
-        return __all_sync(0xffffffffu, mbar_wait(bar + B_STG_FREE, stg_uses & 1, ctx, 141));
-      };
-      // both warpgroups have written their part: the leader may copy it out
-      auto stage_end = [&]() {
-        fence_proxy_async_smem();
-        mbar_arrive(bar + B_STG_FULL);
-        return !leader || mbar_wait(bar + B_STG_FULL, stg_uses & 1, ctx, 142);
-      };
-      // dQ partial k -> staging tile (this warpgroup's half) -> one TMA reduce-add into the fp32
-      // accumulator
-      auto drain = [&](uint32_t k, int q0, int qh) {
-        bool good = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, k & 1, ctx, 140));
-        if (!good) return false;
-        tc_fence_after();
-        uint32_t vr[DCOLS / 32][32];  // this thread's TMEM columns of the partial
-#pragma unroll
-        for (int c = 0; c < DCOLS / 32; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + dcol0 + c * 32), vr[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < DCOLS / 32; ++c) reg_fence(vr[c]);
-        const uint32_t* v = &vr[0][0];
-        tc_fence_before();
-        mbar_arrive(bar + B_DQ_FREE);
-        if (!stage_begin()) return false;
-        if constexpr (C::DQT) {
-          // [64 queries][128 d] fp32, row-major: TMEM lane = d (rit), columns = this warpgroup's
-          // 32 queries
-          float* st = reinterpret_cast<float*>(stg) + rit;
-#pragma unroll
-          for (int j = 0; j < DCOLS; ++j) st[(dcol0 + j) * D] = __uint_as_float(v[j]);
-        } else {
-          // [128 queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns; TMEM lane =
-          // query row (rit), columns = this thread's d (one box per 32)
-#pragma unroll
-          for (int j = 0; j < DCOLS / 4; ++j) {
-            uint8_t* bx = stg + (dcol0 / 32 + j / 8) * (BM * 128) + rit * 128;
-            *reinterpret_cast<uint4*>(bx + (((uint32_t)(j & 7) ^ sw) << 4)) =
-                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-        }
-        good = stage_end();
-        if (leader && good) {
-          if constexpr (C::DQT) {
-            tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
-          } else {
-            tma_reduce_add_3d(&tm_dq, stg, 0, q0, qh);
-            tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, qh);
-          }
-          bulk_commit_group();
-        }
-        ++stg_uses;
-        return good;
-      };
       uint32_t gs = 0;  // steps processed (all items)
       for (int r = 0, item = next_item(0, ok); ok && item >= 0; item = next_item(++r, ok)) {
         const BwdItem w = item_at(item);
@@ -906,7 +714,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tc_fence_before();
           mbar_arrive(bar + B_KT_READY);
         }
-        int prev_q0 = 0, prev_qh = 0;
         for (int i = 0, ii = 0, g = 0; ok && i < w.nsteps; ++i, ++gs, step_next(ii, g, w.nsteps_head)) {
           const int s = gs % C::QSTAGES;
           int gm, q0;
@@ -1019,43 +826,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar + B_DS_READY);
-          if (i > 0 && !(ok = drain(gs - 1, prev_q0, prev_qh))) break;
-          prev_q0 = q0;
-          prev_qh = w.kvh * group + gm;
         }
-        if (ok && w.nsteps > 0) ok = drain(gs - 1, prev_q0, prev_qh);
-        if (!ok) break;
-        // epilogue of this item: WG0 dV, WG1 dK (x tau), each a [128 rows][64 columns] 16-bit
-        // box of the staging tile, then TMA stores (rows past N are not written).  An item
-        // without steps (masked) stores zeros.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, r & 1, ctx, 132));
-        if (!ok) break;
-        uint32_t pa[D / 32][16] = {};
-        if (w.nsteps > 0) {
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c)
-            load_acc32(lane_base, (wg ? C::COL_DK : C::COL_DV) + c * 32, wg ? scale : 1.f, pa[c]);
-        }
-        tc_fence_before();
-        mbar_arrive(bar + B_ACC_EMPTY);  // the accumulators may be overwritten
-        // one [128 rows][64 columns] box of dV (warpgroup 0) and of dK (warpgroup 1) per round
-#pragma unroll
-        for (int b = 0; b < D / 64 && ok; ++b) {
-          if (!(ok = stage_begin())) break;
-          stage_row32(stg + wg * (BN * 128), rit, 0, pa[2 * b]);
-          stage_row32(stg + wg * (BN * 128), rit, 1, pa[2 * b + 1]);
-          ok = stage_end();
-          if (leader && ok) {
-            tma_store_3d(&tm_dv, stg, b * 64, w.k0, w.kvh);
-            tma_store_3d(&tm_dk, stg + BN * 128, b * 64, w.k0, w.kvh);
-            bulk_commit_group();
-          }
-          ++stg_uses;
-        }
-        if (!ok) break;
       }
-      if (leader) bulk_wait_group<0>();  // every reduction and store issued here has completed
     }
   }
   tc_fence_before();
@@ -1101,7 +873,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
   if (!MASKED && !a.sched) return cudaErrorInvalidValue;
   // causal order: groups of key/value heads whose query-side streams (Q, dO, the fp32 dQ
   // accumulator, L and D of each of their `group` query heads) stay in L2
-  const int hgroup = head_group_for_l2((int64_t)a.group * ((int64_t)npad * D * 8 + (int64_t)npad * 8));
+  const int hgroup = head_group_for_l2((int64_t)a.group * ((int64_t)npad * D * 8 + (int64_t)npad * 8), kL2HeadBudgetBwd);
   kern<<<(unsigned)grid, C::THREADS, smem, a.stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a.lse2, a.delta, a.n, npad,
                                                        bh_kv, ktiles, a.scale, a.causal, a.group, a.err, a.window,
                                                        a.block_mask, a.mask_heads, a.heads, a.sched, hgroup);

@@ -1026,7 +1026,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, F8Scales f8 = F8Scales()) {
   const int64_t items = (int64_t)a.bh * tiles;
   const int64_t grid = MASKED ? items : std::min<int64_t>(items, device_sm_count());
   // causal order: groups of query heads whose K, V (shared by `group` query heads) stay in L2
-  const int hgroup = head_group_for_l2((int64_t)2 * a.n * C::ROW / a.group);
+  const int hgroup = head_group_for_l2((int64_t)2 * a.n * C::ROW / a.group, kL2HeadBudgetFwd);
   const int snake = (!MASKED && a.causal && grid < items &&
                      max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, true, hgroup) <
                          max_cta_tiles(a.bh, tiles, a.n, C::NQ, (int)grid, false, hgroup))
