@@ -226,17 +226,18 @@ def test_fp8_argument_checks(fa):
             fa.attention_forward_fp8(z, z, z, s, s, s)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("h,hkv", [(4, 2), (4, 1)])
-def test_fp8_forward_grouped_query_heads(fa, causal, h, hkv):
+def test_fp8_forward_grouped_query_heads(fa, causal, h, hkv, d):
     """fa_fwd_fp8_gqa: query head i reads key/value head i / (H / Hkv); against the fp64 oracle
     of grouped-query attention on the dequantised inputs."""
     n = 300
-    q = _draw((2, h, n, 128), 70 + h + hkv)
-    k, v = (_draw((2, hkv, n, 128), 80 + i + hkv) for i in range(2))
+    q = _draw((2, h, n, d), 70 + h + hkv + d)
+    k, v = (_draw((2, hkv, n, d), 80 + i + hkv + d) for i in range(2))
     (qc, qs), (kc, ks), (vc, vs) = (F8.quantize_blocks(t) for t in (q, k, v))
     dev = [_codes_to_bytes(c).cuda() for c in (qc, kc, vc)] + [torch.from_numpy(x).cuda() for x in (qs, ks, vs)]
-    scale = 128 ** -0.5
+    scale = d ** -0.5
     o, lse = fa.attention_forward_fp8(*dev[:3], *dev[3:], scale=scale, causal=causal)
     fa.fa_check_device_error()
     deq = [F8.dequantize_blocks(c, x) for c, x in ((qc, qs), (kc, ks), (vc, vs))]
