@@ -252,7 +252,9 @@ FA_API fa_status fa_bwd_masked(const void* Q, const void* K, const void* V, cons
  *   d        64, 128 or 256
  * For each block, scale = amax / 448 (1 when the block is all zero) and
  * code = E4M3(x / scale), rounded to nearest even and saturated at +-448; both divisions are
- * fp32 divisions rounded to nearest. One kernel, one thread block per 128-row block.
+ * fp32 divisions rounded to nearest. One kernel launch: for 16-bit inputs a persistent grid
+ * (three thread blocks per SM) streams the blocks; for fp32 inputs one thread block takes one
+ * block.
  */
 FA_API fa_status fa_quantize_fp8(const void* X, void* X8, float* scales, int B, int H, int N, int d, fa_dtype dtype,
                                  void* stream);
