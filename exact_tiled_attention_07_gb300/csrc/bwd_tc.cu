@@ -54,16 +54,23 @@ constexpr int BN = 128;  // key rows per CTA
 
 template <int D>
 struct BwdCfg {
-  static constexpr bool DQT = (D == 128);        // dQ^T = K^T dS^T (TMEM lanes = d)
-  static constexpr int BM = DQT ? 64 : 128;      // query rows per step
+  // d = 256: a work item is one half of d of a key tile's outputs (dK, dV and dQ columns
+  // [128 h, 128 h + 128)); both halves recompute S^T and dP^T over all 256 dimensions, since the
+  // dV and dK accumulators of a whole row (2 x 256 columns) would fill all of TMEM
+  static constexpr bool SPLITD = (D == 256);
+  static constexpr int DH = SPLITD ? 128 : D;  // output columns of d per item
+  static constexpr bool DQT = (D >= 128);      // dQ^T = K^T dS^T (TMEM lanes = d)
+  static constexpr int BM = D == 64 ? 128 : (D == 128 ? 64 : 32);  // query rows per step
+  static constexpr bool K_IN_TMEM = !SPLITD;   // K_j as the TMEM A operand of S^T (d/2 columns)
+  static constexpr bool DS_SW64 = (BM == 32);  // dS^T rows of 64 bytes: the 64-byte swizzle
   static constexpr int KB = D / 64;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int QT_BYTES = BM * D * 2;
   static constexpr int DS_BYTES = BN * BM * 2;
-  static constexpr int STG_BYTES = BM * D * 4;
-  // WG0 and WG1 compute (half the queries of a step each), WG2 drains; then the TMA producer
-  // warp and the MMA warp.
-  static constexpr int COMPUTE_WGS = 2;
+  static constexpr int STG_BYTES = BM * DH * 4;
+  // WG0 and WG1 compute (half the queries of a step each; d = 256: WG0 alone, 32 queries), then
+  // the drain warpgroup, the TMA producer warp and the MMA warp.
+  static constexpr int COMPUTE_WGS = BM / 32 >= 2 ? 2 : 1;
   static constexpr int DRAIN_WARP0 = 4 * COMPUTE_WGS;  // first warp of the drain warpgroup
   static constexpr int PRODUCER_WARP = DRAIN_WARP0 + 4;
   static constexpr int MMA_WARP = PRODUCER_WARP + 1;
@@ -71,7 +78,7 @@ struct BwdCfg {
   static constexpr uint32_t ITEM_READERS = 1 + 4 * COMPUTE_WGS + 4;  // MMA, compute and drain warps
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int QSTAGES = 3;                          // query-tile ring depth
+  static constexpr int QSTAGES = SPLITD ? 2 : 3;             // query-tile ring depth
   static constexpr int OFF_Q = OFF_V + KV_BYTES;                 // [QSTAGES]
   static constexpr int OFF_DO = OFF_Q + QSTAGES * QT_BYTES;      // [QSTAGES]
   static constexpr int OFF_DS = OFF_DO + QSTAGES * QT_BYTES;
@@ -94,17 +101,21 @@ struct BwdCfg {
   static constexpr int CH_COLS = 32;
   static constexpr int EPI_THREADS = 128;  // threads that read dK, dV out of TMEM (the drain warpgroup)
   // the staging tile also carries an item's dV and dK as 16-bit [128 rows][64 columns] boxes with
-  // the 128-byte swizzle (d = 128: dV, then dK, two boxes each; d = 64: dV and dK side by side)
-  static_assert(STG_BYTES >= 2 * BN * 128 && OFF_STG % 1024 == 0, "staging tile");
-  // TMEM columns: K_j as a 16-bit A operand (d/2 columns), S^T (P^T packed into the first 16
-  // of each 32-query chunk's columns), dP^T (dS^T likewise), the dQ partial and the dV, dK
-  // accumulators
+  // the 128-byte swizzle (d = 128: dV, then dK, two boxes each; d = 64: dV and dK side by side;
+  // d = 256: one box at a time)
+  static_assert(STG_BYTES >= (SPLITD ? 1 : 2) * BN * 128 && OFF_STG % 1024 == 0 && OFF_DS % 1024 == 0,
+                "staging tile");
+  static_assert(SMEM <= 232448, "shared memory");
+  // TMEM columns: K_j as a 16-bit A operand (d/2 columns; not at d = 256), S^T (P^T packed into
+  // the first 16 of each 32-query chunk's columns), dP^T (dS^T likewise), the dQ partial and the
+  // dV, dK accumulators (DH columns each)
   static constexpr uint32_t COL_K = DQT ? 0 : 448;
-  static constexpr uint32_t COL_S = DQT ? 64 : 0;
+  static constexpr uint32_t COL_S = SPLITD ? 0 : (DQT ? 64 : 0);
   static constexpr uint32_t COL_DP = COL_S + BM;
   static constexpr uint32_t COL_DQ = COL_DP + BM;
-  static constexpr uint32_t COL_DV = DQT ? 256 : 320;
-  static constexpr uint32_t COL_DK = 384;
+  static constexpr uint32_t COL_DV = SPLITD ? 128 : (DQT ? 256 : 320);
+  static constexpr uint32_t COL_DK = SPLITD ? 256 : 384;
+  static_assert(COL_DK + DH <= 512 && COL_DQ + (DQT ? BM : D) <= COL_DV, "TMEM columns");
 };
 
 enum BwdBar {
@@ -143,6 +154,7 @@ __device__ __forceinline__ void step_next(int& ii, int& g, int tiles_per_head) {
 // Work item of the persistent backward: one 128-key tile of one key/value head.
 struct BwdItem {
   int kvh;          // key/value head
+  int dh;           // d = 256: which half of d this item's outputs cover (0 or 1), else 0
   int k0;           // first key row
   int i_start;      // first query tile reaching this key tile's diagonal (causal), else 0
   int nsteps_head;  // query tiles per query head
@@ -184,7 +196,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const ErrCtx ctx{err, abort_flag};
 
   const int qtiles = (n + BM - 1) / BM;
-  const int64_t total_items = (int64_t)bh_count * ktiles;
+  // d = 256: two items per key tile (the two halves of d, adjacent in the order, so both read
+  // the tile's K, V and the query-side streams while they are in L2)
+  constexpr int kHalves = C::SPLITD ? 2 : 1;
+  const int64_t total_items = (int64_t)bh_count * ktiles * kHalves;
   // work item -> key/value head and key tile: head-major (CTAs running together share Q/dO in
   // L2); causal: heaviest (first) key tiles first within groups of heads
   auto tile_of = [&](int item, int* kvh, int* kt) {
@@ -200,7 +215,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if constexpr (MASKED) {
     if (warp == C::PRODUCER_WARP) {
       int kvh, kt;
-      tile_of((int)blockIdx.x, &kvh, &kt);
+      tile_of((int)blockIdx.x / kHalves, &kvh, &kt);
       const int k0 = kt * BN;
       const int nblk = (n + 127) / 128;
       const int kmax = min(n, k0 + BN) - 1;
@@ -269,7 +284,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   auto item_at = [&](int item) {
     BwdItem w;
     int kt;
-    tile_of(item, &w.kvh, &kt);
+    tile_of(item / kHalves, &w.kvh, &kt);
+    w.dh = C::SPLITD ? (item & 1) : 0;
     w.k0 = kt * BN;
     w.i_start = causal ? kt * (BN / BM) : 0;
     w.nsteps_head = qtiles - w.i_start;
@@ -414,8 +430,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (start_ok) {
       const bool leader = elect_one_sync();
       const uint32_t idesc_s = make_idesc_f16(BN, BM, BF16, false, false);  // S^T, dP^T: M = keys, N = queries
-      const uint32_t idesc_kv = make_idesc_f16(BN, D, BF16, false, true);   // dV, dK: M = keys, N = d
-      const uint32_t idesc_q = C::DQT ? make_idesc_f16(D, BM, BF16, true, true)    // dQ^T: M = d, N = queries
+      const uint32_t idesc_kv = make_idesc_f16(BN, C::DH, BF16, false, true);   // dV, dK: M = keys, N = d (half)
+      const uint32_t idesc_q = C::DQT ? make_idesc_f16(C::DH, BM, BF16, true, true)  // dQ^T: M = d (half), N = queries
                                       : make_idesc_f16(BM, D, BF16, true, true);   // dQ: M = queries, N = d
       const uint32_t ks = smem_u32(smem + C::OFF_K), vs = smem_u32(smem + C::OFF_V);
       const uint32_t dss = smem_u32(smem + C::OFF_DS);
@@ -430,14 +446,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       };
       // K-major operand rows of 128 bytes in 64-column blocks: offset of K-slice kk (16 wide)
       auto kmaj = [](int kk, int rows) { return (uint32_t)((kk * 16 / 64) * (rows * 128) + (kk * 16 % 64) * 2); };
-      // S^T = K Q_i^T with K_j from TMEM (A) and Q_i K-major in smem (B)
+      // S^T = K Q_i^T with K_j from TMEM (A) and Q_i K-major in smem (B); d = 256: K_j K-major
+      // in smem as well
       auto issue_s = [&](uint32_t b) {
         uint64_t bd[D / 16];
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) bd[kk] = make_sdesc_sw128(b + kmaj(kk, BM), 16, 1024);
-        if (leader) {
+        if constexpr (C::K_IN_TMEM) {
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) umma_ts(tbase + C::COL_S, tbase + C::COL_K + kk * 8, bd[kk], idesc_s, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_ts(tbase + C::COL_S, tbase + C::COL_K + kk * 8, bd[kk], idesc_s, kk > 0);
+          }
+        } else {
+          uint64_t ad[D / 16];
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) ad[kk] = make_sdesc_sw128(ks + kmaj(kk, BN), 16, 1024);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) umma_ss(tbase + C::COL_S, ad[kk], bd[kk], idesc_s, kk > 0);
+          }
         }
         __syncwarp();
       };
@@ -481,11 +509,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             __syncwarp();
           }
           commit(bar + B_DP_FULL);
-          // dV += P^T dO_i (P^T from TMEM, K = queries; dO_i as MN-major B)
+          // dV += P^T dO_i (P^T from TMEM, K = queries; dO_i as MN-major B: the item's DH columns,
+          // 64-column boxes of BM rows)
           {
             uint64_t bd[BM / 16];
 #pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk) bd[kk] = make_sdesc_sw128(dos + kk * 2048, BM * 128, 1024);
+            for (int kk = 0; kk < BM / 16; ++kk)
+              bd[kk] = make_sdesc_sw128(dos + w.dh * (C::DH / 64) * (BM * 128) + kk * 2048, BM * 128, 1024);
             if (!(ok = wait(bar + B_P_READY, gs & 1, 123))) break;
             if (!acc_free) {
               if (!(ok = wait(bar + B_ACC_EMPTY, (r - 1) & 1, 127))) break;
@@ -517,13 +547,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           {
             uint64_t dk_b[BM / 16], kd[BN / 16], sd[BN / 16];
 #pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk) dk_b[kk] = make_sdesc_sw128(qs + kk * 2048, BM * 128, 1024);
+            for (int kk = 0; kk < BM / 16; ++kk)
+              dk_b[kk] = make_sdesc_sw128(qs + w.dh * (C::DH / 64) * (BM * 128) + kk * 2048, BM * 128, 1024);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
-              kd[kk] = make_sdesc_sw128(ks + kk * 2048, BN * 128, 1024);   // K as MN-major (d contiguous)
-              sd[kk] = make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024);  // dS^T as MN-major (queries contiguous)
+              // K as MN-major (d contiguous; the item's DH columns), dS^T as MN-major (queries
+              // contiguous: 128-byte rows, or 64-byte rows with the 64-byte swizzle at d = 256)
+              kd[kk] = make_sdesc_sw128(ks + w.dh * (C::DH / 64) * (BN * 128) + kk * 2048, BN * 128, 1024);
+              if constexpr (C::DS_SW64)
+                sd[kk] = make_sdesc_sw64(dss + kk * 1024, BN * 64, 512);
+              else
+                sd[kk] = make_sdesc_sw128(dss + kk * 2048, BN * 128, 1024);
             }
-            constexpr int kDkHead = BM / 64;  // 1 at d = 128, 2 at d = 64
+            constexpr int kDkHead = BM / 64;  // 1 at d = 128, 2 at d = 64, 0 at d = 256
             if (!(ok = wait(bar + B_DS_READY, gs & 1, 124))) break;
             tc_fence_after();
             if (leader) {
@@ -550,7 +586,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     umma_ss(tbase + C::COL_DQ, sd[kk], kd[kk], idesc_q, kk > 0);
                 } else {
                   const int kk = kDkHead + b++;
-                  umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + packed_col(kk, C::CH_COLS), dk_b[kk], idesc_kv, 1u);
+                  umma_ts(tbase + C::COL_DK, tbase + C::COL_DP + packed_col(kk, C::CH_COLS), dk_b[kk], idesc_kv,
+                          (i > 0 || kk > 0) ? 1u : 0u);
                   if (b == NB) umma_commit(bar + B_QD_EMPTY + s);  // Q_i, dO_i no longer read
                 }
               }
@@ -581,7 +618,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // partial, its dV and dK (x tau) go through the same staging tile to global memory (TMA
     // stores), while the compute warpgroups start the next item.
     const uint32_t lane_base = (warp & 3) * 32;
-    // TMEM lane: d index (d = 128) or query row (d = 64) of a dQ partial; key row of dK, dV
+    // TMEM lane: d index (d = 128; d = 256: within the item's half) or query row (d = 64) of a dQ
+    // partial; key row of dK, dV
     const int rr = (warp & 3) * 32 + lane;
     const bool leader = (warp == C::DRAIN_WARP0 && lane == 0);
     uint8_t* stg = smem + C::OFF_STG;
@@ -602,22 +640,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         step_rows(w, i, ii, g, &gm, &q0);
         ok = __all_sync(0xffffffffu, mbar_wait(bar + B_DQ_FULL, gs & 1, ctx, 140)) && ok;
         tc_fence_after();
-        uint32_t vr[2][32];
+        constexpr int DQC = (C::DQT ? BM : D) / 32;  // 32-column TMEM chunks of a dQ partial
+        uint32_t vr[DQC][32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + c * 32), vr[c]);
+        for (int c = 0; c < DQC; ++c) tmem_ld32(tmem_addr(tbase, lane_base, C::COL_DQ + c * 32), vr[c]);
         tmem_wait_ld();
-        reg_fence(vr[0]);
-        reg_fence(vr[1]);
+#pragma unroll
+        for (int c = 0; c < DQC; ++c) reg_fence(vr[c]);
         const uint32_t* v = &vr[0][0];
         tc_fence_before();
         mbar_arrive(bar + B_DQ_FREE);
         if (leader) bulk_wait_group_read<0>();  // the previous bulk copy has finished reading the tile
         named_bar_sync(1, 128);
         if constexpr (C::DQT) {
-          // [BM queries][D] fp32, row-major: column rr (this thread's d) of each query row
+          // [BM queries][DH] fp32, row-major: column rr (this thread's d) of each query row
           float* st = reinterpret_cast<float*>(stg) + rr;
 #pragma unroll
-          for (int q = 0; q < BM; ++q) st[q * D] = __uint_as_float(v[q]);
+          for (int q = 0; q < BM; ++q) st[q * C::DH] = __uint_as_float(v[q]);
         } else {
           // [BM queries][64] fp32 as two 128-byte-swizzled boxes of 32 columns: row rr (this
           // thread's query), 16-byte chunks
@@ -632,7 +671,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (leader && ok) {
-          tma_reduce_add_3d(&tm_dq, stg, 0, q0, w.kvh * group + gm);
+          tma_reduce_add_3d(&tm_dq, stg, w.dh * C::DH, q0, w.kvh * group + gm);
           if constexpr (!C::DQT) tma_reduce_add_3d(&tm_dq, stg + BM * 128, 32, q0, w.kvh * group + gm);
           bulk_commit_group();
         }
@@ -643,6 +682,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar + B_ACC_FULL, r & 1, ctx, 132)) && ok;
       const bool acc = ok && w.nsteps > 0;
       if (acc) tc_fence_after();
+      if constexpr (C::SPLITD) {
+        // d = 256: this row's DH columns of dV and of dK (x tau) into registers, the accumulators
+        // released, then one 16 KB box at a time through the staging tile (dV's two, then dK's)
+        uint32_t pvv[C::DH / 32][16], pkv[C::DH / 32][16];
+#pragma unroll
+        for (int c = 0; c < C::DH / 32; ++c) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) pvv[c][t] = pkv[c][t] = 0u;
+          if (acc) {
+            load_acc32(lane_base, C::COL_DV + c * 32, 1.f, pvv[c]);
+            load_acc32(lane_base, C::COL_DK + c * 32, scale, pkv[c]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar + B_ACC_EMPTY);  // the accumulators may be overwritten
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+          for (int b = 0; b < C::DH / 64; ++b) {
+            if (leader) bulk_wait_group_read<0>();  // the previous bulk copy has read the tile
+            named_bar_sync(1, 128);
+            stage_row32(stg, rr, 0, t ? pkv[2 * b] : pvv[2 * b]);
+            stage_row32(stg, rr, 1, t ? pkv[2 * b + 1] : pvv[2 * b + 1]);
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (leader && ok) {
+              tma_store_3d(t ? &tm_dk : &tm_dv, stg, w.dh * C::DH + b * 64, w.k0, w.kvh);
+              bulk_commit_group();
+            }
+          }
+        }
+      } else {
       uint32_t pkk[D / 2];  // this row of dK x tau, packed
       if (leader) bulk_wait_group_read<0>();  // the last dQ reduction has read the staging tile
       named_bar_sync(1, 128);
@@ -684,6 +755,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_dk, stg + b * (BN * 128), b * 64, w.k0, w.kvh);
         bulk_commit_group();
       }
+      }
     }
     if (leader) bulk_wait_group<0>();  // every reduction and store issued here has completed
 
@@ -698,7 +770,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const int rit = (warp & 3) * 32 + lane;  // key row within the tile (and TMEM lane)
       uint8_t* ds_row = smem + C::OFF_DS + rit * 128;
       const uint32_t sw = (uint32_t)(rit & 7);
-      constexpr int NCH = BM / 64;  // 32-query chunks a compute warpgroup takes
+      constexpr int NCH = BM / (32 * C::COMPUTE_WGS);  // 32-query chunks a compute warpgroup takes
       const int c0 = wg * NCH;
       bool ok = start_ok;
       uint32_t gs = 0;  // steps processed (all items)
@@ -710,7 +782,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           // K_j -> TMEM: the previous item's last S^T (which read it) completed before its last step
           ok = __all_sync(0xffffffffu, mbar_wait(bar + B_KV, r & 1, ctx, 134));
           if (!ok) break;
-          k_to_tmem(rit, lane_base);
+          if constexpr (C::K_IN_TMEM) k_to_tmem(rit, lane_base);
           tc_fence_before();
           mbar_arrive(bar + B_KT_READY);
         }
@@ -823,13 +895,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 dsk[t] = pack2<BF16>(ds01.x, ds01.y);
                 dsk[t + 1] = pack2<BF16>(ds23.x, ds23.y);
               }
-              // 32 queries = 64 bytes = four 16-byte chunks of this key's row, 128-byte swizzle
-              uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
+              // 32 queries = 64 bytes = four 16-byte chunks of this key's row: 128-byte rows with
+              // the 128-byte swizzle, or (32 queries a step) 64-byte rows with the 64-byte swizzle
+              // (chunk index XOR bits 1-2 of the row)
+              if constexpr (C::DS_SW64) {
+                uint8_t* row64 = smem + C::OFF_DS + rit * 64;
+                const uint32_t sw64 = (uint32_t)((rit >> 1) & 3);
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
-                *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
-                    make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
+                for (int u = 0; u < 4; ++u)
+                  *reinterpret_cast<uint4*>(row64 + (((uint32_t)u ^ sw64) << 4)) =
+                      make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
+              } else {
+                uint8_t* blk = ds_row + (c >> 1) * (BN * 128);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const uint32_t ch = (uint32_t)((c & 1) * 4 + u);
+                  *reinterpret_cast<uint4*>(blk + ((ch ^ sw) << 4)) =
+                      make_uint4(dsk[4 * u], dsk[4 * u + 1], dsk[4 * u + 2], dsk[4 * u + 3]);
+                }
               }
               // and packed into TMEM over this chunk's dP^T columns, already read (A operand of
               // dK += dS^T Q)
@@ -872,7 +955,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
   if (!make_tmap_16bit_3d(&tq, a.q, BF16, D, a.n, a.bh, C::BM) || !make_tmap_16bit_3d(&tk, a.k, BF16, D, a.n, bh_kv, BN) ||
       !make_tmap_16bit_3d(&tv, a.v, BF16, D, a.n, bh_kv, BN) ||
       !make_tmap_16bit_3d(&tdo, a.dout, BF16, D, a.n, a.bh, C::BM) ||
-      !make_tmap_f32_3d(&tdq, a.dq_acc, D, npad, a.bh, C::DQT ? D : 32, C::BM, !C::DQT) ||
+      !make_tmap_f32_3d(&tdq, a.dq_acc, D, npad, a.bh, C::DQT ? C::DH : 32, C::BM, !C::DQT) ||
       !make_tmap_16bit_3d(&tdk, a.dk, BF16, D, a.n, bh_kv, BN) || !make_tmap_16bit_3d(&tdv, a.dv, BF16, D, a.n, bh_kv, BN))
     return cudaErrorInvalidValue;
   auto kern = bwd_tc_kernel<D, BF16, MASKED>;
@@ -882,7 +965,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int ktiles = (a.n + BN - 1) / BN;
-  const int64_t items = (int64_t)bh_kv * ktiles;
+  const int64_t items = (int64_t)bh_kv * ktiles * (C::SPLITD ? 2 : 1);
   const int64_t grid = MASKED ? items : std::min<int64_t>(items, device_sm_count());
   if (!MASKED && !a.sched) return cudaErrorInvalidValue;
   // causal order: groups of key/value heads whose query-side streams (Q, dO, the fp32 dQ
@@ -901,15 +984,18 @@ cudaError_t launch_bwd_dm(const BwdArgs& a) {
 
 }  // namespace
 
-bool bwd_tc_supported(int dtype, int d) { return (dtype == DT_BF16 || dtype == DT_FP16) && (d == 64 || d == 128); }
+bool bwd_tc_supported(int dtype, int d) {
+  return (dtype == DT_BF16 || dtype == DT_FP16) && (d == 64 || d == 128 || d == 256);
+}
 
 bool bwd_masked_fits(int group, int n, int d) {
   // step-list entries pack (query head of the group, 128-row block) into 16 bits, and the
   // list must fit in shared memory beside the kernel's tiles
   const int nblk = (n + 127) / 128;
   if (group > 16 || nblk > 4096) return false;
-  const int smem = (d == 128 ? BwdCfg<128>::SMEM + BwdCfg<128>::list_bytes(group * nblk)
-                             : BwdCfg<64>::SMEM + BwdCfg<64>::list_bytes(group * nblk));
+  const int smem = d == 256   ? BwdCfg<256>::SMEM + BwdCfg<256>::list_bytes(group * nblk)
+                   : d == 128 ? BwdCfg<128>::SMEM + BwdCfg<128>::list_bytes(group * nblk)
+                              : BwdCfg<64>::SMEM + BwdCfg<64>::list_bytes(group * nblk);
   return smem <= 232448;
 }
 
@@ -918,6 +1004,7 @@ cudaError_t launch_bwd_tc(const BwdArgs& a) {
   switch (a.d) {
     case 64: return bf ? launch_bwd_dm<64, true>(a) : launch_bwd_dm<64, false>(a);
     case 128: return bf ? launch_bwd_dm<128, true>(a) : launch_bwd_dm<128, false>(a);
+    case 256: return bf ? launch_bwd_dm<256, true>(a) : launch_bwd_dm<256, false>(a);
     default: return cudaErrorNotSupported;
   }
 }

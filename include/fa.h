@@ -30,13 +30,12 @@
  *             word and reported by fa_check_device_error. No C++ exception crosses
  *             this interface. fa_last_error_message() describes the last failure of
  *             the calling thread.
- *   Paths     bf16/fp16 with d in {64, 128, 256} (forward) or {64, 128} (backward)
- *             run the tensor-core kernels (TMA, tcgen05 MMAs accumulating in tensor
- *             memory); fp32, and any other d in [1, 256], run CUDA-core kernels that
- *             compute in fp32. The choice is never silent: fa_uses_tensor_cores() tells it
- *             in advance, and a bf16/fp16 call that runs on the CUDA-core kernels (another
- *             d, or the d = 256 backward) returns FA_OK with a notice in
- *             fa_last_error_message() naming the path that ran.
+ *   Paths     bf16/fp16 with d in {64, 128, 256} run the tensor-core kernels (TMA,
+ *             tcgen05 MMAs accumulating in tensor memory), forward and backward; fp32, and
+ *             any other d in [1, 256], run CUDA-core kernels that compute in fp32. The
+ *             choice is never silent: fa_uses_tensor_cores() tells it in advance, and a
+ *             bf16/fp16 call that runs on the CUDA-core kernels (another d) returns FA_OK
+ *             with a notice in fa_last_error_message() naming the path that ran.
  */
 #ifndef FA_H_
 #define FA_H_

@@ -109,7 +109,8 @@ def test_kernel_selection(lib):
         assert lib.fa_uses_tensor_cores(0, 0, d) == 1  # bf16 forward
         assert lib.fa_uses_tensor_cores(0, 1, d) == 1  # fp16 forward
         assert lib.fa_uses_tensor_cores(0, 2, d) == 0  # fp32: CUDA cores
-    assert lib.fa_uses_tensor_cores(1, 0, 128) == 1 and lib.fa_uses_tensor_cores(1, 0, 256) == 0
+    assert lib.fa_uses_tensor_cores(1, 0, 128) == 1 and lib.fa_uses_tensor_cores(1, 0, 256) == 1
+    assert lib.fa_uses_tensor_cores(1, 1, 96) == 0
     assert lib.fa_uses_tensor_cores(0, 0, 96) == 0
 
 

@@ -2,8 +2,8 @@
 
 The debug library (``build.build(debug=True)``) is loaded in place of the release one for this
 module and the release one is put back afterwards.  Small problems of every tensor-core path
-(forward and backward at d = 64 and 128, grouped-query heads, a sliding window, the d = 256
-forward, FP8 at d = 64, 128 and 256) must run through it with no device error and match the fp64 oracle, so the checks
+(forward and backward at d = 64, 128 and 256, grouped-query heads, a sliding window, FP8 at
+d = 64, 128 and 256) must run through it with no device error and match the fp64 oracle, so the checks
 raise no false alarm; the self-test launches one check with an index out of range, which must
 come back as a device error while the context stays usable.
 """
@@ -83,14 +83,17 @@ def test_debug_build_grouped_query_window_and_d256(fa):
     o_ref, l_ref = M.attn_fwd64_masked(x64["q"], x64["k"], x64["v"], w.scale, M.visible_mask(w.N, causal=True,
                                                                                              window=100))
     _check_fwd(w, x, o, lse, o_ref, l_ref)
-    # d = 256 forward
-    w = Workload("dbg_256", 1, 2, 300, 256, "bf16", False, "normal", 7300)
-    x = make_inputs(w, with_do=False)
+    # d = 256 forward and backward
+    w = Workload("dbg_256", 1, 2, 300, 256, "bf16", True, "normal", 7300)
+    x = make_inputs(w)
     dev = {k_: to_device(v_, w.dtype) for k_, v_ in x.items()}
-    o, lse = fa.attention_forward(dev["q"], dev["k"], dev["v"], scale=w.scale)
+    o, lse = fa.attention_forward(dev["q"], dev["k"], dev["v"], causal=True, scale=w.scale)
+    dq, dk, dv = fa.attention_backward(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, causal=True, scale=w.scale)
     fa.fa_check_device_error()
     x64 = {k_: to_float64(v_, w.dtype) for k_, v_ in x.items()}
-    _check_fwd(w, x, o, lse, *oracle.attn_fwd64(x64["q"], x64["k"], x64["v"], w.scale, False))
+    _check_fwd(w, x, o, lse, *oracle.attn_fwd64(x64["q"], x64["k"], x64["v"], w.scale, True))
+    for g, r in zip((dq, dk, dv), oracle.attn_bwd64(x64["q"], x64["k"], x64["v"], x64["do"], w.scale, True)[:3]):
+        assert rel_rms(to_f64(g), r) <= TOL_GRAD_RELRMS
 
 
 @pytest.mark.parametrize("d,causal", [(64, False), (128, True), (256, False)])

@@ -54,6 +54,13 @@ def test_gqa_tensor_cores(fa, dtype, causal, d, h, hkv, n):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("h,hkv,n", [(4, 2, 257), (4, 1, 130)])
+def test_gqa_d256_forward_backward(fa, causal, h, hkv, n):
+    # both halves of d of each key tile sum the gradients of every query head of the group
+    _check(fa, Workload("gqa256b", 1, h, n, 256, "bf16", causal, "normal", 9150 + h + hkv + n, Hkv=hkv))
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_gqa_forward_d256(fa, causal):
     w = Workload("gqa256", 1, 4, 257, 256, "bf16", causal, "normal", 9100, Hkv=2)
     x = make_inputs(w, with_do=False)

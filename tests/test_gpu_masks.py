@@ -98,6 +98,15 @@ def test_forward_d256_masked(fa):
     _check(fa, Workload("m256", 1, 2, 600, 256, "bf16", True, "normal", 702), window=250, bm=bm, backward=False)
 
 
+@pytest.mark.parametrize("causal,window", [(True, 250), (False, 129)])
+def test_d256_masked_forward_backward(fa, causal, window):
+    # the d = 256 backward's masked variant: one CTA per (key tile, half of d), step list built
+    # from the block mask and the window
+    bm = _block_mask(2, 600, 0.6, 25)
+    bm[..., 0] = 1
+    _check(fa, Workload("m256b", 1, 2, 600, 256, "bf16", causal, "normal", 703 + window), window=window, bm=bm)
+
+
 def test_visited_tiles_follow_the_nonzero_blocks(fa):
     # Proposition 4: the work is the number of (query tile, key tile) pairs with a visible score
     n, h = 2048, 2

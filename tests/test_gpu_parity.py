@@ -105,10 +105,27 @@ def test_tensor_core_fwd_d256(fa, dtype, causal, n):
     _check_fwd(w, x64, got)
 
 
-@pytest.mark.parametrize("d", [32, 96, 256])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 31, 130, 300, 515])
+def test_tensor_core_bwd_d256(fa, dtype, causal, n):
+    # d = 256 backward on the tensor cores: each key tile's dK, dV in two halves of d (two work
+    # items recomputing S and dP over all of d), 32 queries a step; ragged N and one-row problems
+    w = Workload("tcb256", 2, 2, n, 256, dtype, causal, "normal", 2100 + n + causal)
+    assert fa.fa_uses_tensor_cores("bwd", torch.bfloat16 if dtype == "bf16" else torch.float16, 256)
+    x64, got = _run(fa, w)
+    assert fa.fa_last_error_message() == ""  # no CUDA-core notice
+    # the forward's element-wise bound is checked by the forward tests; here the rows of a few
+    # keys (n = 31, causal) reach |O| > 2, where a bf16 output's own rounding is up to 2^-7
+    o_ref, l_ref = oracle.attn_fwd64(x64["q"], x64["k"], x64["v"], w.scale, w.causal)
+    assert rel_rms(got["o"], o_ref) <= TOL_O_RELRMS and max_abs(got["lse"], l_ref) <= TOL_L_MAXABS
+    _check_bwd(w, x64, got)
+
+
+@pytest.mark.parametrize("d", [32, 96, 200])
 def test_cuda_core_path_16bit(fa, d):
-    # head dims without a tensor-core kernel (and the d = 256 backward) use the CUDA-core kernels;
-    # the binding warns about it before the call
+    # head dims without a tensor-core kernel use the CUDA-core kernels; the binding warns about
+    # it before the call
     w = Workload("simt16", 1, 2, 150, d, "bf16", True, "normal", 3000 + d)
     with pytest.warns(UserWarning, match="CUDA-core"):
         x64, got = _run(fa, w)
@@ -116,7 +133,7 @@ def test_cuda_core_path_16bit(fa, d):
     _check_bwd(w, x64, got)
 
 
-@pytest.mark.parametrize("d,pass_", [(96, "forward"), (256, "backward"), (32, "backward")])
+@pytest.mark.parametrize("d,pass_", [(96, "forward"), (200, "backward"), (32, "backward")])
 def test_cuda_core_path_is_reported_by_the_c_abi(fa, d, pass_):
     # a 16-bit call that runs on the CUDA-core kernels succeeds and leaves a notice naming the
     # path; a tensor-core call leaves none

@@ -81,12 +81,14 @@ def _check_oracle(w, x, got):
 
 
 def test_noalloc_calls_in_a_row_with_different_shapes(fa):
-    """A larger causal bf16 d = 128 call, a smaller non-causal fp16 d = 64 call, then the first
-    again: each finds the previous call's queue counters and accumulator rows in the array."""
+    """A larger causal bf16 d = 128 call, a smaller non-causal fp16 d = 64 call, a d = 256 call,
+    then the first again: each finds the previous call's queue counters and accumulator rows in
+    the array."""
     big = Workload("noalloc_bf16", 2, 2, 700, 128, "bf16", True, "normal", 8100)
     small = Workload("noalloc_fp16", 1, 3, 513, 64, "fp16", False, "normal", 8200)
-    cases = {w.name: (w,) + _case(w) for w in (big, small)}
-    for name in ("noalloc_bf16", "noalloc_fp16", "noalloc_bf16"):
+    wide = Workload("noalloc_d256", 1, 2, 300, 256, "bf16", True, "normal", 8250)
+    cases = {w.name: (w,) + _case(w) for w in (big, small, wide)}
+    for name in ("noalloc_bf16", "noalloc_fp16", "noalloc_d256", "noalloc_bf16"):
         w, x, dev = cases[name]
         got = _noalloc_vs_workspace(fa, w, dev)
         _check_oracle(w, x, got)
