@@ -61,7 +61,7 @@ struct BwdCfg {
   static constexpr int DH = SPLITD ? 128 : D;  // output columns of d per item
   static constexpr bool DQT = (D >= 128);      // dQ^T = K^T dS^T (TMEM lanes = d)
   static constexpr int BM = D == 64 ? 128 : (D == 128 ? 64 : 32);  // query rows per step
-  static constexpr bool K_IN_TMEM = !SPLITD;   // K_j as the TMEM A operand of S^T (d/2 columns)
+  static constexpr bool K_IN_TMEM = true;      // K_j as the TMEM A operand of S^T (d/2 columns)
   static constexpr bool DS_SW64 = (BM == 32);  // dS^T rows of 64 bytes: the 64-byte swizzle
   static constexpr int KB = D / 64;
   static constexpr int KV_BYTES = BN * D * 2;
@@ -106,16 +106,17 @@ struct BwdCfg {
   static_assert(STG_BYTES >= (SPLITD ? 1 : 2) * BN * 128 && OFF_STG % 1024 == 0 && OFF_DS % 1024 == 0,
                 "staging tile");
   static_assert(SMEM <= 232448, "shared memory");
-  // TMEM columns: K_j as a 16-bit A operand (d/2 columns; not at d = 256), S^T (P^T packed into
+  // TMEM columns: K_j as a 16-bit A operand (d/2 columns), S^T (P^T packed into
   // the first 16 of each 32-query chunk's columns), dP^T (dS^T likewise), the dQ partial and the
   // dV, dK accumulators (DH columns each)
-  static constexpr uint32_t COL_K = DQT ? 0 : 448;
+  static constexpr uint32_t COL_K = SPLITD ? 384 : (DQT ? 0 : 448);
   static constexpr uint32_t COL_S = SPLITD ? 0 : (DQT ? 64 : 0);
   static constexpr uint32_t COL_DP = COL_S + BM;
   static constexpr uint32_t COL_DQ = COL_DP + BM;
   static constexpr uint32_t COL_DV = SPLITD ? 128 : (DQT ? 256 : 320);
   static constexpr uint32_t COL_DK = SPLITD ? 256 : 384;
-  static_assert(COL_DK + DH <= 512 && COL_DQ + (DQT ? BM : D) <= COL_DV, "TMEM columns");
+  static_assert(COL_DK + DH <= 512 && COL_DQ + (DQT ? BM : D) <= COL_DV &&
+                    (COL_K >= COL_DK + DH || COL_K + D / 2 <= COL_S), "TMEM columns");
 };
 
 enum BwdBar {
