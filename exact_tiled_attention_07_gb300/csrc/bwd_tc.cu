@@ -1,4 +1,4 @@
-// Tensor-core backward for bf16/fp16, head dims 64/128 (sm_103a: TMA, tcgen05, TMEM).
+// Tensor-core backward for bf16/fp16, head dims 64/128/256 (sm_103a: TMA, tcgen05, TMEM).
 //
 // Recomputing backward ("Lecture 8 · GPU Performance & FlashAttention" §5.4; "FlashAttention
 // and GPU memory" §09): nothing N x N was stored, so every (key tile j, query tile i) pair
@@ -31,6 +31,8 @@
 // be drained:
 //   d = 64:  128 queries per step, dQ = dS K   (M = 128 queries, N = 64)
 //   d = 128:  64 queries per step, dQ^T = K^T dS^T (M = 128 = d, N = 64 queries)
+//   d = 256:  32 queries per step, one half of d per work item: dQ^T of that half
+//             (M = 128, N = 32 queries), dK, dV of that half; S^T, dP^T over all of d
 //
 // Issue order per step i (one thread): dP_i, dV_i, S_{i+1}, dK_i, dQ_i, so the softmax-side
 // work on step i+1's scores overlaps the tensor core's dK_i and dQ_i.
