@@ -1,4 +1,5 @@
-"""The five workloads at full size, in the launch configuration bench.py times.
+"""The five workloads at full size, in the launch configuration bench.py times (and the
+backward of the head-dimension-256 shape, which that workload does not time).
 
 The GPU runs each whole problem; the oracle checks what it can compute exactly one by
 one: every row of a few whole heads, a random sample of query rows (O, L, dQ) over all
@@ -188,3 +189,28 @@ def test_head_dim_256_forward_bf16(fa):
     x, host = _run_full(fa, w)
     _check_properties(w, x, host)
     _check_sampled_rows(w, x, host, _sample(w, 512, 51), with_bwd=False)
+
+
+def test_head_dim_256_backward_full_size_sampled(fa):
+    # the head-dimension-256 shape (B 4, H 16, N 16384) with its backward on the tensor cores:
+    # query-side rows (O, L, dQ) sampled over all heads, key-side rows (dK, dV) of 16 keys in each
+    # of four heads (random keys plus tile edges), each head's exact statistics in a worker pool
+    w = WORKLOADS["hd256_bf16"].with_shape(fwd_only=False, seed=52)
+    x, host = _run_full(fa, w)
+    _check_sampled_rows(w, x, host, _sample(w, 96, 53), with_bwd=True)
+    rng = np.random.default_rng(54)
+    edges = np.array([0, 31, 32, 127, 128, w.N - 129, w.N - 1])
+    heads = [(0, 0), (1, 7), (2, 11), (3, 15)]
+    jobs, keys_of = [], {}
+    for b, h in heads:
+        rnd = rng.choice(np.setdiff1d(np.arange(w.N), edges), 16 - edges.size, replace=False)
+        keys = np.sort(np.concatenate([rnd, edges]))
+        keys_of[(b, h)] = keys
+        q, k, v, do = (_head64(w, x, nm, b, h)[None, None] for nm in ("q", "k", "v", "do"))
+        jobs.append((q, k, v, do, w.scale, w.causal, keys))
+    refs = oracle_pool_map(key_side_reference, jobs)
+    for (b, h), (dk_ref, dv_ref, l_ref) in zip(heads, refs):
+        kt = torch.as_tensor(keys_of[(b, h)], dtype=torch.long)
+        assert rel_rms(to_f64(host["dk"][b, h][kt]), dk_ref) <= TOL_GRAD_RELRMS, (b, h)
+        assert rel_rms(to_f64(host["dv"][b, h][kt]), dv_ref) <= TOL_GRAD_RELRMS, (b, h)
+        assert max_abs(to_f64(host["lse"][b, h]), l_ref) <= TOL_L_MAXABS, (b, h)
