@@ -57,6 +57,7 @@ def _run_host(fa, dev, w, chunk):
     (128, "fp16", False, 1, 8, 8, 257),
     (128, "bf16", True, 3, 4, 4, 384),
     (64, "fp32", True, 1, 2, 2, 130),  # the CUDA-core kernels
+    (64, "bf16", False, 4, 16, 16, 130),  # 64 key/value heads: eight automatic chunks of 8
 ])
 def test_host_pipeline_matches_device_path(fa, chunk, d, dtype, causal, b, h, hkv, n):
     w = Workload("host", b, h, n, d, dtype, causal, "normal", 9500 + d + n, Hkv=hkv)
